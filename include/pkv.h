@@ -1,0 +1,301 @@
+/*
+ * pkv.h -- C ABI of the paged KV cache library (libpkv.so).
+ *
+ * The library implements the data-parallel hot path of PagedAttention for one
+ * GPU (sm_103a):
+ *
+ *   pkv_paged_attention_decode  single-query decode attention that reads the
+ *                               KV cache through per-sequence block tables;
+ *   pkv_reshape_and_cache       the slot-mapped write of new tokens' K/V;
+ *   pkv_copy_blocks             the whole-block copy behind copy-on-write;
+ *   pkv_alloc_* / pkv_seq_* ... the host block manager that hands out blocks,
+ *                               counts references, forks and copies on write,
+ *                               and exports the block tables.
+ *
+ * Sources (cited by page title and section):
+ *   [P1] "Paged Attention: OS-Inspired Memory Management for KV Caches",
+ *        modernaiengineering.com, lesson 13.6;
+ *   [P2] "What is PagedAttention and how does it manage KV cache?", n4n.ai;
+ *   [P3] worksonmygpu.com, deep-dive post "PagedAttention (vLLM)".
+ *
+ * Conventions for every call:
+ *   - Every entry point returns an int status (pkv_status below).  A call that
+ *     fails leaves every host-side object exactly as it was.
+ *   - Device pointers are BORROWED: the caller owns and allocates all device
+ *     memory (KV pools, tables, outputs, workspace).  The library never
+ *     allocates device memory itself.
+ *   - Kernels are launched asynchronously on the caller's stream (NULL = the
+ *     legacy default stream).  Argument errors are detected on the host before
+ *     any launch.  Errors that depend on device data (a slot or table entry
+ *     outside the pool, a device wait that gave up) are written to the
+ *     caller's int32 device status word: the first error wins (0 -> code), the
+ *     word is never cleared by the library, and a NULL status pointer means
+ *     "do not report".  Kernels never trap: after a device error the affected
+ *     outputs are unspecified but the CUDA context stays usable.
+ *   - Cache layout (chosen here; [P2] "How PagedAttention works" only fixes
+ *     that tokens are contiguous inside a block): key_cache and value_cache
+ *     are separate fp16 tensors [num_blocks][num_kv_heads][block_size][head_dim],
+ *     row-major.  Token `off` of physical block `b`, KV head `h`, element `i`
+ *     sits at element ((b*num_kv_heads + h)*block_size + off)*head_dim + i.
+ *   - A slot names one token position of the pool: slot = b*block_size + off
+ *     ([P1] paged_vs_contiguous.py example: token 37 -> logical block 2,
+ *     offset 5).
+ *   - Base pointers of the caches, query, key, value and out must be 16-byte
+ *     aligned (torch allocations are 256-byte aligned).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,     /* bad pointer, size, shape or id (host check) */
+    PKV_ERR_OUT_OF_BLOCKS = 2,   /* block manager: free list cannot satisfy the call */
+    PKV_ERR_CUDA = 3,            /* a CUDA runtime call failed (launch, attribute) */
+    PKV_ERR_DEVICE_TIMEOUT = 4,  /* device: a bounded wait gave up (status word only) */
+    PKV_ERR_OUT_OF_RANGE = 5,    /* device: slot / table entry / context outside the pool or table */
+    PKV_ERR_NOT_FOUND = 6,       /* block manager: unknown or released sequence id */
+    PKV_ERR_UNSUPPORTED = 7      /* shape not compiled into this build (head_dim, block_size, group) */
+} pkv_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *pkv_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * pkv_paged_attention_decode
+ *
+ * [P1] "How PagedAttention works", step 4: each decode step walks the block
+ * table, loads each block's keys and values and computes attention exactly as
+ * if they were contiguous.  For every sequence s and query head h, with
+ * L = context_lens[s], kvh = h / (num_heads / num_kv_heads) (consecutive
+ * query-head groups share a KV head), and token t stored in physical block
+ * block_tables[s][t / block_size] at offset t % block_size:
+ *
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . K[t][kvh]) * V[t][kvh]
+ *
+ * computed in fp32 (online softmax, fp32 accumulation) and rounded to fp16 to
+ * nearest even.  L == 0 gives an all-zero row.  Entries of a table row past
+ * ceil(L / block_size) are never read (they may hold -1).
+ *
+ * Arguments (all device pointers unless noted):
+ *   out          fp16 [num_seqs][num_heads][head_dim]           (written)
+ *   query        fp16 [num_seqs][num_heads][head_dim]
+ *   key_cache    fp16 [num_blocks][num_kv_heads][block_size][head_dim]
+ *   value_cache  same shape as key_cache
+ *   block_tables int32 [num_seqs][max_blocks_per_seq], row-major
+ *   context_lens int32 [num_seqs]
+ *   scale        softmax scale (host value), usually 1/sqrt(head_dim)
+ *   num_ctas     persistent grid size; 0 = one full wave (SM count x CTAs
+ *                per SM).  Any value >= 1 gives the same result within
+ *                rounding; 1 makes every sequence a single pass.
+ *   workspace    device scratch of at least pkv_decode_workspace_size(...)
+ *                bytes for the same (num_seqs, num_heads, num_kv_heads,
+ *                head_dim, block_size, num_ctas); 256-byte aligned.  Contents
+ *                on entry do not matter; it must not be used by another call
+ *                that runs at the same time.
+ *   dev_status   int32 device status word (nullable), see conventions.
+ *   stream       CUDA stream.
+ *
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32, 64, 128};
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; 1 <= num_seqs <= 4096.
+ * A context longer than max_blocks_per_seq*block_size, or a table entry
+ * outside [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in dev_status; such a
+ * context is clamped to its table and such an entry reads block 0.
+ * Launches two kernels (decode, then merge) on `stream`.
+ */
+int pkv_paged_attention_decode(void *out, const void *query,
+                               const void *key_cache, const void *value_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               float scale, int num_ctas,
+                               void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, pkv_stream_t stream);
+
+/* Bytes of workspace pkv_paged_attention_decode needs (host call; queries the
+ * current device's SM count when num_ctas == 0).  Returns 0 for unsupported
+ * shapes. */
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                 int head_dim, int block_size, int num_ctas);
+
+/* The grid size num_ctas == 0 resolves to on the current device for this
+ * shape (host call), or 0 for unsupported shapes. */
+int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim,
+                            int block_size);
+
+/* ------------------------------------------------------------------------ */
+/* Cache writes                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * pkv_reshape_and_cache
+ *
+ * [P1] "How PagedAttention works", steps 2-3: a new token goes into the next
+ * slot of its sequence's last block.  For t in [0, num_tokens): if
+ * slot_mapping[t] >= 0, copy key[t][h][:] and value[t][h][:] (every KV head h)
+ * to slot slot_mapping[t] of key_cache / value_cache.  A negative slot is
+ * skipped.  Bit-exact copies.
+ *
+ *   key, value    fp16 [num_tokens][num_kv_heads][head_dim] (device)
+ *   key_cache, value_cache   pool, layout above (device, written)
+ *   slot_mapping  int64 [num_tokens] (device)
+ *   dev_status    a slot >= num_blocks*block_size sets PKV_ERR_OUT_OF_RANGE
+ *                 and that token is not written.
+ * head_dim must be a multiple of 8.  num_tokens == 0 launches nothing.
+ * Two tokens with the same slot race (the caller's block manager never
+ * produces that).
+ */
+int pkv_reshape_and_cache(const void *key, const void *value,
+                          void *key_cache, void *value_cache,
+                          const int64_t *slot_mapping, int num_tokens,
+                          int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, int32_t *dev_status,
+                          pkv_stream_t stream);
+
+/*
+ * pkv_copy_blocks
+ *
+ * [P1] "Memory sharing across requests": copy-on-write copies a shared block
+ * to a fresh block before the writer's token goes in.  For each pair
+ * (src, dst) = block_pairs[2*i], block_pairs[2*i+1], copy the block_bytes
+ * bytes of physical block src over block dst, in key_cache and in
+ * value_cache.  Bit-exact.  Must run before the pkv_reshape_and_cache that
+ * writes the copying sequence's token.
+ *
+ *   block_pairs  int64 [num_pairs][2] (device)
+ *   block_bytes  bytes of one physical block in one cache
+ *                (num_kv_heads*block_size*head_dim*2 for fp16); multiple of 16
+ *   dev_status   a pair outside [0, num_blocks) sets PKV_ERR_OUT_OF_RANGE and
+ *                is skipped.
+ * The destinations must be pairwise distinct and no destination may also be
+ * a source in the same call (pkv_validate_block_pairs checks this on a host
+ * copy).  num_pairs == 0 launches nothing.
+ */
+int pkv_copy_blocks(void *key_cache, void *value_cache,
+                    const int64_t *block_pairs, int num_pairs,
+                    size_t block_bytes, int num_blocks,
+                    int32_t *dev_status, pkv_stream_t stream);
+
+/* Host check of a pair list for pkv_copy_blocks: ids in range, destinations
+ * distinct, no destination also a source.  PKV_OK or PKV_ERR_INVALID_ARG. */
+int pkv_validate_block_pairs(const int64_t *host_pairs, int num_pairs,
+                             int num_blocks);
+
+/* ------------------------------------------------------------------------ */
+/* Block manager (host)                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * A pool of num_blocks physical blocks of block_size token slots each
+ * ([P1] "What PagedAttention is"; [P2] "How PagedAttention works": a global
+ * pool handed out block by block).
+ *
+ * Rules ([P1] "How PagedAttention works", "Memory sharing across requests",
+ * practice block manager and its exercises):
+ *   - The free list is FIFO: blocks are taken from the front and released
+ *     blocks are put at the back, in table order.  initial_free_order (host,
+ *     nullable) gives the starting order (a permutation of 0..num_blocks-1);
+ *     NULL means 0, 1, 2, ...
+ *   - Every block has a reference count (sequences using it) and a fill
+ *     (token slots written).
+ *   - Appending a token: if the sequence has no block or its last block is
+ *     full, a fresh block is taken; else if the last block is shared
+ *     (count > 1) it is copied on write: a fresh block takes the old block's
+ *     fill, the table points at it, the old block's count drops by one, and
+ *     the pair (old, new) is returned for pkv_copy_blocks.  Then the token
+ *     takes the next slot of the last block.
+ *   - Fork: the child's table is a copy of the parent's (partial last block
+ *     included); every block's count rises by one.  No device work.
+ *   - Release: every block's count drops by one; blocks reaching zero go back
+ *     to the free list.  No device work.
+ *   - Sequence ids are handed out 0, 1, 2, ... and never reused.
+ * An operation that needs more free blocks than there are returns
+ * PKV_ERR_OUT_OF_BLOCKS and changes nothing.  The object is not thread-safe.
+ */
+typedef struct pkv_alloc pkv_alloc_t;
+
+int pkv_alloc_create(int num_blocks, int block_size,
+                     const int32_t *initial_free_order, pkv_alloc_t **out);
+void pkv_alloc_destroy(pkv_alloc_t *a);
+
+int pkv_seq_new(pkv_alloc_t *a, int *seq_id);
+
+/* Append one token.  *slot_out = its slot; cow_pair_out = {src, dst} of a
+ * copy-on-write, or {-1, -1}.  cow_pair_out may be NULL only if the caller
+ * knows no copy can happen. */
+int pkv_append_token(pkv_alloc_t *a, int seq, int64_t *slot_out,
+                     int32_t cow_pair_out[2]);
+
+/* Append n tokens to one sequence, all or nothing.  slots_out [n] (nullable)
+ * receives their slots.  At most one copy-on-write can happen (the first
+ * token's); cow_pair_out [2] (nullable) receives it, *n_cow (nullable) is 0
+ * or 1. */
+int pkv_append_tokens(pkv_alloc_t *a, int seq, int n, int64_t *slots_out,
+                      int32_t *cow_pair_out, int *n_cow);
+
+/* One decode step's appends: one token to each of the n DISTINCT sequences
+ * seqs[0..n), in that order, all or nothing.  slots_out [n]; cow_pairs_out
+ * [n][2] receives the copy-on-write pairs in order, *n_cow their count. */
+int pkv_append_batch(pkv_alloc_t *a, const int32_t *seqs, int n,
+                     int64_t *slots_out, int32_t *cow_pairs_out, int *n_cow);
+
+int pkv_fork(pkv_alloc_t *a, int parent, int *child);
+
+/* Release a sequence; *n_freed (nullable) = blocks returned to the free list. */
+int pkv_release(pkv_alloc_t *a, int seq, int *n_freed);
+
+/* Block tables and context lengths of n sequences, for the decode call.
+ * tables [n][max_blocks_per_seq] row-major, padded with -1; ctx_lens [n]
+ * (nullable).  A table longer than max_blocks_per_seq is an
+ * PKV_ERR_INVALID_ARG (nothing written). */
+int pkv_export_tables(const pkv_alloc_t *a, const int32_t *seqs, int n,
+                      int32_t *tables, int max_blocks_per_seq,
+                      int32_t *ctx_lens);
+
+int pkv_seq_length(const pkv_alloc_t *a, int seq, int *num_tokens);
+int pkv_seq_num_blocks(const pkv_alloc_t *a, int seq, int *num_blocks);
+int pkv_seq_table(const pkv_alloc_t *a, int seq, int32_t *table, int cap,
+                  int *num_blocks);
+int pkv_block_refcount(const pkv_alloc_t *a, int block, int *refs);
+int pkv_block_fill(const pkv_alloc_t *a, int block, int *fill);
+int pkv_num_free(const pkv_alloc_t *a, int *num_free);
+/* The free list, front first: out [cap]; *n = its length. */
+int pkv_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n);
+
+/* ------------------------------------------------------------------------ */
+/* Self-test                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Launches one CTA that waits, with the same bounded mbarrier wait the decode
+ * kernel uses, on a barrier that nothing ever completes, giving up after
+ * limit_ns nanoseconds.  The kernel then writes PKV_ERR_DEVICE_TIMEOUT to
+ * dev_status and returns normally.  Lets a test check the give-up path
+ * without a hang.  limit_ns must be in [1e3, 1e9].
+ */
+int pkv_selftest_wait_timeout(int32_t *dev_status, uint64_t limit_ns,
+                              pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,343 @@
+"""Python binding of libpkv.so, the paged KV cache library for GB300 (sm_103a).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels or its C++ block manager.  Functions take torch tensors (device
+memory and streams are torch's) and pass raw pointers, sizes and the current
+CUDA stream to the C ABI declared in include/pkv.h.  If the shared library is
+missing or fails to load, every call raises -- there is no fallback.
+
+Names mirror the C ABI without its ``pkv_`` prefix:
+
+* paged_attention_decode(out, query, key_cache, value_cache, block_tables,
+  context_lens, scale, ...)
+* reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, ...)
+* copy_blocks(key_cache, value_cache, block_pairs, ...)
+* BlockAllocator: pkv_alloc_* / pkv_seq_* / pkv_append_* / pkv_fork /
+  pkv_release / pkv_export_tables.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_INVALID_ARG = 1
+PKV_ERR_OUT_OF_BLOCKS = 2
+PKV_ERR_CUDA = 3
+PKV_ERR_DEVICE_TIMEOUT = 4
+PKV_ERR_OUT_OF_RANGE = 5
+PKV_ERR_NOT_FOUND = 6
+PKV_ERR_UNSUPPORTED = 7
+
+# Every symbol include/pkv.h declares, with (restype, argtypes).
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_intp = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [_c_int]),
+    "pkv_version": (_c_int, []),
+    "pkv_paged_attention_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
+                                            _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size,
+                                            _vp, _vp]),
+    "pkv_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pkv_decode_default_ctas": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
+    "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _vp, _vp]),
+    "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_size, _c_int, _vp, _vp]),
+    "pkv_validate_block_pairs": (_c_int, [_i64p, _c_int, _c_int]),
+    "pkv_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),
+    "pkv_alloc_destroy": (None, [_vp]),
+    "pkv_seq_new": (_c_int, [_vp, _intp]),
+    "pkv_append_token": (_c_int, [_vp, _c_int, _i64p, _i32p]),
+    "pkv_append_tokens": (_c_int, [_vp, _c_int, _c_int, _i64p, _i32p, _intp]),
+    "pkv_append_batch": (_c_int, [_vp, _i32p, _c_int, _i64p, _i32p, _intp]),
+    "pkv_fork": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_release": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_export_tables": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _i32p]),
+    "pkv_seq_length": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_seq_num_blocks": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_seq_table": (_c_int, [_vp, _c_int, _i32p, _c_int, _intp]),
+    "pkv_block_refcount": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_block_fill": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_num_free": (_c_int, [_vp, _intp]),
+    "pkv_free_list": (_c_int, [_vp, _i32p, _c_int, _intp]),
+    "pkv_selftest_wait_timeout": (_c_int, [_vp, ctypes.c_uint64, _vp]),
+}
+
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class OutOfBlocks(PkvError):
+    pass
+
+
+def load(path=LIB_PATH):
+    """Load libpkv.so (once) and attach the C signatures.  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run paged_kv_cache_152_gb300.build.build() "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().pkv_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status == PKV_ERR_OUT_OF_BLOCKS:
+        raise OutOfBlocks(status, what)
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# device calls
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None, device=True):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device and t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {tuple(t.shape)}")
+    return torch
+
+
+def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0):
+    return int(load().pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                num_ctas))
+
+
+def decode_default_ctas(num_heads, num_kv_heads, head_dim, block_size):
+    return int(load().pkv_decode_default_ctas(num_heads, num_kv_heads, head_dim, block_size))
+
+
+def new_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0, device="cuda"):
+    """A device workspace of the size pkv_decode_workspace_size asks for."""
+    import torch
+    n = decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas)
+    if n == 0:
+        raise PkvError(PKV_ERR_UNSUPPORTED, "decode_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens, scale,
+                           num_ctas=0, workspace=None, status=None, stream=None):
+    """pkv_paged_attention_decode on torch tensors (see include/pkv.h).
+
+    out, query: fp16 [N][H][D]; key_cache, value_cache: fp16 [NB][Hkv][bs][D];
+    block_tables: int32 [N][MB]; context_lens: int32 [N]; status: int32 [1]
+    device tensor or None.  A workspace is allocated (by torch) when None.
+    """
+    torch = _need(query, __import__("torch").float16, "query", 3)
+    _need(out, torch.float16, "out", 3)
+    _need(key_cache, torch.float16, "key_cache", 4)
+    _need(value_cache, torch.float16, "value_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    n, h, d = query.shape
+    nb, hkv, bs, d2 = key_cache.shape
+    if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
+            or block_tables.shape[0] != n or context_lens.shape[0] != n:
+        raise ValueError("inconsistent shapes")
+    if workspace is None:
+        workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+    rc = load().pkv_paged_attention_decode(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale), int(num_ctas),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode")
+    return out
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None, stream=None):
+    """pkv_reshape_and_cache: key/value fp16 [T][Hkv][D], slot_mapping int64 [T]."""
+    torch = _need(key, __import__("torch").float16, "key", 3)
+    _need(value, torch.float16, "value", 3)
+    _need(key_cache, torch.float16, "key_cache", 4)
+    _need(value_cache, torch.float16, "value_cache", 4)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    t, hkv, d = key.shape
+    nb, hkv2, bs, d2 = key_cache.shape
+    if hkv2 != hkv or d2 != d or tuple(value.shape) != tuple(key.shape) or slot_mapping.shape[0] != t:
+        raise ValueError("inconsistent shapes")
+    rc = load().pkv_reshape_and_cache(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                      _ptr(slot_mapping), t, hkv, d, bs, nb, _ptr(status), _stream(stream))
+    _check(rc, "pkv_reshape_and_cache")
+
+
+def copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None):
+    """pkv_copy_blocks: block_pairs int64 [n][2] (src, dst) on the device."""
+    torch = _need(key_cache, __import__("torch").float16, "key_cache", 4)
+    _need(value_cache, torch.float16, "value_cache", 4)
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    nb = key_cache.shape[0]
+    block_bytes = key_cache[0].numel() * key_cache.element_size()
+    rc = load().pkv_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_pairs), block_pairs.shape[0],
+                                block_bytes, nb, _ptr(status), _stream(stream))
+    _check(rc, "pkv_copy_blocks")
+
+
+def validate_block_pairs(pairs, num_blocks):
+    """Host check of (src, dst) pairs for copy_blocks; True if valid."""
+    a = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    return load().pkv_validate_block_pairs(a.ctypes.data_as(_i64p), a.shape[0], num_blocks) == PKV_OK
+
+
+def selftest_wait_timeout(status, limit_ns, stream=None):
+    rc = load().pkv_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream))
+    _check(rc, "pkv_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# host block manager
+
+class BlockAllocator:
+    """The C++ block manager (pkv_alloc_*).  Same method names as the rules
+    describe: new_seq, append_token, append_tokens, append_batch, fork,
+    release, export."""
+
+    def __init__(self, num_blocks, block_size, initial_free_order=None):
+        lib = load()
+        self._lib = lib
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        handle = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            self._order = np.ascontiguousarray(np.asarray(initial_free_order, dtype=np.int32))
+            if self._order.shape != (self.num_blocks,):
+                raise ValueError("initial_free_order must hold num_blocks entries")
+            order = self._order.ctypes.data_as(_i32p)
+        _check(lib.pkv_alloc_create(self.num_blocks, self.block_size, order, ctypes.byref(handle)),
+               "pkv_alloc_create")
+        self._h = handle
+        self._i = ctypes.c_int()
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_seq(self):
+        _check(self._lib.pkv_seq_new(self._h, ctypes.byref(self._i)), "pkv_seq_new")
+        return self._i.value
+
+    def append_token(self, seq):
+        """-> (slot, cow) with cow = (src, dst) or None."""
+        slot = ctypes.c_int64()
+        pair = (ctypes.c_int32 * 2)()
+        _check(self._lib.pkv_append_token(self._h, seq, ctypes.byref(slot), pair), "pkv_append_token")
+        return slot.value, ((pair[0], pair[1]) if pair[0] >= 0 else None)
+
+    def append_tokens(self, seq, n):
+        """-> (slots list, cows list); all or nothing."""
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pair = (ctypes.c_int32 * 2)()
+        ncow = ctypes.c_int()
+        _check(self._lib.pkv_append_tokens(self._h, seq, n, slots.ctypes.data_as(_i64p), pair,
+                                           ctypes.byref(ncow)), "pkv_append_tokens")
+        return slots[:n].tolist(), ([(pair[0], pair[1])] if ncow.value else [])
+
+    def append_batch(self, seqs, slots_out=None, pairs_out=None):
+        """One token for each distinct seq, in order.
+
+        -> (slots int64 array [n], cow pairs int32 array [k][2]).  Optional
+        preallocated outputs (e.g. pinned host tensors' numpy views) avoid
+        allocation in a serving loop.
+        """
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = s.shape[0]
+        slots = slots_out if slots_out is not None else np.empty(max(n, 1), dtype=np.int64)
+        pairs = pairs_out if pairs_out is not None else np.empty((max(n, 1), 2), dtype=np.int32)
+        ncow = ctypes.c_int()
+        _check(self._lib.pkv_append_batch(self._h, s.ctypes.data_as(_i32p), n, slots.ctypes.data_as(_i64p),
+                                          pairs.ctypes.data_as(_i32p), ctypes.byref(ncow)), "pkv_append_batch")
+        return slots[:n], pairs[:ncow.value]
+
+    def fork(self, parent):
+        _check(self._lib.pkv_fork(self._h, parent, ctypes.byref(self._i)), "pkv_fork")
+        return self._i.value
+
+    def release(self, seq):
+        """-> number of blocks returned to the free list."""
+        _check(self._lib.pkv_release(self._h, seq, ctypes.byref(self._i)), "pkv_release")
+        return self._i.value
+
+    def export(self, seqs, max_blocks_per_seq, tables_out=None, lens_out=None):
+        """-> (tables int32 [n][MB] padded with -1, context_lens int32 [n])."""
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = s.shape[0]
+        tables = tables_out if tables_out is not None else np.empty((n, max_blocks_per_seq), np.int32)
+        lens = lens_out if lens_out is not None else np.empty(n, np.int32)
+        _check(self._lib.pkv_export_tables(self._h, s.ctypes.data_as(_i32p), n, tables.ctypes.data_as(_i32p),
+                                           max_blocks_per_seq, lens.ctypes.data_as(_i32p)), "pkv_export_tables")
+        return tables, lens
+
+    def seq_len(self, seq):
+        _check(self._lib.pkv_seq_length(self._h, seq, ctypes.byref(self._i)), "pkv_seq_length")
+        return self._i.value
+
+    def table(self, seq):
+        _check(self._lib.pkv_seq_num_blocks(self._h, seq, ctypes.byref(self._i)), "pkv_seq_num_blocks")
+        n = self._i.value
+        out = np.empty(max(n, 1), np.int32)
+        _check(self._lib.pkv_seq_table(self._h, seq, out.ctypes.data_as(_i32p), n, None), "pkv_seq_table")
+        return out[:n].tolist()
+
+    def refcount(self, block):
+        _check(self._lib.pkv_block_refcount(self._h, block, ctypes.byref(self._i)), "pkv_block_refcount")
+        return self._i.value
+
+    def fill(self, block):
+        _check(self._lib.pkv_block_fill(self._h, block, ctypes.byref(self._i)), "pkv_block_fill")
+        return self._i.value
+
+    def num_free(self):
+        _check(self._lib.pkv_num_free(self._h, ctypes.byref(self._i)), "pkv_num_free")
+        return self._i.value
+
+    def free_list(self):
+        out = np.empty(max(self.num_blocks, 1), np.int32)
+        _check(self._lib.pkv_free_list(self._h, out.ctypes.data_as(_i32p), self.num_blocks,
+                                       ctypes.byref(self._i)), "pkv_free_list")
+        return out[:self._i.value].tolist()

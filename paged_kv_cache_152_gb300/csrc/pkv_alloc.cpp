@@ -1,0 +1,316 @@
+// pkv_alloc.cpp -- the host block manager that produces block tables.
+//
+// [P1] "Paged Attention: OS-Inspired Memory Management for KV Caches"
+// (modernaiengineering.com): "How PagedAttention works" (allocate on demand,
+// free on finish), "Memory sharing across requests" (reference counts,
+// copy-on-write of a shared partial block), the practice block manager and
+// its exercises (fork, release).  [P2] "What is PagedAttention..." (n4n.ai),
+// "How PagedAttention works": one global pool handed out block by block.
+//
+// Every operation first checks that it can complete (free blocks, ids,
+// buffer sizes) and only then mutates, so a failed call changes nothing.
+#include <cstdint>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+struct pkv_alloc {
+    int num_blocks = 0;
+    int block_size = 0;
+    std::deque<int32_t> free_list;  // FIFO: take from the front, return to the back
+    std::vector<int32_t> refs;      // sequences using each block
+    std::vector<int32_t> fill;      // token slots written in each block
+    struct Seq {
+        bool alive = false;
+        std::vector<int32_t> table;  // logical block -> physical block
+    };
+    std::vector<Seq> seqs;  // indexed by id; ids are never reused
+
+    Seq *find(int id) {
+        if (id < 0 || id >= (int)seqs.size() || !seqs[id].alive) return nullptr;
+        return &seqs[id];
+    }
+    const Seq *find(int id) const {
+        if (id < 0 || id >= (int)seqs.size() || !seqs[id].alive) return nullptr;
+        return &seqs[id];
+    }
+
+    int32_t take() {
+        const int32_t b = free_list.front();
+        free_list.pop_front();
+        refs[b] = 1;
+        fill[b] = 0;
+        return b;
+    }
+
+    int64_t length(const Seq &s) const {
+        if (s.table.empty()) return 0;
+        return (int64_t)(s.table.size() - 1) * block_size + fill[s.table.back()];
+    }
+
+    // Fresh blocks that appending n tokens to s takes: a copy-on-write of a
+    // shared, not yet full last block, plus new blocks for what overflows it.
+    int64_t blocks_needed(const Seq &s, int64_t n) const {
+        if (n <= 0) return 0;
+        int64_t need = 0, room = 0;
+        if (!s.table.empty()) {
+            const int32_t last = s.table.back();
+            room = block_size - fill[last];
+            if (room > 0 && refs[last] > 1) need += 1;
+        }
+        const int64_t overflow = n > room ? n - room : 0;
+        return need + (overflow + block_size - 1) / block_size;
+    }
+
+    // One token; the caller has checked that a block is available if needed.
+    int64_t append_one(Seq &s, int32_t *cow_src, int32_t *cow_dst) {
+        *cow_src = *cow_dst = -1;
+        if (s.table.empty() || fill[s.table.back()] == block_size) {
+            s.table.push_back(take());
+        } else if (refs[s.table.back()] > 1) {
+            const int32_t old = s.table.back();
+            const int32_t fresh = take();
+            fill[fresh] = fill[old];
+            refs[old] -= 1;
+            s.table.back() = fresh;
+            *cow_src = old;
+            *cow_dst = fresh;
+        }
+        const int32_t last = s.table.back();
+        const int64_t slot = (int64_t)last * block_size + fill[last];
+        fill[last] += 1;
+        return slot;
+    }
+};
+
+extern "C" int pkv_alloc_create(int num_blocks, int block_size, const int32_t *initial_free_order,
+                                pkv_alloc_t **out) {
+    if (!out || num_blocks <= 0 || block_size <= 0) return PKV_ERR_INVALID_ARG;
+    if ((int64_t)num_blocks * block_size > INT64_C(1) << 40) return PKV_ERR_INVALID_ARG;
+    if (initial_free_order) {
+        std::vector<char> seen(num_blocks, 0);
+        for (int i = 0; i < num_blocks; ++i) {
+            const int32_t b = initial_free_order[i];
+            if (b < 0 || b >= num_blocks || seen[b]) return PKV_ERR_INVALID_ARG;
+            seen[b] = 1;
+        }
+    }
+    pkv_alloc *a = new (std::nothrow) pkv_alloc;
+    if (!a) return PKV_ERR_INVALID_ARG;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->refs.assign(num_blocks, 0);
+    a->fill.assign(num_blocks, 0);
+    for (int i = 0; i < num_blocks; ++i) a->free_list.push_back(initial_free_order ? initial_free_order[i] : i);
+    *out = a;
+    return PKV_OK;
+}
+
+extern "C" void pkv_alloc_destroy(pkv_alloc_t *a) { delete a; }
+
+extern "C" int pkv_seq_new(pkv_alloc_t *a, int *seq_id) {
+    if (!a || !seq_id) return PKV_ERR_INVALID_ARG;
+    a->seqs.emplace_back();
+    a->seqs.back().alive = true;
+    *seq_id = (int)a->seqs.size() - 1;
+    return PKV_OK;
+}
+
+extern "C" int pkv_append_token(pkv_alloc_t *a, int seq, int64_t *slot_out, int32_t cow_pair_out[2]) {
+    if (!a || !slot_out) return PKV_ERR_INVALID_ARG;
+    pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    if (a->blocks_needed(*s, 1) > (int64_t)a->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
+    int32_t src, dst;
+    const bool shared_partial = !s->table.empty() && a->fill[s->table.back()] < a->block_size &&
+                                a->refs[s->table.back()] > 1;
+    if (shared_partial && !cow_pair_out) return PKV_ERR_INVALID_ARG;
+    *slot_out = a->append_one(*s, &src, &dst);
+    if (cow_pair_out) {
+        cow_pair_out[0] = src;
+        cow_pair_out[1] = dst;
+    }
+    return PKV_OK;
+}
+
+extern "C" int pkv_append_tokens(pkv_alloc_t *a, int seq, int n, int64_t *slots_out, int32_t *cow_pair_out,
+                                 int *n_cow) {
+    if (!a || n < 0) return PKV_ERR_INVALID_ARG;
+    pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    if (a->blocks_needed(*s, n) > (int64_t)a->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
+    int cows = 0;
+    if (cow_pair_out) cow_pair_out[0] = cow_pair_out[1] = -1;
+    for (int i = 0; i < n; ++i) {
+        int32_t src, dst;
+        const int64_t slot = a->append_one(*s, &src, &dst);
+        if (slots_out) slots_out[i] = slot;
+        if (src >= 0) {
+            ++cows;
+            if (cow_pair_out) {
+                cow_pair_out[0] = src;
+                cow_pair_out[1] = dst;
+            }
+        }
+    }
+    if (n_cow) *n_cow = cows;
+    return PKV_OK;
+}
+
+extern "C" int pkv_append_batch(pkv_alloc_t *a, const int32_t *seqs, int n, int64_t *slots_out,
+                                int32_t *cow_pairs_out, int *n_cow) {
+    if (!a || n < 0 || (n > 0 && (!seqs || !slots_out || !cow_pairs_out))) return PKV_ERR_INVALID_ARG;
+    // check ids, distinctness and the total number of fresh blocks first
+    std::vector<char> seen(a->seqs.size(), 0);
+    int64_t need = 0;
+    std::vector<int32_t> touched;  // blocks whose count this batch lowers (copy-on-write)
+    std::vector<int32_t> drop;     // ... and by how much, to simulate in order
+    for (int i = 0; i < n; ++i) {
+        const pkv_alloc::Seq *s = a->find(seqs[i]);
+        if (!s) return PKV_ERR_NOT_FOUND;
+        if (seen[seqs[i]]) return PKV_ERR_INVALID_ARG;
+        seen[seqs[i]] = 1;
+        if (s->table.empty() || a->fill[s->table.back()] == a->block_size) {
+            need += 1;
+            continue;
+        }
+        const int32_t last = s->table.back();
+        int32_t lowered = 0;
+        size_t k = 0;
+        for (; k < touched.size(); ++k)
+            if (touched[k] == last) break;
+        if (k < touched.size()) lowered = drop[k];
+        if (a->refs[last] - lowered > 1) {
+            need += 1;
+            if (k < touched.size()) {
+                drop[k] += 1;
+            } else {
+                touched.push_back(last);
+                drop.push_back(1);
+            }
+        }
+    }
+    if (need > (int64_t)a->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
+    int cows = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t src, dst;
+        slots_out[i] = a->append_one(*a->find(seqs[i]), &src, &dst);
+        if (src >= 0) {
+            cow_pairs_out[2 * cows] = src;
+            cow_pairs_out[2 * cows + 1] = dst;
+            ++cows;
+        }
+    }
+    if (n_cow) *n_cow = cows;
+    return PKV_OK;
+}
+
+extern "C" int pkv_fork(pkv_alloc_t *a, int parent, int *child) {
+    if (!a || !child) return PKV_ERR_INVALID_ARG;
+    if (!a->find(parent)) return PKV_ERR_NOT_FOUND;
+    a->seqs.emplace_back();
+    pkv_alloc::Seq &c = a->seqs.back();
+    const pkv_alloc::Seq &p = a->seqs[parent];  // after emplace_back: re-read
+    c.alive = true;
+    c.table = p.table;
+    for (int32_t b : c.table) a->refs[b] += 1;
+    *child = (int)a->seqs.size() - 1;
+    return PKV_OK;
+}
+
+extern "C" int pkv_release(pkv_alloc_t *a, int seq, int *n_freed) {
+    if (!a) return PKV_ERR_INVALID_ARG;
+    pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    int freed = 0;
+    for (int32_t b : s->table) {
+        a->refs[b] -= 1;
+        if (a->refs[b] == 0) {
+            a->fill[b] = 0;
+            a->free_list.push_back(b);
+            ++freed;
+        }
+    }
+    s->alive = false;
+    std::vector<int32_t>().swap(s->table);
+    if (n_freed) *n_freed = freed;
+    return PKV_OK;
+}
+
+extern "C" int pkv_export_tables(const pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *tables,
+                                 int max_blocks_per_seq, int32_t *ctx_lens) {
+    if (!a || n < 0 || max_blocks_per_seq < 0 || (n > 0 && (!seqs || !tables))) return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const pkv_alloc::Seq *s = a->find(seqs[i]);
+        if (!s) return PKV_ERR_NOT_FOUND;
+        if ((int64_t)s->table.size() > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
+        if (a->length(*s) > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < n; ++i) {
+        const pkv_alloc::Seq &s = *a->find(seqs[i]);
+        int32_t *row = tables + (int64_t)i * max_blocks_per_seq;
+        const size_t nb = s.table.size();
+        if (nb) std::memcpy(row, s.table.data(), nb * sizeof(int32_t));
+        for (int j = (int)nb; j < max_blocks_per_seq; ++j) row[j] = -1;
+        if (ctx_lens) ctx_lens[i] = (int32_t)a->length(s);
+    }
+    return PKV_OK;
+}
+
+extern "C" int pkv_seq_length(const pkv_alloc_t *a, int seq, int *num_tokens) {
+    if (!a || !num_tokens) return PKV_ERR_INVALID_ARG;
+    const pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    const int64_t len = a->length(*s);
+    if (len > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    *num_tokens = (int)len;
+    return PKV_OK;
+}
+
+extern "C" int pkv_seq_num_blocks(const pkv_alloc_t *a, int seq, int *num_blocks) {
+    if (!a || !num_blocks) return PKV_ERR_INVALID_ARG;
+    const pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    *num_blocks = (int)s->table.size();
+    return PKV_OK;
+}
+
+extern "C" int pkv_seq_table(const pkv_alloc_t *a, int seq, int32_t *table, int cap, int *num_blocks) {
+    if (!a || cap < 0 || (cap > 0 && !table)) return PKV_ERR_INVALID_ARG;
+    const pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    if ((int64_t)s->table.size() > cap) return PKV_ERR_INVALID_ARG;
+    if (!s->table.empty()) std::memcpy(table, s->table.data(), s->table.size() * sizeof(int32_t));
+    if (num_blocks) *num_blocks = (int)s->table.size();
+    return PKV_OK;
+}
+
+extern "C" int pkv_block_refcount(const pkv_alloc_t *a, int block, int *refs) {
+    if (!a || !refs || block < 0 || block >= a->num_blocks) return PKV_ERR_INVALID_ARG;
+    *refs = a->refs[block];
+    return PKV_OK;
+}
+
+extern "C" int pkv_block_fill(const pkv_alloc_t *a, int block, int *fill) {
+    if (!a || !fill || block < 0 || block >= a->num_blocks) return PKV_ERR_INVALID_ARG;
+    *fill = a->fill[block];
+    return PKV_OK;
+}
+
+extern "C" int pkv_num_free(const pkv_alloc_t *a, int *num_free) {
+    if (!a || !num_free) return PKV_ERR_INVALID_ARG;
+    *num_free = (int)a->free_list.size();
+    return PKV_OK;
+}
+
+extern "C" int pkv_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n) {
+    if (!a || cap < 0 || (cap > 0 && !out)) return PKV_ERR_INVALID_ARG;
+    if ((int64_t)a->free_list.size() > cap) return PKV_ERR_INVALID_ARG;
+    int i = 0;
+    for (int32_t b : a->free_list) out[i++] = b;
+    if (n) *n = i;
+    return PKV_OK;
+}

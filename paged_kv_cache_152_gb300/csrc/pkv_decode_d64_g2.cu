@@ -1,0 +1,4 @@
+// Decode kernels for head_dim 64, 2 query head(s) per KV head.
+#define PKV_D 64
+#define PKV_G 2
+#include "pkv_decode_inst.cuh"

@@ -1,0 +1,49 @@
+// pkv_decode_inst.cuh -- instantiates the decode kernel for one (head_dim,
+// group) pair and every supported block size.  Each pkv_decode_d*_g*.cu
+// includes it once, so the 8 instantiation sets compile in parallel.
+#include "pkv_decode_impl.cuh"
+
+#ifndef PKV_D
+#error "define PKV_D and PKV_G"
+#endif
+
+#define PKV_CAT2(a, b, c) a##b##_g##c
+#define PKV_CAT(a, b, c) PKV_CAT2(a, b, c)
+#define PKV_INFO_FN PKV_CAT(decode_kernel_info_d, PKV_D, PKV_G)
+
+namespace pkv {
+namespace {
+
+// Warps (workers) per CTA and ring stages per warp.  A stage holds one K
+// chunk, one V chunk (4 KB each at head_dim 128) and the group's query rows.
+constexpr int kWarps = 4;
+constexpr int kStages = (PKV_D == 64) ? 4 : 3;
+
+template <int BS>
+DecodeKernelInfo info_of() {
+    using Geo = DecodeGeometry<PKV_D, BS, PKV_G>;
+    using Smem = DecodeSmem<kWarps, kStages, Geo::kStageBytes>;
+    DecodeKernelInfo i;
+    i.fn = reinterpret_cast<const void *>(&paged_decode_kernel<PKV_D, BS, PKV_G, kWarps, kStages>);
+    i.threads = kWarps * 32;
+    i.warps = kWarps;
+    i.rows_per_chunk = Geo::kRows;
+    i.smem_fixed = Smem::kFixed;
+    i.smem_per_seq = Smem::kPerSeq;
+    return i;
+}
+
+}  // namespace
+
+bool PKV_INFO_FN(int block_size, DecodeKernelInfo *info) {
+    switch (block_size) {
+        case 8: *info = info_of<8>(); return true;
+        case 16: *info = info_of<16>(); return true;
+        case 32: *info = info_of<32>(); return true;
+        case 64: *info = info_of<64>(); return true;
+        case 128: *info = info_of<128>(); return true;
+        default: return false;
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,76 @@
+// pkv_decode_params.h -- kernel parameter blocks of the decode path.
+#ifndef PKV_DECODE_PARAMS_H
+#define PKV_DECODE_PARAMS_H
+
+#include <cuda_fp16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct DecodeParams {
+    __half *out;                  // [N][H][D]
+    const __half *query;          // [N][H][D]
+    const __half *key_cache;      // [NB][Hkv][BS][D]
+    const __half *value_cache;    // [NB][Hkv][BS][D]
+    const int32_t *block_tables;  // [N][MB]
+    const int32_t *context_lens;  // [N]
+    int *ws_cum;                  // [N+1] chunk prefix sums (written by CTA 0)
+    float *ws_ml;                 // [W][2][G][2] partial (max, sum)
+    float *ws_acc;                // [W][2][G][D] partial unnormalised outputs
+    int32_t *status;              // nullable
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int max_blocks_per_seq;
+    int num_blocks;
+    float scale_log2;             // scale * log2(e)
+    uint64_t wait_limit_ns;
+};
+
+struct MergeParams {
+    __half *out;
+    const int32_t *context_lens;
+    const int *ws_cum;
+    const float *ws_ml;
+    const float *ws_acc;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int group;
+    int rows_per_chunk;
+    int max_ctx;                  // max_blocks_per_seq * block_size
+    int64_t num_workers;
+};
+
+// Workspace carve-up (byte offsets), shared by the size query and the launch.
+struct DecodeWorkspace {
+    size_t cum, ml, acc, total;
+    static DecodeWorkspace plan(int num_seqs, int64_t workers, int group, int head_dim) {
+        auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+        DecodeWorkspace w;
+        w.cum = 0;
+        w.ml = up(4 * (size_t)(num_seqs + 1));
+        w.acc = w.ml + up(4 * (size_t)workers * 2 * group * 2);
+        w.total = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
+        return w;
+    }
+};
+
+// Host-side description of one compiled decode instantiation.
+struct DecodeKernelInfo {
+    const void *fn;        // __global__ function
+    int threads;           // threads per CTA
+    int warps;             // workers per CTA
+    int rows_per_chunk;
+    size_t smem_fixed;     // dynamic shared memory without the per-sequence arrays
+    size_t smem_per_seq;   // bytes per sequence (+ one extra int)
+};
+
+// Defined in pkv_decode_d{64,128}_g{1,2,4,8}.cu; false if not compiled.
+bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInfo *info);
+
+}  // namespace pkv
+
+#endif  // PKV_DECODE_PARAMS_H

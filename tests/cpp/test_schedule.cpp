@@ -1,0 +1,151 @@
+// Exhaustive CPU check of the decode kernel's work split (pkv_schedule.h).
+// Built and run by tests/test_native_host.py.  Exits non-zero on the first
+// violation, printing it.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+#include <random>
+#include <map>
+#include <set>
+
+#include "pkv_schedule.h"
+
+using namespace pkv;
+
+static int fails = 0;
+#define CHECK(c, ...) do { if (!(c)) { std::printf("FAIL %s:%d: ", __FILE__, __LINE__); \
+    std::printf(__VA_ARGS__); std::printf("\n"); if (++fails > 5) std::exit(1); } } while (0)
+
+static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W) {
+    const int n = (int)ctx.size();
+    std::vector<int> cum(n + 1, 0);
+    for (int s = 0; s < n; ++s) cum[s + 1] = cum[s] + hkv * chunks_for(ctx[s], sr);
+    const int64_t T = cum[n];
+    // brute-force owner of each chunk: (s, kvh, c)
+    std::vector<ChunkPos> truth;
+    for (int s = 0; s < n; ++s)
+        for (int h = 0; h < hkv; ++h)
+            for (int c = 0; c < chunks_for(ctx[s], sr); ++c)
+                truth.push_back({s, h, c, chunks_for(ctx[s], sr)});
+    CHECK((int64_t)truth.size() == T, "T");
+    if (T == 0) return;
+    // ranges partition [0, T)
+    std::vector<int> owner(T, -1);
+    for (int64_t w = 0; w < W; ++w) {
+        const int64_t st = worker_start(w, W, T), en = worker_start(w + 1, W, T);
+        CHECK(st <= en, "range order");
+        for (int64_t g = st; g < en; ++g) { CHECK(owner[g] == -1, "overlap"); owner[g] = (int)w; }
+    }
+    for (int64_t g = 0; g < T; ++g) {
+        CHECK(owner[g] >= 0, "uncovered chunk %lld", (long long)g);
+        CHECK(worker_of(g, W, T) == owner[g], "worker_of(%lld)=%lld want %d", (long long)g,
+              (long long)worker_of(g, W, T), owner[g]);
+        const ChunkPos p = locate_chunk(cum.data(), n, hkv, g);
+        CHECK(p.s == truth[g].s && p.kvh == truth[g].kvh && p.c == truth[g].c && p.nch == truth[g].nch,
+              "locate %lld", (long long)g);
+        // addressing stays inside the table row and the block
+        const int lb = chunk_block(p.c, bs, sr);
+        CHECK(lb >= 0 && lb < mb, "logical block %d outside table of %d", lb, mb);
+        const int rows = chunk_rows(p.c, ctx[p.s], sr);
+        CHECK(rows >= 1 && rows <= sr, "rows %d", rows);
+        const int row0 = (p.c * sr) % bs;
+        CHECK(row0 + rows <= bs, "chunk crosses block");
+        CHECK(p.c * sr + rows <= ctx[p.s], "chunk past context");
+        const int nb = 7;
+        for (int phys : {0, nb - 1}) {
+            const int64_t off = chunk_src_offset(phys, p.kvh, p.c, hkv, bs, sr, 64);
+            CHECK(off >= 0 && off + (int64_t)rows * 64 <= (int64_t)nb * hkv * bs * 64, "src offset");
+        }
+    }
+    // walk every worker as the kernel does; record pieces and partial slots
+    std::map<std::pair<int, int>, std::vector<std::pair<int64_t, int>>> partials;  // seg -> (worker, slot)
+    std::set<std::pair<int, int>> whole_done;
+    for (int64_t w = 0; w < W; ++w) {
+        const int64_t gb = worker_start(w, W, T), ge = worker_start(w + 1, W, T);
+        if (gb == ge) continue;
+        ChunkPos p = locate_chunk(cum.data(), n, hkv, gb);
+        bool in_piece = false;
+        int64_t piece_start = 0;
+        int slots_used[2] = {0, 0};
+        for (int64_t g = gb; g < ge; ++g) {
+            const ChunkPos q = locate_chunk(cum.data(), n, hkv, g);
+            CHECK(p.s == q.s && p.kvh == q.kvh && p.c == q.c && p.nch == q.nch, "walk at %lld", (long long)g);
+            const int f = chunk_flags(p, g, gb, ge);
+            const bool seg_start = (g == gb) || (locate_chunk(cum.data(), n, hkv, g - 1).s != p.s ||
+                                                 locate_chunk(cum.data(), n, hkv, g - 1).kvh != p.kvh);
+            CHECK(((f & kFirst) != 0) == seg_start, "first flag");
+            if (f & kFirst) { CHECK(!in_piece, "nested piece"); in_piece = true; piece_start = g; }
+            CHECK(in_piece, "chunk outside piece");
+            const bool seg_end = (g == ge - 1) || (locate_chunk(cum.data(), n, hkv, g + 1).s != p.s ||
+                                                   locate_chunk(cum.data(), n, hkv, g + 1).kvh != p.kvh);
+            CHECK(((f & kLast) != 0) == seg_end, "last flag");
+            if (f & kLast) {
+                const int64_t g0 = g - p.c, g1 = g0 + p.nch;
+                const bool whole = piece_start == g0 && g + 1 == g1;
+                CHECK(((f & kWhole) != 0) == whole, "whole flag");
+                const auto seg = std::make_pair(p.s, p.kvh);
+                if (whole) {
+                    CHECK(!whole_done.count(seg), "segment finished twice");
+                    whole_done.insert(seg);
+                } else {
+                    const int slot = (f & kSlot1) ? 1 : 0;
+                    CHECK(slot == (piece_start == gb ? 0 : 1), "slot rule");
+                    CHECK(slot == 0 || g == ge - 1, "slot 1 only for the last piece");
+                    CHECK(slots_used[slot] == 0, "slot %d used twice by worker %lld", slot, (long long)w);
+                    slots_used[slot] = 1;
+                    partials[seg].push_back({w, slot});
+                }
+                in_piece = false;
+            }
+            if (g + 1 < ge) next_chunk(p, cum.data(), n, hkv);
+        }
+        CHECK(!in_piece, "unterminated piece");
+    }
+    // the merge kernel finds exactly the stored partials of every cut segment
+    for (int s = 0; s < n; ++s) {
+        const int nch = chunks_for(ctx[s], sr);
+        for (int h = 0; h < hkv; ++h) {
+            const auto seg = std::make_pair(s, h);
+            if (nch == 0) { CHECK(!partials.count(seg) && !whole_done.count(seg), "empty seg touched"); continue; }
+            const int64_t g0 = cum[s] + (int64_t)h * nch, g1 = g0 + nch;
+            const int64_t wa = worker_of(g0, W, T), wb = worker_of(g1 - 1, W, T);
+            if (wa == wb) { CHECK(whole_done.count(seg) && !partials.count(seg), "uncut seg %d,%d", s, h); continue; }
+            CHECK(!whole_done.count(seg), "cut seg written whole");
+            std::vector<std::pair<int64_t, int>> found;
+            for (int64_t w = wa; w <= wb; ++w) {
+                const int64_t st = worker_start(w, W, T), en = worker_start(w + 1, W, T);
+                if (st == en) continue;
+                found.push_back({w, partial_slot(st, g0)});
+            }
+            CHECK(found == partials[seg], "merge pieces of seg %d,%d", s, h);
+        }
+    }
+}
+
+int main() {
+    std::mt19937_64 rng(152);
+    int cases = 0;
+    const int bss[] = {8, 16, 32, 64, 128};
+    for (int it = 0; it < 3000; ++it) {
+        const int bs = bss[rng() % 5];
+        const int row_bytes = (rng() % 2) ? 256 : 128;
+        const int sr = (bs * row_bytes <= 4096) ? bs : 4096 / row_bytes;
+        const int n = 1 + (int)(rng() % 40);
+        const int hkv = 1 + (int)(rng() % 4);
+        const int maxctx = 1 + (int)(rng() % 600);
+        const int mb = (maxctx + bs - 1) / bs;
+        std::vector<int> ctx(n);
+        for (auto &c : ctx) c = (rng() % 5 == 0) ? 0 : 1 + (int)(rng() % maxctx);
+        const int64_t W = 1 + (int64_t)(rng() % 300);
+        run_case(ctx, hkv, bs, sr, mb, W);
+        ++cases;
+    }
+    // hand-picked edge cases
+    run_case({0, 0, 0}, 2, 16, 16, 1, 4);
+    run_case({1}, 1, 16, 16, 1, 1000);
+    run_case({0, 5, 0, 0, 17, 0}, 3, 16, 16, 2, 3);
+    run_case({4096, 256, 1000}, 8, 32, 16, 128, 1216);
+    if (fails) { std::printf("%d failures\n", fails); return 1; }
+    std::printf("schedule ok: %d random cases\n", cases);
+    return 0;
+}

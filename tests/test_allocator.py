@@ -1,0 +1,185 @@
+"""The C++ block manager (libpkv) against the oracle model: bit-exact.
+
+Same operations on both; tables, context lengths, reference counts, fills,
+the free list (order included), slots and copy-on-write pairs must agree
+exactly, and failing operations must fail on both without changing state.
+"""
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle.block_manager import BlockManagerModel, OutOfBlocks
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_152_gb300 import build
+    build.build()
+    import paged_kv_cache_152_gb300 as m
+    return m
+
+
+def assert_same_state(model, alloc):
+    assert alloc.free_list() == list(model.free)
+    for b in range(model.num_blocks):
+        assert alloc.refcount(b) == model.refs[b], b
+        assert alloc.fill(b) == model.fill[b], b
+    for seq, table in model.tables.items():
+        assert alloc.table(seq) == table
+        assert alloc.seq_len(seq) == model.seq_len(seq)
+
+
+def test_practice_run(pkv, golden):
+    g = golden("practice_block_manager.json")
+    a = pkv.BlockAllocator(g["setup"]["pool"], g["setup"]["block_size"], g["setup"]["free_order"])
+    A = a.new_seq()
+    a.append_tokens(A, g["setup"]["prompt_tokens"])
+    B = a.fork(A)
+    assert a.table(A) == g["after_fork"]["A"] and a.table(B) == g["after_fork"]["B"]
+    slot, cow = a.append_token(A)
+    assert a.table(A) == g["after_A_writes"]["A"] and cow == (1, 2) and slot == 10
+    assert {str(b): a.refcount(b) for b in range(8) if a.refcount(b)} == g["after_A_writes"]["refs"]
+    slot, cow = a.append_token(B)
+    assert cow is None and slot == 6
+    assert {str(b): a.refcount(b) for b in range(8) if a.refcount(b)} == g["after_B_writes"]["refs"]
+
+
+def test_paged_vs_contiguous_table(pkv, golden):
+    g = golden("paged_vs_contiguous.json")
+    rng = np.random.default_rng(g["setup"]["numpy_seed"])
+    lengths = rng.integers(50, 900, size=8)
+    perm = rng.permutation(400)
+    a = pkv.BlockAllocator(400, 16, perm[::-1].copy())
+    s = a.new_seq()
+    slots, _ = a.append_tokens(s, int(lengths[0]))
+    assert a.table(s)[:6] == g["request0"]["table_head"] and len(a.table(s)) == g["request0"]["blocks"]
+    assert slots[37] == 308 * 16 + 5
+
+
+def test_lifecycle(pkv, golden):
+    g = golden("lifecycle.json")
+    order = g["free_blocks_in_order"] + [b for b in range(16) if b not in g["free_blocks_in_order"]]
+    a = pkv.BlockAllocator(16, 16, order)
+    s = a.new_seq()
+    a.append_tokens(s, 48)
+    assert a.table(s) == g["blocks_after_prompt"]
+    a.append_token(s)
+    assert a.table(s) == g["blocks_after_token_48"]
+    assert a.release(s) == 4 and a.num_free() == 16
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_operations_bit_exact(pkv, seed):
+    rng = np.random.default_rng(1000 + seed)
+    nb = int(rng.integers(4, 40))
+    bs = int(rng.choice([1, 2, 4, 16]))
+    order = rng.permutation(nb)
+    model = BlockManagerModel(nb, bs, order)
+    alloc = pkv.BlockAllocator(nb, bs, order)
+    live = []
+    for step in range(400):
+        op = rng.integers(0, 10)
+        if op == 0 or not live:
+            assert alloc.new_seq() == model.new_seq()
+            live.append(model.next_seq - 1)
+        elif op <= 4:
+            s = int(rng.choice(live))
+            n = int(rng.integers(1, 3 * bs + 2))
+            try:
+                expect = model.append_tokens(s, n)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    alloc.append_tokens(s, n)
+            else:
+                got = alloc.append_tokens(s, n)
+                assert got[0] == expect[0] and [tuple(c) for c in got[1]] == expect[1]
+        elif op == 5:
+            s = int(rng.choice(live))
+            try:
+                expect = model.append_token(s)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    alloc.append_token(s)
+            else:
+                assert alloc.append_token(s) == expect
+        elif op == 6:
+            batch = [int(x) for x in rng.permutation(live)[: int(rng.integers(1, len(live) + 1))]]
+            # the model applies the same rule one sequence at a time; a batch is
+            # all or nothing, so check the model's feasibility on a copy first
+            import copy
+            trial = copy.deepcopy(model)
+            try:
+                exp = [trial.append_token(s) for s in batch]
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    alloc.append_batch(batch)
+            else:
+                model = trial
+                slots, pairs = alloc.append_batch(batch)
+                assert slots.tolist() == [e[0] for e in exp]
+                assert [tuple(p) for p in pairs.tolist()] == [e[1] for e in exp if e[1] is not None]
+        elif op <= 8:
+            s = int(rng.choice(live))
+            assert alloc.fork(s) == model.fork(s)
+            live.append(model.next_seq - 1)
+        else:
+            s = int(rng.choice(live))
+            assert alloc.release(s) == len(model.release(s))
+            live.remove(s)
+        if step % 25 == 0:
+            assert_same_state(model, alloc)
+    assert_same_state(model, alloc)
+    tables, lens = alloc.export(live, 64)
+    mt, ml = model.export(live, 64)
+    assert tables.tolist() == mt and lens.tolist() == ml
+
+
+@pytest.mark.parametrize("name", W.NAMES)
+def test_workload_traces_bit_exact(pkv, name):
+    wl = W.make(name)
+    model = BlockManagerModel(wl.num_blocks, wl.block_size, wl.free_order)
+    alloc = pkv.BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+    r_model = W.replay(model, wl.ops)
+    r_alloc = W.replay(alloc, wl.ops)
+    for a, b in zip(r_alloc, r_model):
+        if isinstance(b, tuple):
+            assert list(a[0]) == b[0] and [tuple(c) for c in a[1]] == b[1]
+        elif isinstance(b, list):
+            assert a == len(b)          # release: count of freed blocks
+        else:
+            assert a == b
+    slots, pairs = alloc.append_batch(wl.batch)
+    exp = [model.append_token(s) for s in wl.batch]
+    assert slots.tolist() == [e[0] for e in exp]
+    mb = wl.max_blocks_per_seq()
+    tables, lens = alloc.export(wl.batch, mb)
+    mt, ml = model.export(wl.batch, mb)
+    assert tables.tolist() == mt and lens.tolist() == ml == wl.context_lens
+    assert alloc.free_list() == list(model.free)
+
+
+def test_errors_leave_state_unchanged(pkv):
+    a = pkv.BlockAllocator(4, 4)
+    s = a.new_seq()
+    a.append_tokens(s, 14)
+    before = (a.free_list(), a.table(s), a.seq_len(s))
+    with pytest.raises(pkv.OutOfBlocks):
+        a.append_tokens(s, 3)
+    t = a.fork(s)
+    with pytest.raises(pkv.OutOfBlocks):
+        a.append_batch([t, s])
+    assert (a.free_list(), a.table(s), a.seq_len(s)) == before
+    with pytest.raises(pkv.PkvError):
+        a.append_batch([s, s])          # duplicate sequence in one batch
+    with pytest.raises(pkv.PkvError):
+        a.release(99)
+    with pytest.raises(pkv.PkvError):
+        a.export([s], 3)                # table has 4 blocks
+    with pytest.raises(pkv.PkvError):
+        pkv.BlockAllocator(4, 4, [0, 1, 1, 2])
+    a.release(t)
+    a.release(s)
+    with pytest.raises(pkv.PkvError):
+        a.append_token(s)               # released
+    assert a.num_free() == 4
