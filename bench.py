@@ -1,0 +1,598 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+Prints ONE JSON line (rank 0).  Workload (default): 7B-class decode, one layer
+-- batch 64, 32 query heads = 32 KV heads, head_dim 128, fp16 cache in blocks
+of 16, context lengths uniform integers in [50, 900], pool 1.25x the blocks
+needed with tables assigned from a shuffled free list (workloads.decode_7b).
+
+One step = one pass of the whole device hot path over the batch:
+reshape_and_cache of the decode step's new token of every sequence, then
+paged decode attention (decode kernel + merge kernel).  The workload has no
+copy-on-write pair at its decode step, so copy_blocks launches nothing.
+
+* value: KV bytes the decode reads (2 * sum(ctx) * Hkv * D * 2) per step,
+  times K steps, over the device-timed K steps (CUDA events, barrier +
+  synchronize on both sides, max over ranks), inputs resident in HBM.
+  The KV read per step (0.57 GB) is larger than L2 (129 MB), so no L2 flush.
+* e2e: the same metric through the public API with host buffers: every step
+  the C++ block manager appends one token per sequence and exports the tables,
+  queries/new K,V/slots/tables/context lengths go host->device from pinned
+  memory, the two kernels run, the output comes back device->host.
+* roofline: decode launch (both kernels) timed alone with CUDA events on its
+  stream over the timed region; algorithmic bytes / mean duration vs the
+  measured HBM copy bandwidth.
+* cpu_baseline: the fp64 oracle on the host cores, on a bounded sample of the
+  same workload.
+* --impl reference: the oracle as the reference arm (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-read HBM GB/s (% of GB300 peak), seqs/s per layer"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_7b_traffic.txt")
+KERNEL_SOURCES = ["pkv_decode_impl.cuh", "pkv_decode_inst.cuh", "pkv_decode.cu", "pkv_device.cuh",
+                  "pkv_schedule.h", "pkv_decode_params.h"]
+
+WORKLOAD_TEXT = {
+    "7b": "7B-class decode, one layer: batch 64, 32 query heads = 32 KV heads, head_dim 128, fp16, "
+          "block_size 16, context uniform integers in [50, 900], pool 1.25x needed, shuffled free list",
+    "tiny": "tiny: 4 sequences, context 40/17/100/5, 8 heads, head_dim 64, block 16, pool 64",
+    "chat": "chat, one layer: batch 128, prompt U[100,2000] + generated U[50,500], 32 heads, head_dim 128, "
+            "block 16, arrival-order allocation with interleaved frees",
+    "gqa": "GQA long context, one layer: batch 256, 32 query / 8 KV heads, head_dim 128, block 32, "
+           "context log-uniform in [256, 4096], shuffled pool",
+    "prefix": "prefix sharing, one layer: 128 sequences sharing a 500-token prefix, suffix U[50,500], "
+              "32 heads, head_dim 128, block 16",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    p.add_argument("--config", choices=list(WORKLOAD_TEXT), default="7b")
+    p.add_argument("--num-ctas", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--identity-tables", action="store_true",
+                   help="same workload with each sequence's blocks contiguous and in order")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29512")
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value, device="cpu"):
+    """Max of a float over ranks (the timing rule: the slowest rank counts)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value, device="cpu"):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# environment facts
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_152_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source and this workload (else None)."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash() or kv.get("workload") != workload:
+            return None
+        return float(kv["dram_bytes_per_decode_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        from datetime import datetime
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.15 <= r[0] <= self.t1 + 0.15]
+        use = inside if inside else rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, flag in zip(names, r[3][1:5]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "whole run (timed region shorter than the sampling period)"}
+
+
+# ---------------------------------------------------------------------------
+# the product arm
+
+def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0):
+    """Allocator + device tensors of a workload at its decode step."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_152_gb300 as pkv
+    import workloads as W
+
+    wl = W.make(cfg)
+    n = wl.num_seqs
+    extra = n * (-(-e2e_headroom_steps // wl.block_size) + 1) if e2e_headroom_steps else 0
+    nb = wl.num_blocks + extra
+    if identity_tables:
+        order = np.arange(nb, dtype=np.int32)   # each sequence's blocks contiguous, in order
+    else:
+        order = np.concatenate([wl.free_order, np.arange(wl.num_blocks, nb, dtype=np.int32)])
+    alloc = pkv.BlockAllocator(nb, wl.block_size, order)
+    W.replay(alloc, wl.ops)
+    slots, pairs = alloc.append_batch(wl.batch)
+    mb = wl.max_blocks_per_seq() + (-(-e2e_headroom_steps // wl.block_size) + 1)
+    tables, lens = alloc.export(wl.batch, mb)
+    assert lens.tolist() == wl.context_lens
+    t = W.tensors(wl, device, with_pool=False)
+    shape = (nb, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    t["key_cache"] = W.normal_fp16_large(shape, wl.seed * 1000 + 4, device)
+    t["value_cache"] = W.normal_fp16_large(shape, wl.seed * 1000 + 5, device)
+    st = {
+        "wl": wl, "alloc": alloc, "mb": mb, "nb": nb, "t": t,
+        "slots": torch.from_numpy(slots.astype(np.int64)).to(device),
+        "pairs": torch.from_numpy(pairs.astype(np.int64)).reshape(-1, 2).to(device),
+        "tables": torch.from_numpy(tables).to(device),
+        "lens": torch.from_numpy(lens).to(device),
+        "out": torch.empty((n, wl.num_heads, wl.head_dim), dtype=torch.float16, device=device),
+        "status": torch.zeros(1, dtype=torch.int32, device=device),
+    }
+    return st
+
+
+def device_step(pkv, st, ws, num_ctas, ev=None):
+    """One pass of the hot path with inputs resident in HBM; returns launches."""
+    t = st["t"]
+    launches = 0
+    if st["pairs"].shape[0]:
+        pkv.copy_blocks(t["key_cache"], t["value_cache"], st["pairs"], status=st["status"])
+        launches += 1
+    pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"], st["slots"],
+                          status=st["status"])
+    launches += 1
+    if ev is not None:
+        ev[0].record()
+    pkv.paged_attention_decode(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"],
+                               st["lens"], st["wl"].scale, num_ctas=num_ctas, workspace=ws,
+                               status=st["status"])
+    if ev is not None:
+        ev[1].record()
+    return launches + 2
+
+
+def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
+    """Serving-loop steps through the public API with host buffers."""
+    import numpy as np
+    import torch
+    wl, alloc = st["wl"], st["alloc"]
+    n, h, hkv, d, mb = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, st["mb"]
+    pin = dict(pin_memory=True)
+    rng = np.random.default_rng(wl.seed + 77)
+    h_q = torch.from_numpy(rng.standard_normal((steps, n, h, d)).astype(np.float16))
+    h_k = torch.from_numpy(rng.standard_normal((steps, n, hkv, d)).astype(np.float16))
+    h_v = torch.from_numpy(rng.standard_normal((steps, n, hkv, d)).astype(np.float16))
+    h_q, h_k, h_v = h_q.pin_memory(), h_k.pin_memory(), h_v.pin_memory()
+    h_slots = torch.empty(n, dtype=torch.int64, **pin)
+    h_pairs = torch.empty((n, 2), dtype=torch.int32, **pin)
+    h_tables = torch.empty((n, mb), dtype=torch.int32, **pin)
+    h_lens = torch.empty(n, dtype=torch.int32, **pin)
+    h_out = torch.empty((n, h, d), dtype=torch.float16, **pin)
+    d_q = torch.empty((n, h, d), dtype=torch.float16, device=device)
+    d_k = torch.empty((n, hkv, d), dtype=torch.float16, device=device)
+    d_v = torch.empty_like(d_k)
+    d_slots = torch.empty(n, dtype=torch.int64, device=device)
+    d_pairs = torch.empty((n, 2), dtype=torch.int64, device=device)
+    d_tables = torch.empty((n, mb), dtype=torch.int32, device=device)
+    d_lens = torch.empty(n, dtype=torch.int32, device=device)
+    t = st["t"]
+    batch = np.asarray(wl.batch, dtype=np.int32)
+    bytes_total = 0
+    h2d = d2h = 0
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        slots, pairs = alloc.append_batch(batch, slots_out=h_slots.numpy(), pairs_out=h_pairs.numpy())
+        alloc.export(batch, mb, tables_out=h_tables.numpy(), lens_out=h_lens.numpy())
+        bytes_total += 2 * int(h_lens.numpy().sum()) * hkv * d * 2
+        d_q.copy_(h_q[i], non_blocking=True)
+        d_k.copy_(h_k[i], non_blocking=True)
+        d_v.copy_(h_v[i], non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_tables.copy_(h_tables, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        h2d += (h_q[i].numel() + h_k[i].numel() + h_v[i].numel()) * 2 + n * 8 + n * mb * 4 + n * 4
+        if len(pairs):
+            d_pairs[:len(pairs)].copy_(h_pairs[:len(pairs)], non_blocking=True)
+            h2d += len(pairs) * 8
+            pkv.copy_blocks(t["key_cache"], t["value_cache"], d_pairs[:len(pairs)], status=st["status"])
+        pkv.reshape_and_cache(d_k, d_v, t["key_cache"], t["value_cache"], d_slots, status=st["status"])
+        pkv.paged_attention_decode(st["out"], d_q, t["key_cache"], t["value_cache"], d_tables, d_lens,
+                                   wl.scale, num_ctas=num_ctas, workspace=ws, status=st["status"])
+        h_out.copy_(st["out"], non_blocking=True)
+        d2h += h_out.numel() * 2
+        torch.cuda.current_stream().synchronize()
+    elapsed = time.perf_counter() - t0
+    elapsed = max_over_ranks(dist, elapsed, device)
+    barrier(dist, device)
+    return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // steps, "d2h": d2h // steps}
+
+
+def run_pkv(args):
+    import torch
+    import paged_kv_cache_152_gb300 as pkv
+
+    rank, local_rank, world = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    from paged_kv_cache_152_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    barrier(dist, device)
+    pkv.load()
+
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+    st = build_state(args.config, device, args.identity_tables, e2e_headroom_steps=e2e_steps)
+    wl = st["wl"]
+    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                           args.num_ctas, device)
+    kv_bytes = wl.kv_read_bytes()
+    clocks = ClockSampler(local_rank)
+
+    # warm-up (untimed)
+    for _ in range(max(3, args.warmup)):
+        device_step(pkv, st, ws, args.num_ctas)
+    torch.cuda.synchronize()
+    assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
+
+    # timed region: K steps, device events, barrier + synchronize both sides
+    stream = torch.cuda.current_stream()
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    clocks.start()
+    e_start.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        launches += device_step(pkv, st, ws, args.num_ctas, dec_ev[i])
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(dist, device)
+    elapsed_ms = e_start.elapsed_time(e_stop)
+    dec_ms = [a.elapsed_time(b_) for a, b_ in dec_ev]
+    assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
+    ms_total = max_over_ranks(dist, elapsed_ms, device)
+    dec_mean = max_over_ranks(dist, statistics.fmean(dec_ms), device)
+
+    e2e = None
+    if e2e_steps:
+        e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist)
+    clock_info = clocks.finish()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peak, peak_kind = measured_hbm_peak()
+    value = world * kv_bytes * args.steps / (ms_total / 1e3) / 1e9
+    achieved = kv_bytes / (dec_mean / 1e3) / 1e9
+    traffic = recorded_traffic(args.config)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage_dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+                   "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": st["nb"],
+                   "sum_context": int(sum(wl.context_lens)), "kv_bytes_per_step": kv_bytes,
+                   "tables": "identity (contiguous, in order)" if args.identity_tables else "shuffled pool",
+                   "num_ctas": args.num_ctas or pkv.decode_default_ctas(wl.num_heads, wl.num_kv_heads,
+                                                                        wl.head_dim, wl.block_size),
+                   "l2": "no flush: the KV read per step (%.2f GB) is larger than L2 (129 MB)" % (kv_bytes / 1e9),
+                   "parallelism": f"replicas x{world} (independent pools and sequences, no collective)"},
+        "seqs_per_s_per_layer": round(world * wl.num_seqs * args.steps / (ms_total / 1e3), 1),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "gpu_launches": launches * world,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pkv_paged_attention_decode (paged_decode_kernel + paged_decode_merge_kernel)",
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "decode_ms_mean": round(dec_mean, 5),
+                     "decode_ms_median": round(statistics.median(dec_ms), 5)},
+        "clocks": clock_info,
+    }
+    if e2e is not None:
+        line["e2e"] = {"value": round(world * e2e["bytes"] / e2e["elapsed"] / 1e9, 2), "unit": UNIT,
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "steps": e2e_steps,
+                       "includes": "host block manager append + table export, H2D from pinned memory, "
+                                   "reshape_and_cache, decode, D2H of the output, stream sync per step"}
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+
+def _oracle_worker(cfg, seqs, barrier_, results):
+    """Spawned process: build the workload (untimed), wait for the others at
+    the barrier, run the oracle on `seqs`, report the elapsed seconds."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    import torch
+    torch.set_num_threads(1)
+    st = _oracle_state(cfg)
+    barrier_.wait()
+    t0 = time.perf_counter()
+    _oracle_decode(st, seqs)
+    results.put(time.perf_counter() - t0)
+
+
+_ORACLE_CACHE = {}
+
+
+def _oracle_state(cfg):
+    """The workload at its decode step, with the oracle's own tables (CPU)."""
+    if cfg in _ORACLE_CACHE:
+        return _ORACLE_CACHE[cfg]
+    import numpy as np
+    import workloads as W
+    from oracle.block_manager import BlockManagerModel
+    wl = W.make(cfg)
+    model = BlockManagerModel(wl.num_blocks, wl.block_size, wl.free_order)
+    W.replay(model, wl.ops)
+    slots = [model.append_token(s)[0] for s in wl.batch]
+    tables, lens = model.export(wl.batch, wl.max_blocks_per_seq())
+    t = W.tensors(wl, "cpu")
+    st = {"wl": wl, "tables": np.array(tables), "lens": np.array(lens), "slots": np.array(slots),
+          "q": t["query"].numpy(), "k": t["key"].numpy(), "v": t["value"].numpy(),
+          "kc": t["key_cache"].numpy(), "vc": t["value_cache"].numpy()}
+    _ORACLE_CACHE[cfg] = st
+    return st
+
+
+def _oracle_decode(st, seqs):
+    """One oracle pass over `seqs`: write their new tokens, then attend."""
+    from oracle import attention as OA
+    from oracle import cache_ops as OC
+    idx = list(seqs)
+    OC.reshape_and_cache(st["k"][idx], st["v"][idx], st["kc"], st["vc"], st["slots"][idx])
+    return OA.paged_decode_attention(st["q"], st["kc"], st["vc"], st["tables"], st["lens"], st["wl"].scale,
+                                     seqs=idx)
+
+
+def _seq_bytes(wl, seqs):
+    return sum(2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * 2 for s in seqs)
+
+
+def cpu_baseline(cfg, seconds):
+    """Oracle throughput on the host cores, on a bounded sample of the workload.
+
+    Single core: the first sequences of the batch, as many as fit in about
+    `seconds` / 2.  All cores: the whole batch split over a spawn pool of
+    os.cpu_count() processes (single-threaded BLAS each), timed once.
+    """
+    import multiprocessing as mp
+    st = _oracle_state(cfg)
+    wl = st["wl"]
+    t0 = time.perf_counter()
+    _oracle_decode(st, [0])
+    one = max(time.perf_counter() - t0, 1e-4)
+    k = int(max(1, min(wl.num_seqs, (seconds / 2) / one)))
+    seqs = list(range(k))
+    t0 = time.perf_counter()
+    _oracle_decode(st, seqs)
+    t1 = time.perf_counter() - t0
+    v1 = _seq_bytes(wl, seqs) / t1 / 1e9
+    cores = os.cpu_count() or 1
+    vn, cores_used = None, 1
+    if cores > 1:
+        chunks = [list(range(i, wl.num_seqs, cores)) for i in range(cores)]
+        chunks = [c for c in chunks if c]
+        ctx = mp.get_context("spawn")
+        bar = ctx.Barrier(len(chunks) + 1)
+        results = ctx.Queue()
+        procs = [ctx.Process(target=_oracle_worker, args=(cfg, c, bar, results)) for c in chunks]
+        for p in procs:
+            p.start()
+        bar.wait()
+        t0 = time.perf_counter()
+        for _ in procs:
+            results.get()
+        tn = time.perf_counter() - t0
+        for p in procs:
+            p.join()
+        vn = _seq_bytes(wl, range(wl.num_seqs)) / tn / 1e9
+        cores_used = len(chunks)
+    best = vn if vn is not None else v1
+    return {"value": round(best, 4), "unit": UNIT, "cores": cores_used if vn is not None else 1,
+            "kind": "oracle",
+            "sample": (f"all-cores: the whole {wl.num_seqs}-sequence batch split over {cores_used} spawned "
+                       f"processes (1 BLAS thread each); single core: first {k} sequences"),
+            "single_core_value": round(v1, 4),
+            "ms_per_step_all_cores": round(_seq_bytes(wl, range(wl.num_seqs)) / (best * 1e9) * 1e3, 2)}
+
+
+def run_reference(args):
+    """The reference arm: the oracle as it stands, rank 0 only."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    st = _oracle_state(args.config)
+    wl = st["wl"]
+    t0 = time.perf_counter()
+    _oracle_decode(st, [0])
+    one = max(time.perf_counter() - t0, 1e-4)
+    budget = 90.0 / max(1, args.steps + args.warmup)      # whole run in about 1.5 minutes
+    k = int(max(1, min(wl.num_seqs, budget / one)))
+    seqs = list(range(k))
+    for _ in range(args.warmup):
+        _oracle_decode(st, seqs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_decode(st, seqs)
+    el = time.perf_counter() - t0
+    value = _seq_bytes(wl, seqs) * args.steps / el / 1e9
+    sample = f"first {k} of {wl.num_seqs} sequences per step (all heads), 1 process"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "sample": sample},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_pkv(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
