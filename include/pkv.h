@@ -141,6 +141,53 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
 int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim,
                             int block_size);
 
+/*
+ * pkv_paged_attention_decode_noalloc
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory themselves.  Typical ones are a serving
+ * engine or framework that has already handed nearly all of the GPU's memory
+ * to its own KV pool and caching allocator (a separate cudaMalloc would fail,
+ * or fragment memory the engine budgets to the byte), a plug-in that the host
+ * application gives no allocation rights, and hot loops that cannot afford
+ * cudaMalloc/cudaFree, which may synchronise the whole device.
+ *
+ * It computes exactly what pkv_paged_attention_decode computes, with the same
+ * arguments minus workspace / workspace_bytes.  Its scratch is a fixed array
+ * of PKV_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB) that lives inside the library
+ * as a static device variable: every GPU that loads the library holds those
+ * 16 MiB until the process exits.  The call itself allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Limit: the scratch a call needs is pkv_decode_workspace_size(num_seqs,
+ * num_heads, num_kv_heads, head_dim, block_size, num_ctas); a call that needs
+ * more than PKV_DECODE_NOALLOC_SCRATCH_BYTES returns PKV_ERR_INVALID_ARG and
+ * launches nothing.  (At the default grid of one wave on 152 SMs this allows
+ * every supported shape; it bounds how large num_ctas may be.)
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture.  A failed look-up returns
+ * PKV_ERR_CUDA.
+ *
+ * Sharing: all calls in the process share the one array, and it keeps what
+ * the last call left in it; the kernels overwrite every scratch word they
+ * read, so nothing needs clearing between calls.  Two calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race on
+ * the array and give wrong results: serialise them, for example on one
+ * stream.  Other errors and the device status word behave as for
+ * pkv_paged_attention_decode.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int pkv_paged_attention_decode_noalloc(void *out, const void *query,
+                                       const void *key_cache, const void *value_cache,
+                                       const int32_t *block_tables, int max_blocks_per_seq,
+                                       const int32_t *context_lens,
+                                       int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks,
+                                       float scale, int num_ctas,
+                                       int32_t *dev_status, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache writes                                                              */
 /* ------------------------------------------------------------------------ */

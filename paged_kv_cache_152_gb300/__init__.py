@@ -45,6 +45,9 @@ SIGNATURES = {
                                             _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size,
                                             _vp, _vp]),
     "pkv_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int,
+                                                    _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _c_int,
+                                                    _vp, _vp]),
     "pkv_decode_default_ctas": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "pkv_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _vp, _vp]),
