@@ -9,8 +9,10 @@ needed with tables assigned from a shuffled free list (workloads.decode_7b).
 
 One step = one pass of the whole device hot path over the batch:
 reshape_and_cache of the decode step's new token of every sequence, then
-paged decode attention (decode kernel + merge kernel).  The workload has no
-copy-on-write pair at its decode step, so copy_blocks launches nothing.
+paged decode attention (one kernel; split pieces are merged inside it).  The
+workload has no copy-on-write pair at its decode step, so copy_blocks
+launches nothing.  By default the two launches are captured once as CUDA
+graphs and replayed every step (--no-graph: direct binding calls).
 
 * value: KV bytes the decode reads (2 * sum(ctx) * Hkv * D * 2) per step,
   times K steps, over the device-timed K steps (CUDA events, barrier +
@@ -73,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch every step directly instead of replaying captured CUDA graphs")
     p.add_argument("--identity-tables", action="store_true",
                    help="same workload with each sequence's blocks contiguous and in order")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -258,27 +262,36 @@ def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0):
         "out": torch.empty((n, wl.num_heads, wl.head_dim), dtype=torch.float16, device=device),
         "status": torch.zeros(1, dtype=torch.int32, device=device),
     }
+    # our kernels per step: copy_blocks (only with pairs), reshape_and_cache, decode
+    st["launches_per_step"] = (1 if len(pairs) else 0) + 2
     return st
+
+
+def write_step(pkv, st):
+    """copy_blocks (if the step has copy-on-write pairs), then reshape_and_cache."""
+    t = st["t"]
+    if st["pairs"].shape[0]:
+        pkv.copy_blocks(t["key_cache"], t["value_cache"], st["pairs"], status=st["status"])
+    pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"], st["slots"],
+                          status=st["status"])
+
+
+def decode_step(pkv, st, ws, num_ctas):
+    t = st["t"]
+    pkv.paged_attention_decode(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"],
+                               st["lens"], st["wl"].scale, num_ctas=num_ctas, workspace=ws,
+                               status=st["status"])
 
 
 def device_step(pkv, st, ws, num_ctas, ev=None):
     """One pass of the hot path with inputs resident in HBM; returns launches."""
-    t = st["t"]
-    launches = 0
-    if st["pairs"].shape[0]:
-        pkv.copy_blocks(t["key_cache"], t["value_cache"], st["pairs"], status=st["status"])
-        launches += 1
-    pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"], st["slots"],
-                          status=st["status"])
-    launches += 1
+    write_step(pkv, st)
     if ev is not None:
         ev[0].record()
-    pkv.paged_attention_decode(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"],
-                               st["lens"], st["wl"].scale, num_ctas=num_ctas, workspace=ws,
-                               status=st["status"])
+    decode_step(pkv, st, ws, num_ctas)
     if ev is not None:
         ev[1].record()
-    return launches + 2
+    return st["launches_per_step"]
 
 
 def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
@@ -367,19 +380,43 @@ def run_pkv(args):
     torch.cuda.synchronize()
     assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
 
-    # timed region: K steps, device events, barrier + synchronize both sides
+    # the step as two CUDA graphs (cache write, decode): one graph launch each
+    # per step instead of the Python binding's per-call host work
     stream = torch.cuda.current_stream()
+    graphs = None
+    if not args.no_graph:
+        g_write, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_write, capture_error_mode="relaxed"):
+            write_step(pkv, st)
+        with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
+            decode_step(pkv, st, ws, args.num_ctas)
+        graphs = (g_write, g_dec)
+        for _ in range(3):
+            g_write.replay()
+            g_dec.replay()
+        torch.cuda.synchronize()
+
+    # timed region: K steps, device events, barrier + synchronize both sides
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize()
     clocks.start()
+    h0 = time.perf_counter()
     e_start.record(stream)
     launches = 0
     for i in range(args.steps):
-        launches += device_step(pkv, st, ws, args.num_ctas, dec_ev[i])
+        if graphs is None:
+            launches += device_step(pkv, st, ws, args.num_ctas, dec_ev[i])
+        else:
+            graphs[0].replay()
+            dec_ev[i][0].record(stream)
+            graphs[1].replay()
+            dec_ev[i][1].record(stream)
+            launches += st["launches_per_step"]
     e_stop.record(stream)
+    host_s = time.perf_counter() - h0
     torch.cuda.synchronize()
     clocks.stop()
     barrier(dist, device)
@@ -429,9 +466,12 @@ def run_pkv(args):
         "seqs_per_s_per_layer": round(world * wl.num_seqs * args.steps / (ms_total / 1e3), 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches * world,
+        "launch_mode": "direct binding calls" if args.no_graph else
+                       "CUDA graphs (cache write graph + decode graph replayed per step)",
+        "host_us_per_step": round(host_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pkv_paged_attention_decode (paged_decode_kernel + paged_decode_merge_kernel)",
+                     "kernel": "pkv_paged_attention_decode (paged_decode_kernel, merge fused)",
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "decode_ms_mean": round(dec_mean, 5),

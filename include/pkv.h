@@ -108,8 +108,13 @@ int pkv_version(void);
  *   workspace    device scratch of at least pkv_decode_workspace_size(...)
  *                bytes for the same (num_seqs, num_heads, num_kv_heads,
  *                head_dim, block_size, num_ctas); 256-byte aligned.  Contents
- *                on entry do not matter; it must not be used by another call
- *                that runs at the same time.
+ *                on entry do not matter: its per-segment counters carry a tag
+ *                unique to each call and are left at zero by a successful
+ *                call, so a launch recorded once and replayed (a CUDA graph)
+ *                also works, except right after a replay that reported
+ *                PKV_ERR_DEVICE_TIMEOUT (zero the workspace before replaying
+ *                again).  It must not be used by another call that runs at
+ *                the same time.
  *   dev_status   int32 device status word (nullable), see conventions.
  *   stream       CUDA stream.
  *
@@ -118,7 +123,7 @@ int pkv_version(void);
  * A context longer than max_blocks_per_seq*block_size, or a table entry
  * outside [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in dev_status; such a
  * context is clamped to its table and such an entry reads block 0.
- * Launches two kernels (decode, then merge) on `stream`.
+ * Launches one kernel on `stream`.
  */
 int pkv_paged_attention_decode(void *out, const void *query,
                                const void *key_cache, const void *value_cache,
@@ -171,8 +176,10 @@ int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim,
  * PKV_ERR_CUDA.
  *
  * Sharing: all calls in the process share the one array, and it keeps what
- * the last call left in it; the kernels overwrite every scratch word they
- * read, so nothing needs clearing between calls.  Two calls whose kernels
+ * the last call left in it.  Nothing needs clearing between calls: partial
+ * results are rewritten before they are read, and the per-segment counters
+ * carry a tag unique to each call, so leftovers of an earlier call (even one
+ * that failed) are never taken for the current one.  Two calls whose kernels
  * overlap on the GPU (different streams, or different host threads) race on
  * the array and give wrong results: serialise them, for example on one
  * stream.  Other errors and the device status word behave as for

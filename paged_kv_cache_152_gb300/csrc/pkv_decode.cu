@@ -1,11 +1,13 @@
-// pkv_decode.cu -- host entry points of decode attention, and the merge kernel.
+// pkv_decode.cu -- host entry points of decode attention.
 //
 // pkv_paged_attention_decode validates its arguments on the host, picks the
 // compiled instantiation for (head_dim, group, block_size), sizes the
-// persistent grid (one full wave unless the caller fixes it) and launches the
-// decode kernel followed by the merge kernel on the caller's stream.
+// persistent grid (one full wave unless the caller fixes it), tags the call
+// with a fresh generation number and launches the decode kernel on the
+// caller's stream.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <math.h>
 #include <mutex>
 
@@ -38,51 +40,6 @@ bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInf
     PKV_CASE(128, 8)
 #undef PKV_CASE
     return false;
-}
-
-// M = max_p m_p;  out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M),
-// over the pieces of a cut segment in worker order.
-__global__ void __launch_bounds__(128) paged_decode_merge_kernel(const MergeParams p) {
-    const int seg = blockIdx.x;
-    const int s = seg / p.num_kv_heads;
-    const int kvh = seg - s * p.num_kv_heads;
-    const int G = p.group;
-    const int D = p.head_dim;
-    int c = p.context_lens[s];
-    c = c < 0 ? 0 : (c > p.max_ctx ? p.max_ctx : c);
-    const int nch = chunks_for(c, p.rows_per_chunk);
-    __half *out = p.out + ((int64_t)s * p.num_heads + kvh * G) * D;
-    if (nch == 0) {
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = __float2half_rn(0.f);
-        return;
-    }
-    const int64_t T = p.ws_cum[p.num_seqs];
-    const int64_t W = p.num_workers;
-    const int64_t g0 = p.ws_cum[s] + (int64_t)kvh * nch;
-    const int64_t wa = worker_of(g0, W, T);
-    const int64_t wb = worker_of(g0 + nch - 1, W, T);
-    if (wa == wb) return;  // finished by its only worker
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-        const int g = i / D;
-        const int e = i - g * D;
-        float M = -CUDART_INF_F;
-        for (int64_t w = wa; w <= wb; ++w) {
-            const int64_t st = worker_start(w, W, T);
-            if (st == worker_start(w + 1, W, T)) continue;
-            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
-            M = fmaxf(M, p.ws_ml[b * 2]);
-        }
-        float L = 0.f, O = 0.f;
-        for (int64_t w = wa; w <= wb; ++w) {
-            const int64_t st = worker_start(w, W, T);
-            if (st == worker_start(w + 1, W, T)) continue;
-            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
-            const float f = exp2f(p.ws_ml[b * 2] - M);
-            L = fmaf(p.ws_ml[b * 2 + 1], f, L);
-            O = fmaf(p.ws_acc[b * D + e], f, O);
-        }
-        out[(int64_t)g * D + e] = __float2half_rn(O / L);
-    }
 }
 
 namespace {
@@ -153,6 +110,14 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Distinct nonzero tag per call (wraps after 2^32 - 1 calls).
+uint32_t next_generation() {
+    static std::atomic<uint32_t> counter{0};
+    uint32_t g;
+    do { g = counter.fetch_add(1, std::memory_order_relaxed) + 1; } while (g == 0);
+    return g;
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -164,7 +129,7 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num
     if (!shape_supported(num_heads, num_kv_heads, head_dim, block_size)) return 0;
     Resolved r;
     if (resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r) != PKV_OK) return 0;
-    return DecodeWorkspace::plan(num_seqs, r.workers, num_heads / num_kv_heads, head_dim).total;
+    return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, num_heads / num_kv_heads, head_dim).total;
 }
 
 extern "C" int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim, int block_size) {
@@ -197,7 +162,7 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     int rc = resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r);
     if (rc != PKV_OK) return rc;
     const int group = num_heads / num_kv_heads;
-    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, r.workers, group, head_dim);
+    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, group, head_dim);
     if (workspace_bytes < ws.total) return PKV_ERR_INVALID_ARG;
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
@@ -208,9 +173,9 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.value_cache = static_cast<const __half *>(value_cache);
     p.block_tables = block_tables;
     p.context_lens = context_lens;
-    p.ws_cum = reinterpret_cast<int *>(wsb + ws.cum);
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml);
     p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc);
+    p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count);
     p.status = dev_status;
     p.num_seqs = num_seqs;
     p.num_heads = num_heads;
@@ -218,6 +183,7 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+    p.generation = next_generation();
     p.wait_limit_ns = kWaitLimitNs;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -227,25 +193,5 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
         return PKV_ERR_CUDA;
     }
 
-    MergeParams mp;
-    mp.out = p.out;
-    mp.context_lens = context_lens;
-    mp.ws_cum = p.ws_cum;
-    mp.ws_ml = p.ws_ml;
-    mp.ws_acc = p.ws_acc;
-    mp.num_seqs = num_seqs;
-    mp.num_heads = num_heads;
-    mp.num_kv_heads = num_kv_heads;
-    mp.head_dim = head_dim;
-    mp.group = group;
-    mp.rows_per_chunk = r.info.rows_per_chunk;
-    mp.max_ctx = max_blocks_per_seq * block_size;
-    mp.num_workers = r.workers;
-    void *margs[] = {&mp};
-    if (cudaLaunchKernel(reinterpret_cast<const void *>(&paged_decode_merge_kernel),
-                         dim3((unsigned)(num_seqs * num_kv_heads)), dim3(128), margs, 0, st) != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ERR_CUDA;
-    }
     return PKV_OK;
 }

@@ -28,9 +28,14 @@
 //    Scores are in log2 units (scale*log2(e) folded into q) and the softmax is
 //    online, per warp, in fp32.
 //  * A piece that covers a whole (sequence, KV head) is normalised and written
-//    as fp16 by the warp.  Cut pieces store (max, sum, unnormalised output) in
-//    the workspace; paged_decode_merge_kernel combines them in worker order
-//    (deterministic, no float atomics).
+//    as fp16 by the warp.  A cut piece stores (max, sum, unnormalised output)
+//    in the workspace and counts itself in on the segment's counter; the warp
+//    that brings the count to the number of pieces merges them, in worker
+//    order (deterministic, no float atomics, no second kernel).  Counters hold
+//    (call tag << 32 | count) and the merging warp zeroes its counter again:
+//    garbage in a fresh workspace, or a count left by a failed call, carries
+//    another call's tag and is ignored, and a replayed launch (same tag) finds
+//    every counter it uses back at zero.
 //  * Rows past the context are never used: the bulk copy of a ragged last
 //    chunk moves only its valid rows, masked scores become -inf, and V rows
 //    past the context are not loaded.
@@ -160,10 +165,67 @@ __device__ __forceinline__ void process_chunk(const unsigned char *sk, const uns
     }
 }
 
-// Finish a piece: fold the row groups of the warp together, then write the
-// output row (whole segment) or the partial (cut segment).
+// Counts one more piece of a segment in for this call; returns the count.
+__device__ __forceinline__ int count_piece(unsigned long long *cnt, uint32_t generation) {
+    unsigned long long cur = atomicAdd(cnt, 0ull);
+#pragma unroll 1
+    while (true) {
+        const unsigned long long want =
+            ((uint32_t)(cur >> 32) == generation) ? cur + 1 : (((unsigned long long)generation << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(cnt, cur, want);
+        if (prev == cur) return (int)(want & 0xffffffffull);
+        cur = prev;
+    }
+}
+
+// Where a worker warp is: what finish_piece needs besides the piece itself.
+struct WorkerCtx {
+    const int *cum;   // chunk prefix sums (shared memory)
+    int64_t W;        // workers in the grid
+    int64_t T;        // chunks in the batch
+    int64_t wid;      // this worker
+    int rows_per_chunk;
+};
+
+// One warp merges the pieces of a cut segment:
+// M = max_p m_p;  out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
 template <int D, int G>
-__device__ __forceinline__ void finish_piece(const DecodeParams &p, const int4 md, int64_t wid,
+__device__ __forceinline__ void merge_segment(const DecodeParams &p, int s, int kvh, int64_t g0, int64_t wa,
+                                           int64_t wb, int64_t W, int64_t T, int lane) {
+    constexpr int PER = D / 32;  // output elements per lane and head
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        float M = -CUDART_INF_F;
+        for (int64_t w = wa; w <= wb; ++w) {
+            const int64_t st = worker_start(w, W, T);
+            if (st == worker_start(w + 1, W, T)) continue;
+            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
+            M = fmaxf(M, __ldcg(p.ws_ml + b * 2));
+        }
+        float L = 0.f, O[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) O[k] = 0.f;
+        for (int64_t w = wa; w <= wb; ++w) {
+            const int64_t st = worker_start(w, W, T);
+            if (st == worker_start(w + 1, W, T)) continue;
+            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
+            const float f = exp2f(__ldcg(p.ws_ml + b * 2) - M);
+            L = fmaf(__ldcg(p.ws_ml + b * 2 + 1), f, L);
+            const float *src = p.ws_acc + b * D + lane * PER;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) O[k] = fmaf(__ldcg(src + k), f, O[k]);
+        }
+        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[k] / L);
+    }
+}
+
+// Finish a piece: fold the row groups of the warp together, then write the
+// output row (whole segment) or the partial (cut segment); the last piece of
+// a cut segment to arrive merges the segment.
+template <int D, int G>
+__device__ __forceinline__ void finish_piece(const DecodeParams &p, const WorkerCtx &wc, const int4 md,
                                              const float (&m)[G], float (&l)[G], float (&acc)[G][8],
                                              int lane) {
     constexpr int LPR = D / 8;
@@ -188,23 +250,42 @@ __device__ __forceinline__ void finish_piece(const DecodeParams &p, const int4 m
                 *reinterpret_cast<uint4 *>(dst) = pack8(o8);
             }
         }
-    } else {
-        const int64_t base = (wid * 2 + ((flags & kSlot1) ? 1 : 0)) * G;
-        if (lane < LPR) {
+        return;
+    }
+    const int64_t base = (wc.wid * 2 + ((flags & kSlot1) ? 1 : 0)) * G;
+    if (lane < LPR) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + (base + g) * D + lane * 8);
-                dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-                dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
-            }
+        for (int g = 0; g < G; ++g) {
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + (base + g) * D + lane * 8);
+            dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+            dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
         }
-        if (lane == 0) {
+    }
+    if (lane == 0) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                p.ws_ml[(base + g) * 2] = m[g];
-                p.ws_ml[(base + g) * 2 + 1] = l[g];
-            }
+        for (int g = 0; g < G; ++g) {
+            p.ws_ml[(base + g) * 2] = m[g];
+            p.ws_ml[(base + g) * 2 + 1] = l[g];
         }
+    }
+    // make the partial visible device-wide, then count it in
+    __threadfence();
+    __syncwarp();
+    const int nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
+    const int64_t g0 = wc.cum[s] + (int64_t)kvh * nch;
+    const int64_t wa = worker_of(g0, wc.W, wc.T);
+    const int64_t wb = worker_of(g0 + nch - 1, wc.W, wc.T);
+    int pieces = 0;
+    for (int64_t w = wa; w <= wb; ++w) pieces += worker_start(w, wc.W, wc.T) < worker_start(w + 1, wc.W, wc.T);
+    int arrived = 0;
+    if (lane == 0) arrived = count_piece(p.ws_count + (int64_t)s * p.num_kv_heads + kvh, p.generation);
+    arrived = __shfl_sync(kFullMask, arrived, 0);
+    if (arrived == pieces) {
+        __threadfence();
+        merge_segment<D, G>(p, s, kvh, g0, wa, wb, wc.W, wc.T, lane);
+        // every piece of this call has arrived: leave the counter at zero, so
+        // that a replay of the same launch (same tag) starts from a clean count
+        if (lane == 0) atomicExch(p.ws_count + (int64_t)s * p.num_kv_heads + kvh, 0ull);
     }
 }
 
@@ -274,8 +355,12 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         if (tid == 0) cum[N] = grand_total;
     }
     __syncthreads();
-    if (blockIdx.x == 0)
-        for (int i = tid; i <= N; i += NW * 32) p.ws_cum[i] = cum[i];
+    // rows of empty contexts are zero; no worker visits them
+    for (int s = blockIdx.x; s < N; s += gridDim.x) {
+        if (ctx[s] != 0) continue;
+        uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)s * p.num_heads * D);
+        for (int i = tid; i < p.num_heads * D / 8; i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
+    }
 
     // ---- this warp's share of the chunks -----------------------------------
     const int64_t T = cum[N];
@@ -285,6 +370,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     const int64_t ge = worker_start(wid + 1, W, T);
     if (gb >= ge) return;
     const int n = (int)(ge - gb);
+    const WorkerCtx wc{cum, W, T, wid, Geo::kRows};
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
@@ -381,7 +467,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
             }
         }
         process_chunk<D, BS, G>(sk, sk + Geo::kChunkBytes, md.z, q, m, l, acc, lane);
-        if (md.w & kLast) finish_piece<D, G>(p, md, wid, m, l, acc, lane);
+        if (md.w & kLast) finish_piece<D, G>(p, wc, md, m, l, acc, lane);
         __syncwarp();
         if (issued < n) {
             issue(issued);
@@ -390,10 +476,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         }
     }
 }
-
-// Combine the pieces of every cut (sequence, KV head) segment; zero the rows
-// of empty contexts.  One CTA per segment.
-__global__ void paged_decode_merge_kernel(const MergeParams p);
 
 }  // namespace pkv
 

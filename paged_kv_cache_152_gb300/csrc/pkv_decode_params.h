@@ -15,9 +15,9 @@ struct DecodeParams {
     const __half *value_cache;    // [NB][Hkv][BS][D]
     const int32_t *block_tables;  // [N][MB]
     const int32_t *context_lens;  // [N]
-    int *ws_cum;                  // [N+1] chunk prefix sums (written by CTA 0)
     float *ws_ml;                 // [W][2][G][2] partial (max, sum)
     float *ws_acc;                // [W][2][G][D] partial unnormalised outputs
+    unsigned long long *ws_count; // [N*Hkv] (call generation << 32 | pieces arrived)
     int32_t *status;              // nullable
     int num_seqs;
     int num_heads;
@@ -25,33 +25,18 @@ struct DecodeParams {
     int max_blocks_per_seq;
     int num_blocks;
     float scale_log2;             // scale * log2(e)
+    uint32_t generation;          // nonzero, distinct for every call
     uint64_t wait_limit_ns;
-};
-
-struct MergeParams {
-    __half *out;
-    const int32_t *context_lens;
-    const int *ws_cum;
-    const float *ws_ml;
-    const float *ws_acc;
-    int num_seqs;
-    int num_heads;
-    int num_kv_heads;
-    int head_dim;
-    int group;
-    int rows_per_chunk;
-    int max_ctx;                  // max_blocks_per_seq * block_size
-    int64_t num_workers;
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
 struct DecodeWorkspace {
-    size_t cum, ml, acc, total;
-    static DecodeWorkspace plan(int num_seqs, int64_t workers, int group, int head_dim) {
+    size_t count, ml, acc, total;
+    static DecodeWorkspace plan(int num_seqs, int num_kv_heads, int64_t workers, int group, int head_dim) {
         auto up = [](size_t x) { return (x + 255) / 256 * 256; };
         DecodeWorkspace w;
-        w.cum = 0;
-        w.ml = up(4 * (size_t)(num_seqs + 1));
+        w.count = 0;
+        w.ml = up(8 * (size_t)num_seqs * num_kv_heads);
         w.acc = w.ml + up(4 * (size_t)workers * 2 * group * 2);
         w.total = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
         return w;

@@ -18,8 +18,8 @@
 // PIECE.  A piece that is a whole segment is finished by the worker itself.
 // Otherwise the worker stores a partial (running max, sum, unnormalised
 // output) in slot 0 if the piece holds the worker's first chunk, else in slot
-// 1 (only the first and the last piece of a worker can be partial), and the
-// merge kernel combines the pieces of every cut segment.
+// 1 (only the first and the last piece of a worker can be partial); the
+// last piece of a cut segment to finish merges the segment's pieces.
 #ifndef PKV_SCHEDULE_H
 #define PKV_SCHEDULE_H
 

@@ -316,3 +316,26 @@ def test_bounded_wait_gives_up_and_context_survives(pkv):
     case.decode()
     torch.cuda.synchronize()
     assert int(case.status.item()) == 0 and torch.isfinite(case.out).all()
+
+
+def test_workspace_contents_do_not_matter(pkv):
+    """One workspace, pre-filled with garbage, reused by calls with different grids."""
+    case = Case(W.make("gqa", num_seqs=20))
+    case.write_new_tokens()
+    case.oracle_write_new_tokens()
+    ref = case.oracle_decode()
+    wl = case.wl
+    grids = [37, 37, 5, 200, 37, 1]
+    size = max(pkv.decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                                         wl.block_size, g) for g in grids)
+    ws = torch.full((size,), 0xFF, dtype=torch.uint8, device="cuda")
+    for i, g in enumerate(grids):
+        if i == 3:
+            ws.random_(0, 256)
+        out = torch.full_like(case.out, float("nan"))
+        pkv.paged_attention_decode(out, case.t["query"], case.t["key_cache"], case.t["value_cache"],
+                                   case.tables, case.lens, wl.scale, num_ctas=g, workspace=ws,
+                                   status=case.status)
+        torch.cuda.synchronize()
+        assert int(case.status.item()) == 0
+        assert max_abs_err(out, ref) <= TOL, (g, max_abs_err(out, ref))
