@@ -107,14 +107,14 @@ int pkv_version(void);
  *                rounding; 1 makes every sequence a single pass.
  *   workspace    device scratch of at least pkv_decode_workspace_size(...)
  *                bytes for the same (num_seqs, num_heads, num_kv_heads,
- *                head_dim, block_size, num_ctas); 256-byte aligned.  Contents
- *                on entry do not matter: its per-segment counters carry a tag
- *                unique to each call and are left at zero by a successful
- *                call, so a launch recorded once and replayed (a CUDA graph)
- *                also works, except right after a replay that reported
- *                PKV_ERR_DEVICE_TIMEOUT (zero the workspace before replaying
- *                again).  It must not be used by another call that runs at
- *                the same time.
+ *                head_dim, block_size, num_ctas); 256-byte aligned.  It
+ *                carries state from call to call (an epoch word that every
+ *                call advances, and completion counters that each call
+ *                prepares for the next), so keep one workspace per stream of
+ *                calls; what it holds on first use does not matter (zeroed
+ *                or not), nor does a call that gave up, and a launch recorded
+ *                once and replayed (a CUDA graph) works.  It must not be used
+ *                by another call that runs at the same time.
  *   dev_status   int32 device status word (nullable), see conventions.
  *   stream       CUDA stream.
  *
@@ -177,9 +177,10 @@ int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim,
  *
  * Sharing: all calls in the process share the one array, and it keeps what
  * the last call left in it.  Nothing needs clearing between calls: partial
- * results are rewritten before they are read, and the per-segment counters
- * carry a tag unique to each call, so leftovers of an earlier call (even one
- * that failed) are never taken for the current one.  Two calls whose kernels
+ * results are rewritten before they are read, and the completion counters
+ * are tagged with an epoch that every call advances, so leftovers of an
+ * earlier call (even one that failed) are never taken for the current one.
+ * Two calls whose kernels
  * overlap on the GPU (different streams, or different host threads) race on
  * the array and give wrong results: serialise them, for example on one
  * stream.  Other errors and the device status word behave as for

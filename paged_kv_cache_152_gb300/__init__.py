@@ -85,11 +85,16 @@ class OutOfBlocks(PkvError):
     pass
 
 
-def load(path=LIB_PATH):
-    """Load libpkv.so (once) and attach the C signatures.  Raises if missing."""
+def load(path=None):
+    """Load libpkv.so (once) and attach the C signatures.  Raises if missing.
+
+    The in-tree build is used unless PKV_LIBRARY names another build of the
+    same sources (tuning variants)."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = os.environ.get("PKV_LIBRARY", LIB_PATH)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is not built: run paged_kv_cache_152_gb300.build.build() "
                            "(there is no fallback implementation)")

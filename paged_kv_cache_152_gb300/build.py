@@ -54,35 +54,42 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile and link libpkv.so if any source changed; returns its path."""
+def build(force=False, verbose=False, ptxas_verbose=False, defines=(), lib_path=None):
+    """Compile and link libpkv.so if any source changed; returns its path.
+
+    defines (e.g. ["PKV_DECODE_WARPS=8"]) and lib_path build a variant into
+    another file (with its own object directory) for tuning experiments.
+    """
+    lib, obj_dir = LIB, OBJ
+    if lib_path is not None:
+        lib, obj_dir = os.path.abspath(lib_path), os.path.abspath(lib_path) + ".obj"
     cu, cpp, deps = _sources()
-    if not force and not _stale(deps):
-        return LIB
-    os.makedirs(OBJ, exist_ok=True)
+    if not force and lib_path is None and not _stale(deps):
+        return lib
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
-    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC]
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC] + [f"-D{d}" for d in defines]
     jobs = []
     for src in cu:
-        obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, "-lineinfo", *common, "-Xcompiler", "-fPIC", "-c", src, "-o", obj]
         if ptxas_verbose:
             cmd += ["-Xptxas", "-v"]
         jobs.append((cmd, obj))
     for src in cpp:
-        obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         jobs.append((["g++", *common, "-fPIC", "-Wall", "-c", src, "-o", obj], obj))
     workers = min(len(jobs), max(2, os.cpu_count() or 2))
     logs = []
     with cf.ThreadPoolExecutor(workers) as ex:
         for out in ex.map(lambda j: _run(j[0]), jobs):
             logs.append(out)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-Xcompiler", "-fPIC"])
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose or ptxas_verbose:
         sys.stdout.write("".join(logs))
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -2,12 +2,12 @@
 //
 // pkv_paged_attention_decode validates its arguments on the host, picks the
 // compiled instantiation for (head_dim, group, block_size), sizes the
-// persistent grid (one full wave unless the caller fixes it), tags the call
-// with a fresh generation number and launches the decode kernel on the
-// caller's stream.
+// persistent grid (one full wave unless the caller fixes it), encodes the
+// caches' tensor maps and launches the decode kernel on the caller's stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
-#include <atomic>
 #include <math.h>
 #include <mutex>
 
@@ -45,6 +45,7 @@ bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInf
 namespace {
 
 constexpr int kMaxSeqs = 4096;
+constexpr int kMaxCtas = 4096;
 
 struct Resolved {
     DecodeKernelInfo info;
@@ -82,7 +83,11 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
             Resolved *r) {
     if (!decode_kernel_info(head_dim, num_heads / num_kv_heads, block_size, &r->info))
         return PKV_ERR_UNSUPPORTED;
-    r->smem = r->info.smem_fixed + r->info.smem_per_seq * (size_t)num_seqs + 4;
+    // [cum (N+1)][ctx (N)] padded to 8 bytes, then [bounds (C+1)]
+    const size_t seq_bytes = ((r->info.smem_per_seq * (size_t)num_seqs + 4) + 7) & ~(size_t)7;
+    auto smem_for = [&](int ctas) { return r->info.smem_fixed + seq_bytes + r->info.smem_per_cta * (size_t)(ctas + 1); };
+    if (num_ctas > kMaxCtas) return PKV_ERR_INVALID_ARG;
+    r->smem = smem_for(num_ctas > 0 ? num_ctas : 1);
     int dev = 0, sms = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -90,19 +95,27 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
-    if (r->smem + 2 * 1024 > (size_t)optin) return PKV_ERR_INVALID_ARG;  // + static shared memory
-    const int rc = ensure_smem_attr(r->info.fn, r->smem);
-    if (rc != PKV_OK) return rc;
     if (num_ctas <= 0) {
+        // one full wave; the bounds array grows with the grid, so settle the
+        // grid and the shared memory together
+        size_t smem = smem_for(sms * 4);
+        if (smem + 2 * 1024 > (size_t)optin) smem = smem_for(sms);
+        if (smem + 2 * 1024 > (size_t)optin) return PKV_ERR_INVALID_ARG;
+        int rc0 = ensure_smem_attr(r->info.fn, smem);
+        if (rc0 != PKV_OK) return rc0;
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r->info.fn, r->info.threads, r->smem) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r->info.fn, r->info.threads, smem) !=
                 cudaSuccess ||
             per_sm < 1) {
             cudaGetLastError();
             return PKV_ERR_CUDA;
         }
-        num_ctas = sms * per_sm;
+        num_ctas = sms * (per_sm < 4 ? per_sm : 4);
+        r->smem = smem_for(num_ctas);
     }
+    if (r->smem + 2 * 1024 > (size_t)optin) return PKV_ERR_INVALID_ARG;  // + static shared memory
+    const int rc = ensure_smem_attr(r->info.fn, r->smem);
+    if (rc != PKV_OK) return rc;
     r->ctas = num_ctas;
     r->workers = (int64_t)num_ctas * r->info.warps;
     return PKV_OK;
@@ -110,12 +123,40 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Distinct nonzero tag per call (wraps after 2^32 - 1 calls).
-uint32_t next_generation() {
-    static std::atomic<uint32_t> counter{0};
-    uint32_t g;
-    do { g = counter.fetch_add(1, std::memory_order_relaxed) + 1; } while (g == 0);
-    return g;
+// cuTensorMapEncodeTiled from the driver (looked up once, no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// The cache as a 3-D tensor: 64 dims (innermost), num_blocks * Hkv *
+// block_size rows (stride head_dim * 2 bytes), head_dim / 64 halves (stride
+// 128 bytes), read with the 128-byte swizzle in boxes of {64, box_rows,
+// box_halves}: a box lands in shared memory as [half][row][64 dims].
+int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int block_size,
+                     int head_dim, int box_rows, int box_halves) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return PKV_ERR_CUDA;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)num_blocks * num_kv_heads * block_size,
+                                (cuuint64_t)(head_dim / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_halves};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(cache), dims, strides,
+                              box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -156,6 +197,7 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     if (!(scale > 0.f) || !isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
     if ((int64_t)max_blocks_per_seq * block_size > (1 << 30)) return PKV_ERR_INVALID_ARG;
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= (INT64_C(1) << 31)) return PKV_ERR_INVALID_ARG;
     if (!shape_supported(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
 
     Resolved r;
@@ -167,6 +209,20 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
     DecodeParams p;
+    {
+        const int chunk_rows = block_size < 16 ? block_size : 16;
+        const int halves = head_dim / 64;
+        rc = encode_cache_map(&p.tmap_k, key_cache, num_blocks, num_kv_heads, block_size, head_dim, chunk_rows,
+                              halves);
+        if (rc == PKV_OK)
+            rc = encode_cache_map(&p.tmap_v, value_cache, num_blocks, num_kv_heads, block_size, head_dim,
+                                  chunk_rows, halves);
+        if (rc == PKV_OK)
+            rc = encode_cache_map(&p.tmap_k8, key_cache, num_blocks, num_kv_heads, block_size, head_dim, 8, 1);
+        if (rc == PKV_OK)
+            rc = encode_cache_map(&p.tmap_v8, value_cache, num_blocks, num_kv_heads, block_size, head_dim, 8, 1);
+        if (rc != PKV_OK) return rc;
+    }
     p.out = static_cast<__half *>(out);
     p.query = static_cast<const __half *>(query);
     p.key_cache = static_cast<const __half *>(key_cache);
@@ -175,6 +231,7 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.context_lens = context_lens;
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml);
     p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc);
+    p.ws_sync = reinterpret_cast<unsigned long long *>(wsb + ws.sync);
     p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count);
     p.status = dev_status;
     p.num_seqs = num_seqs;
@@ -183,7 +240,6 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-    p.generation = next_generation();
     p.wait_limit_ns = kWaitLimitNs;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -9,36 +9,47 @@
 // "Common misconceptions": tokens are contiguous inside a block and the block
 // table lookup is fused into the attention kernel (no separate gather pass).
 //
-// Design (GB300, HBM-bound: each K/V byte is read exactly once):
-//  * The batch's work is cut into 4 KB chunks (pkv_schedule.h) and split into
-//    equal contiguous shares, one per WARP of a persistent grid.  Every warp
-//    is an independent worker; no CTA-wide synchronisation after the prologue.
+// Design (GB300, HBM-bound: each K/V byte is read once):
+//  * The batch's work is cut into chunks of up to 16 rows of one (sequence, KV
+//    head) (pkv_schedule.h) and split among the CTAs of a persistent grid,
+//    with CTA boundaries moved to segment boundaries where one is near, then
+//    into equal contiguous shares, one per WARP.  Every warp is an
+//    independent worker; there is no CTA-wide synchronisation after the
+//    prologue.  A worker walks the cut
+//    pieces at the two ends of its share first, so segments cut between
+//    workers are merged early, under the rest of the stream, not at the tail.
 //  * Each warp owns a ring of ST stages in shared memory.  Lane 0 issues, ST
-//    chunks ahead, one cp.async.bulk (TMA engine) per K chunk and per V chunk
-//    -- the chunk is one contiguous run of rows*head_dim fp16 in the
-//    [block][kv_head][slot][dim] layout -- plus the query rows of the KV group
-//    at the first chunk of each piece, all completing on the stage's
-//    mbarrier.  Block-table entries for the next 32 chunks are prefetched one
-//    per lane into registers, 32 chunks ahead of use.
-//  * Compute: a lane covers 8 consecutive head-dim elements of one row (16-B
-//    shared loads, conflict-free).  q.k partial sums are reduced with xor
-//    shuffles inside the D/8 lanes of a row; each lane then holds the full
-//    score of the rows it loads, so P.V needs no shuffle.  All G query heads
-//    of a KV group use each loaded K/V element (K/V read once per group).
-//    Scores are in log2 units (scale*log2(e) folded into q) and the softmax is
-//    online, per warp, in fp32.
+//    chunks ahead, one TMA tensor copy (cp.async.bulk.tensor.3d, 128-byte
+//    swizzle) per cache of the chunk's K and V rows -- the cache is viewed as
+//    [halves][rows][64 dims] so one box lands the whole 16-row chunk in the
+//    swizzled [half][row][128 B] tile; a short last chunk (<= 8 rows) takes
+//    one 8-row box per half; boxes never leave the chunk's block -- plus, at
+//    the first chunk of each piece, a bulk copy of the KV group's query rows,
+//    all completing on the stage's mbarrier.
+//    Block-table entries for the next 32 chunks are prefetched one per lane.
+//  * Math on the tensor cores, one warp per chunk: query heads on M (G of the
+//    16 rows used), rows of the chunk on N, head_dim on K:
+//        S^T[16 x rows] = Q[16 x D] . K^T       (mma.sync m16n8k16, fp32 acc)
+//        O[16 x D]     += P[16 x rows] . V       (P as fp16 hi + lo parts)
+//    K and V fragments come from the swizzled tiles through ldmatrix (.trans
+//    for V) without bank conflicts; the S accumulator layout is P's operand
+//    layout, so P never leaves registers.  Scores are in log2 units and the
+//    softmax is online, per warp, in fp32.  Products of fp16 inputs are exact
+//    in fp32, and splitting P into two fp16 terms keeps P.V at fp32 accuracy.
 //  * A piece that covers a whole (sequence, KV head) is normalised and written
 //    as fp16 by the warp.  A cut piece stores (max, sum, unnormalised output)
-//    in the workspace and counts itself in on the segment's counter; the warp
-//    that brings the count to the number of pieces merges them, in worker
-//    order (deterministic, no float atomics, no second kernel).  Counters hold
-//    (call tag << 32 | count) and the merging warp zeroes its counter again:
-//    garbage in a fresh workspace, or a count left by a failed call, carries
-//    another call's tag and is ignored, and a replayed launch (same tag) finds
-//    every counter it uses back at zero.
-//  * Rows past the context are never used: the bulk copy of a ragged last
-//    chunk moves only its valid rows, masked scores become -inf, and V rows
-//    past the context are not loaded.
+//    in the workspace and counts itself in on its segment's counter -- in
+//    shared memory when the segment stays inside the CTA, else in the
+//    workspace; the warp that brings a count to the number of pieces merges
+//    the segment, in worker
+//    order (deterministic, no float atomics, no second kernel).  Counters are
+//    tagged with an epoch kept in the workspace (see count_in_tagged): each
+//    call prepares the next call's counters and the last warp out advances
+//    the epoch, so counting in is one atomic, a fresh or half-used workspace
+//    is tolerated, and a launch captured once and replayed works.
+//  * Rows past the context never reach the output: their scores are masked to
+//    -inf, and in a ragged chunk the warp zeroes those V rows in shared memory
+//    before P.V (whatever the cache holds there, 0 * it stays 0).
 //  * Every mbarrier wait gives up after wait_limit_ns, reports
 //    PKV_ERR_DEVICE_TIMEOUT, waits (again bounded) for the warp's copies in
 //    flight and returns.
@@ -55,258 +66,348 @@ namespace pkv {
 
 template <int D, int BS, int G>
 struct DecodeGeometry {
-    static constexpr int kRowBytes = D * 2;
-    // rows per chunk: a whole block, or 4 KB of it when the block is larger
-    static constexpr int kRows = (BS * kRowBytes <= 4096) ? BS : 4096 / kRowBytes;
-    static constexpr int kChunkBytes = kRows * kRowBytes;
-    static constexpr int kQBytes = G * D * 2;
-    static constexpr int kQSlot = (kQBytes + 127) / 128 * 128;
-    static constexpr int kStageBytes = 2 * kChunkBytes + kQSlot;
-    static constexpr int kLanesPerRow = D / 8;
-    static constexpr int kRowsPerLoad = 32 / kLanesPerRow;
-    static constexpr int kLoads = kRows / kRowsPerLoad;               // 16-B loads per lane per chunk
-    static constexpr int kSub = (kLoads * G <= 32) ? kLoads : 32 / G; // loads per softmax sub-step
+    static constexpr int kRows = BS < 16 ? BS : 16;   // rows per chunk
+    static constexpr int kNT = kRows / 8;             // 8-row groups per chunk (mma N tiles)
+    static constexpr int kHalves = D / 64;            // 64-dim (128-byte) swizzle columns
+    static constexpr int kHalfBytes = kRows * 128;    // one column of a tile
+    static constexpr int kTileBytes = kHalves * kHalfBytes;  // K (or V) rows of a chunk
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBytes = G * D * 2;         // query rows of a KV group
+    static constexpr int kKSteps = D / 16;            // mma K steps of Q.K^T
+    static constexpr int kDTiles = D / 8;             // mma N tiles of P.V
+    static constexpr int kBoxBytes = 8 * 128;         // one TMA box: 8 rows x 64 fp16
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(kRows % kRowsPerLoad == 0, "rows per chunk");
-    static_assert(kLoads % kSub == 0, "sub-steps");
-    static_assert(BS % kRows == 0, "a chunk never crosses a block");
-    static_assert(kChunkBytes % 128 == 0, "stage alignment");
+    static_assert(BS % kRows == 0 && kRows % 8 == 0, "a chunk is whole 8-row boxes inside one block");
+    static_assert(G >= 1 && G <= 8, "query heads per KV head");
+    static_assert(kHalfBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
 };
 
-// Dynamic shared memory: [stages][barriers][chunk meta][cum (N+1)][ctx (N)].
-template <int NW, int ST, int STAGE>
+// Dynamic shared memory (from a 1024-byte aligned base):
+// [stages][query slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)].
+template <int NW, int ST, int D, int BS, int G>
 struct DecodeSmem {
-    static constexpr size_t kBars = (size_t)NW * ST * STAGE;
+    using Geo = DecodeGeometry<D, BS, G>;
+    static constexpr size_t kQ = (size_t)NW * ST * Geo::kStageBytes;
+    static constexpr size_t kBars = kQ + (size_t)NW * ST * Geo::kQBytes;
     static constexpr size_t kMeta = kBars + (size_t)NW * ST * 8;
     static constexpr size_t kCum = kMeta + (size_t)NW * ST * 16;
-    static constexpr size_t kFixed = kCum;
+    static constexpr size_t kAlign = 1024;              // slack for aligning the base
+    static constexpr size_t kFixed = kCum + kAlign;
     static constexpr size_t kPerSeq = 8;
-    __host__ __device__ static size_t bytes(int n) { return kCum + 4 * (size_t)(n + 1) + 4 * (size_t)n; }
 };
 
-// One chunk: rows [0, rows) of the K and V tiles in shared memory.
+// Zeroes V rows [R, kRows) of a ragged chunk's tile (every byte of those rows,
+// so the swizzle does not matter).
 template <int D, int BS, int G>
-__device__ __forceinline__ void process_chunk(const unsigned char *sk, const unsigned char *sv, int rows,
-                                              const float (&q)[G][8], float (&m)[G], float (&l)[G],
-                                              float (&acc)[G][8], int lane) {
+__device__ __forceinline__ void zero_tail_rows(unsigned char *vt, int R, int lane) {
     using Geo = DecodeGeometry<D, BS, G>;
-    constexpr int LPR = Geo::kLanesPerRow;
-    constexpr int RPI = Geo::kRowsPerLoad;
-    const int rg = lane / LPR;
-    const int cl = lane % LPR;
-#pragma unroll
-    for (int c0 = 0; c0 < Geo::kLoads; c0 += Geo::kSub) {
-        if (c0 * RPI >= rows) break;  // warp-uniform: the rest of the chunk is past the context
-        float sc[Geo::kSub][G];
-#pragma unroll
-        for (int i = 0; i < Geo::kSub; ++i) {
-            const int row = (c0 + i) * RPI + rg;
-            const uint4 raw = *reinterpret_cast<const uint4 *>(sk + row * Geo::kRowBytes + cl * 16);
-            float kf[8];
-            unpack8(raw, kf);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float d = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) d = fmaf(q[g][e], kf[e], d);
-                sc[i][g] = d;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < Geo::kSub; ++i)
-#pragma unroll
-            for (int g = 0; g < G; ++g)
-#pragma unroll
-                for (int o = LPR / 2; o >= 1; o >>= 1) sc[i][g] += __shfl_xor_sync(kFullMask, sc[i][g], o);
+    constexpr int kVecs = 8 * Geo::kHalves;  // 16-byte vectors per row
+    const int n = (Geo::kRows - R) * kVecs;
+    for (int i = lane; i < n; i += 32) {
+        const int r = R + i / kVecs;
+        const int v = i % kVecs;
+        *reinterpret_cast<uint4 *>(vt + (v >> 3) * Geo::kHalfBytes + r * 128 + (v & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+}
 
-        float mx[G];
+// One chunk of R valid rows: tiles at kt / vt (shared-memory addresses).
+// Lane (g, t) = (lane / 4, lane % 4) owns query head g (valid if g < G), rows
+// 2t, 2t+1 (+8) of the scores and output dims 8j + 2t, 8j + 2t + 1.
+template <int D, int BS, int G>
+__device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, const uint32_t (&qa)[D / 16][2],
+                                              float scale_log2, float &m, float &l, float (&o)[D / 8][4],
+                                              int lane) {
+    using Geo = DecodeGeometry<D, BS, G>;
+    const int t = lane & 3;
+    const int mi = lane >> 3;   // which 8x8 matrix this lane addresses in ldmatrix
+    const int rr = lane & 7;    // which row of it
+
+    // ---- S^T = Q . K^T ------------------------------------------------------
+    float s[Geo::kNT][4];
 #pragma unroll
-        for (int g = 0; g < G; ++g) mx[g] = -CUDART_INF_F;
+    for (int nt = 0; nt < Geo::kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-        for (int i = 0; i < Geo::kSub; ++i) {
-            const bool valid = (c0 + i) * RPI + rg < rows;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                sc[i][g] = valid ? sc[i][g] : -CUDART_INF_F;
-                mx[g] = fmaxf(mx[g], sc[i][g]);
-            }
+    for (int kk = 0; kk < Geo::kKSteps; ++kk) {
+        // matrices: (n-tile mi>>1, dims 16kk + 8(mi&1)); the row's 16-byte chunk
+        // c sits at c ^ (row & 7) in the swizzled tile
+        const int nt = (Geo::kNT == 2) ? (mi >> 1) : 0;
+        const int row = 8 * nt + rr;
+        const int c = (2 * kk + (mi & 1)) & 7;
+        const uint32_t addr = kt + (kk >> 2) * Geo::kHalfBytes + row * 128 + ((c ^ rr) << 4);
+        if (Geo::kNT == 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(addr, b0, b1, b2, b3);
+            mma_16816(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_16816(s[Geo::kNT - 1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+        } else {
+            uint32_t b0, b1;
+            ldsm_x2(addr, b0, b1);
+            mma_16816(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
         }
+    }
+
+    // ---- online softmax (per query head; rows past R masked) ----------------
+    float x[Geo::kNT][2];
+    float mx = -CUDART_INF_F;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+    for (int nt = 0; nt < Geo::kNT; ++nt)
 #pragma unroll
-            for (int o = LPR; o < 32; o <<= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFullMask, mx[g], o));
-            // row 0 of this sub-step is valid, so mx and the new max are finite
-            const float mn = fmaxf(m[g], mx[g]);
-            const float corr = exp2f(m[g] - mn);  // m = -inf at a piece's start -> 0
-            m[g] = mn;
-            l[g] *= corr;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] *= corr;
+        for (int j = 0; j < 2; ++j) {
+            const int row = 8 * nt + 2 * t + j;
+            x[nt][j] = row < R ? s[nt][j] * scale_log2 : -CUDART_INF_F;
+            mx = fmaxf(mx, x[nt][j]);
         }
+    mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2));
+    const float mn = fmaxf(m, mx);          // row 0 is valid: finite
+    const float corr = exp2f(m - mn);       // m = -inf at a piece's start -> 0
+    m = mn;
+    l *= corr;
 #pragma unroll
-        for (int i = 0; i < Geo::kSub; ++i) {
-            const int row = (c0 + i) * RPI + rg;
-            float pr[G];
+    for (int j = 0; j < Geo::kDTiles; ++j) {
+        o[j][0] *= corr;
+        o[j][1] *= corr;
+    }
+    float pr[Geo::kNT][2];
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                pr[g] = exp2f(sc[i][g] - m[g]);  // masked rows: exp2(-inf) = 0
-                l[g] += pr[g];
-            }
-            if (row < rows) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(sv + row * Geo::kRowBytes + cl * 16);
-                float vf[8];
-                unpack8(raw, vf);
+    for (int nt = 0; nt < Geo::kNT; ++nt)
 #pragma unroll
-                for (int g = 0; g < G; ++g)
+        for (int j = 0; j < 2; ++j) {
+            pr[nt][j] = exp2f(x[nt][j] - mn);  // masked rows: exp2(-inf) = 0
+            l += pr[nt][j];
+        }
+    // P as A fragments: hi = fp16(p), lo = fp16(p - hi)
+    const uint32_t h0 = pack_half2(pr[0][0], pr[0][1]);
+    const float2 f0 = unpack_half2(h0);
+    const uint32_t lo0 = pack_half2(pr[0][0] - f0.x, pr[0][1] - f0.y);
+    uint32_t h2 = 0u, lo2 = 0u;
+    if (Geo::kNT == 2) {
+        h2 = pack_half2(pr[Geo::kNT - 1][0], pr[Geo::kNT - 1][1]);
+        const float2 f2 = unpack_half2(h2);
+        lo2 = pack_half2(pr[Geo::kNT - 1][0] - f2.x, pr[Geo::kNT - 1][1] - f2.y);
+    }
+
+    // ---- O += P . V ----------------------------------------------------------
+    if (Geo::kNT == 2) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pr[g], vf[e], acc[g][e]);
+        for (int dp = 0; dp < Geo::kDTiles / 2; ++dp) {
+            // matrices: (rows 8(mi&1).., dims 16dp + 8(mi>>1))
+            const int row = rr + 8 * (mi & 1);
+            const int c = (2 * dp + (mi >> 1)) & 7;
+            const uint32_t addr = vt + (dp >> 2) * Geo::kHalfBytes + row * 128 + ((c ^ rr) << 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(addr, b0, b1, b2, b3);
+            mma_16816(o[2 * dp], h0, 0u, h2, 0u, b0, b1);
+            mma_16816(o[2 * dp], lo0, 0u, lo2, 0u, b0, b1);
+            mma_16816(o[2 * dp + 1], h0, 0u, h2, 0u, b2, b3);
+            mma_16816(o[2 * dp + 1], lo0, 0u, lo2, 0u, b2, b3);
+        }
+    } else {
+#pragma unroll
+        for (int dq = 0; dq < Geo::kDTiles / 4; ++dq) {
+            // matrices: (rows 0-7, dims 32dq + 8mi); rows 8-15 of P are zero
+            const int c = (4 * dq + mi) & 7;
+            const uint32_t addr = vt + (dq >> 1) * Geo::kHalfBytes + rr * 128 + ((c ^ rr) << 4);
+            uint32_t b[4];
+            ldsm_x4_trans(addr, b[0], b[1], b[2], b[3]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                mma_16816(o[4 * dq + j], h0, 0u, 0u, 0u, b[j], 0u);
+                mma_16816(o[4 * dq + j], lo0, 0u, 0u, 0u, b[j], 0u);
             }
         }
     }
 }
 
-// Counts one more piece of a segment in for this call; returns the count.
-__device__ __forceinline__ int count_piece(unsigned long long *cnt, uint32_t generation) {
-    unsigned long long cur = atomicAdd(cnt, 0ull);
+// Completion counters hold (epoch << 32 | arrivals).  Every call prepares the
+// counters of the NEXT call (the other parity) as (epoch + 1, 0), so counting
+// in is normally a single atomic add.  A counter in any other state (a fresh
+// workspace, or one left by a call that gave up) is swung to (epoch, 1) by the
+// first arrival that sees it.  Returns this arrival's 1-based position out of
+// `total` arrivals.
+__device__ __forceinline__ int count_in_tagged(unsigned long long *cnt, uint32_t epoch, int total) {
+    const unsigned long long tag = (unsigned long long)epoch << 32;
+    const unsigned long long kLow = 0xffffffffull;
+    auto valid = [&](unsigned long long v) { return (v & ~kLow) == tag && (v & kLow) < (unsigned long long)total; };
+    unsigned long long old = atomicAdd(cnt, 1ull);
+    if (valid(old)) return (int)(old & kLow) + 1;
+    unsigned long long cur = old + 1;
 #pragma unroll 1
     while (true) {
-        const unsigned long long want =
-            ((uint32_t)(cur >> 32) == generation) ? cur + 1 : (((unsigned long long)generation << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(cnt, cur, want);
-        if (prev == cur) return (int)(want & 0xffffffffull);
+        if (valid(cur)) {
+            old = atomicAdd(cnt, 1ull);
+            if (valid(old)) return (int)(old & kLow) + 1;
+            cur = old + 1;
+            continue;
+        }
+        const unsigned long long prev = atomicCAS(cnt, cur, tag | 1ull);
+        if (prev == cur) return 1;
         cur = prev;
     }
 }
 
 // Where a worker warp is: what finish_piece needs besides the piece itself.
 struct WorkerCtx {
-    const int *cum;   // chunk prefix sums (shared memory)
-    int64_t W;        // workers in the grid
-    int64_t T;        // chunks in the batch
-    int64_t wid;      // this worker
-    int rows_per_chunk;
+    const int *cum;          // chunk prefix sums (shared memory)
+    const int64_t *bounds;   // CTA ranges, [C + 1] (shared memory)
+    int C;                   // CTAs in the grid
+    int nw;                  // workers per CTA
+    int64_t W;               // workers in the grid
+    int64_t T;               // chunks in the batch
+    int64_t wid;             // this worker
+    uint32_t epoch;          // this call's epoch
+    unsigned long long *count;  // this call's per-segment counters (global)
+    int *cta_count;          // per-worker-slot counters of this CTA (shared)
+
+    __device__ __forceinline__ int64_t start(int64_t w) const {
+        return w >= W ? T : worker_start2(bounds, nw, w);
+    }
 };
 
-// One warp merges the pieces of a cut segment:
-// M = max_p m_p;  out = sum_p acc_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+// One warp merges the pieces of a cut segment, in worker order, combining
+// (max, sum, output) online: M' = max(M, m_p), X' = X 2^(M - M') + x_p 2^(m_p - M').
+// Each piece's (m, l) and output slice are loaded together (one L2 round trip).
 template <int D, int G>
-__device__ __forceinline__ void merge_segment(const DecodeParams &p, int s, int kvh, int64_t g0, int64_t wa,
-                                           int64_t wb, int64_t W, int64_t T, int lane) {
+__device__ __forceinline__ void merge_segment(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh,
+                                              int64_t g0, int64_t wa, int64_t wb, int lane) {
     constexpr int PER = D / 32;  // output elements per lane and head
-#pragma unroll 1
+    float M[G], L[G], O[G][PER];
+#pragma unroll
     for (int g = 0; g < G; ++g) {
-        float M = -CUDART_INF_F;
-        for (int64_t w = wa; w <= wb; ++w) {
-            const int64_t st = worker_start(w, W, T);
-            if (st == worker_start(w + 1, W, T)) continue;
-            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
-            M = fmaxf(M, __ldcg(p.ws_ml + b * 2));
-        }
-        float L = 0.f, O[PER];
+        M[g] = -CUDART_INF_F;
+        L[g] = 0.f;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) O[k] = 0.f;
-        for (int64_t w = wa; w <= wb; ++w) {
-            const int64_t st = worker_start(w, W, T);
-            if (st == worker_start(w + 1, W, T)) continue;
-            const int64_t b = (w * 2 + partial_slot(st, g0)) * G + g;
-            const float f = exp2f(__ldcg(p.ws_ml + b * 2) - M);
-            L = fmaf(__ldcg(p.ws_ml + b * 2 + 1), f, L);
-            const float *src = p.ws_acc + b * D + lane * PER;
+        for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
+    }
+#pragma unroll 1
+    for (int64_t w = wa; w <= wb; ++w) {
+        const int64_t st = wc.start(w);
+        if (st == wc.start(w + 1)) continue;
+        const int64_t b = (w * 2 + partial_slot(st, g0)) * G;
+        float2 ml[G];
+        float a[G][PER];
 #pragma unroll
-            for (int k = 0; k < PER; ++k) O[k] = fmaf(__ldcg(src + k), f, O[k]);
+        for (int g = 0; g < G; ++g) {
+            ml[g] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml) + b + g);
+            const float *src = p.ws_acc + (b + g) * D + lane * PER;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) a[g][k] = __ldcg(src + k);
         }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float mn = fmaxf(M[g], ml[g].x);
+            const float f_old = exp2f(M[g] - mn);
+            const float f_new = exp2f(ml[g].x - mn);
+            L[g] = L[g] * f_old + ml[g].y * f_new;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) O[g][k] = O[g][k] * f_old + a[g][k] * f_new;
+            M[g] = mn;
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
         __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[k] / L);
+        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] / L[g]);
     }
 }
 
-// Finish a piece: fold the row groups of the warp together, then write the
-// output row (whole segment) or the partial (cut segment); the last piece of
-// a cut segment to arrive merges the segment.
+// Finish a piece: sum l over the 4 lanes of each head, then write the output
+// row (whole segment) or store the partial (cut segment).  Returns true for a
+// stored partial; the caller counts it in later (count_in).
 template <int D, int G>
-__device__ __forceinline__ void finish_piece(const DecodeParams &p, const WorkerCtx &wc, const int4 md,
-                                             const float (&m)[G], float (&l)[G], float (&acc)[G][8],
-                                             int lane) {
-    constexpr int LPR = D / 8;
-#pragma unroll
-    for (int o = LPR; o < 32; o <<= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            l[g] += __shfl_xor_sync(kFullMask, l[g], o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(kFullMask, acc[g][e], o);
-        }
-    }
+__device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx &wc, const int4 md, float m,
+                                             float l, const float (&o)[D / 8][4], int lane) {
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    l += __shfl_xor_sync(kFullMask, l, 1);
+    l += __shfl_xor_sync(kFullMask, l, 2);
     const int s = md.x, kvh = md.y, flags = md.w;
     if (flags & kWhole) {
-        if (lane < LPR) {
+        if (g < G) {
+            __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + 2 * t;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float o8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o8[e] = acc[g][e] / l[g];
-                __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * 8;
-                *reinterpret_cast<uint4 *>(dst) = pack8(o8);
-            }
+            for (int j = 0; j < D / 8; ++j)
+                *reinterpret_cast<uint32_t *>(dst + 8 * j) = pack_half2(o[j][0] / l, o[j][1] / l);
         }
-        return;
+        return false;
     }
     const int64_t base = (wc.wid * 2 + ((flags & kSlot1) ? 1 : 0)) * G;
-    if (lane < LPR) {
+    if (g < G) {
+        float *dst = p.ws_acc + (base + g) * D + 2 * t;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ws_acc + (base + g) * D + lane * 8);
-            dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-            dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+        for (int j = 0; j < D / 8; ++j) *reinterpret_cast<float2 *>(dst + 8 * j) = make_float2(o[j][0], o[j][1]);
+        if (t == 0) {
+            p.ws_ml[(base + g) * 2] = m;
+            p.ws_ml[(base + g) * 2 + 1] = l;
         }
     }
-    if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            p.ws_ml[(base + g) * 2] = m[g];
-            p.ws_ml[(base + g) * 2 + 1] = l[g];
-        }
-    }
-    // make the partial visible device-wide, then count it in
-    __threadfence();
-    __syncwarp();
+    return true;
+}
+
+// Counts a stored partial of segment (s, kvh) in; the piece that completes
+// the count merges the segment.  Pieces of a segment that stays inside this
+// CTA meet on a shared-memory counter with CTA-scope ordering; a segment that
+// spans CTAs (only one longer than the CTA boundary could snap past) meets on
+// the workspace's epoch-tagged counter with GPU-scope ordering.
+template <int D, int G>
+__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh, int lane) {
     const int nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
     const int64_t g0 = wc.cum[s] + (int64_t)kvh * nch;
-    const int64_t wa = worker_of(g0, wc.W, wc.T);
-    const int64_t wb = worker_of(g0 + nch - 1, wc.W, wc.T);
+    const int64_t wa = worker_of2(wc.bounds, wc.C, wc.nw, g0);
+    const int64_t wb = worker_of2(wc.bounds, wc.C, wc.nw, g0 + nch - 1);
     int pieces = 0;
-    for (int64_t w = wa; w <= wb; ++w) pieces += worker_start(w, wc.W, wc.T) < worker_start(w + 1, wc.W, wc.T);
+    for (int64_t w = wa; w <= wb; ++w) pieces += wc.start(w) < wc.start(w + 1);
+    const bool local = (wa / wc.nw == blockIdx.x) && (wb / wc.nw == blockIdx.x);
     int arrived = 0;
-    if (lane == 0) arrived = count_piece(p.ws_count + (int64_t)s * p.num_kv_heads + kvh, p.generation);
-    arrived = __shfl_sync(kFullMask, arrived, 0);
-    if (arrived == pieces) {
-        __threadfence();
-        merge_segment<D, G>(p, s, kvh, g0, wa, wb, wc.W, wc.T, lane);
-        // every piece of this call has arrived: leave the counter at zero, so
-        // that a replay of the same launch (same tag) starts from a clean count
-        if (lane == 0) atomicExch(p.ws_count + (int64_t)s * p.num_kv_heads + kvh, 0ull);
+    if (local) {
+        __threadfence_block();  // the partial is visible to this CTA before it is counted
+        __syncwarp();
+        if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % wc.nw), 1) + 1;
+        arrived = __shfl_sync(kFullMask, arrived, 0);
+        if (arrived == pieces) __threadfence_block();
+    } else {
+        __threadfence();        // the partial is visible device-wide before it is counted
+        __syncwarp();
+        if (lane == 0) arrived = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, pieces);
+        arrived = __shfl_sync(kFullMask, arrived, 0);
+        if (arrived == pieces) __threadfence();
     }
+    if (arrived == pieces) merge_segment<D, G>(p, wc, s, kvh, g0, wa, wb, lane);
 }
 
 template <int D, int BS, int G, int NW, int ST>
-__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
     using Geo = DecodeGeometry<D, BS, G>;
-    using Smem = DecodeSmem<NW, ST, Geo::kStageBytes>;
-    extern __shared__ __align__(128) unsigned char smem[];
+    using Smem = DecodeSmem<NW, ST, D, BS, G>;
+    extern __shared__ unsigned char smem_raw[];
     __shared__ int warp_sums[32];
     __shared__ int grand_total;
+    // 1024-byte aligned base: the 128-byte swizzle pattern is tied to address bits
+    unsigned char *smem =
+        smem_raw + ((Smem::kAlign - (smem_addr(smem_raw) & (Smem::kAlign - 1))) & (Smem::kAlign - 1));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::kBars);
     int4 *meta = reinterpret_cast<int4 *>(smem + Smem::kMeta);
     int *cum = reinterpret_cast<int *>(smem + Smem::kCum);
     const int N = p.num_seqs;
     int *ctx = cum + N + 1;
+    int64_t *bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
+    __shared__ int cta_count[NW];
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int Hkv = p.num_kv_heads;
     const int max_ctx = p.max_blocks_per_seq * BS;
+
+    if (tid == 0) {
+        prefetch_tensormap(&p.tmap_k);
+        prefetch_tensormap(&p.tmap_v);
+        prefetch_tensormap(&p.tmap_k8);
+        prefetch_tensormap(&p.tmap_v8);
+    }
 
     // ---- prologue: chunk counts per sequence and their prefix sums ----------
     const int per = (N + NW * 32 - 1) / (NW * 32);
@@ -329,10 +430,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         if (lane >= o) incl += y;
     }
     if (lane == 31) warp_sums[warp] = incl;
+    __shared__ uint32_t epoch_s;
     if (tid == 0) {
         for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), 1);
         fence_barrier_init();
+        epoch_s = (uint32_t)__ldcg(p.ws_sync);
     }
+    if (tid < NW) cta_count[tid] = 0;
     __syncthreads();
     if (warp == 0) {
         const int v = lane < NW ? warp_sums[lane] : 0;
@@ -355,6 +459,18 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         if (tid == 0) cum[N] = grand_total;
     }
     __syncthreads();
+    // this call counts on the counters of its epoch's parity, and prepares the
+    // other parity's counters for the next call
+    const uint32_t epoch = epoch_s;
+    const int parity = epoch & 1;
+    unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;
+    {
+        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * N * Hkv;
+        const unsigned long long next_tag = (unsigned long long)(epoch + 1) << 32;
+        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)gridDim.x * NW * 32)
+            count_next[i] = next_tag;
+        if (blockIdx.x == 0 && tid == 0) p.ws_sync[1 + (parity ^ 1)] = next_tag;
+    }
     // rows of empty contexts are zero; no worker visits them
     for (int s = blockIdx.x; s < N; s += gridDim.x) {
         if (ctx[s] != 0) continue;
@@ -362,41 +478,63 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
         for (int i = tid; i < p.num_heads * D / 8; i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
     }
 
-    // ---- this warp's share of the chunks -----------------------------------
+    // ---- CTA ranges snapped to segment boundaries, then this warp's share ----
     const int64_t T = cum[N];
-    const int64_t W = (int64_t)gridDim.x * NW;
+    const int C = gridDim.x;
+    for (int c = tid; c <= C; c += NW * 32)
+        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, 3 * NW);
+    __syncthreads();
+    const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
-    const int64_t gb = worker_start(wid, W, T);
-    const int64_t ge = worker_start(wid + 1, W, T);
-    if (gb >= ge) return;
+    const int64_t gb = worker_start2(bounds, NW, wid);
+    const int64_t ge = wid + 1 >= W ? T : worker_start2(bounds, NW, wid + 1);
+    // every warp counts itself out at the end; the last one advances the epoch
+    auto exit_warp = [&]() {
+        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
+            atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
+    };
+    if (gb >= ge) {
+        exit_warp();
+        return;
+    }
     const int n = (int)(ge - gb);
-    const WorkerCtx wc{cum, W, T, wid, Geo::kRows};
+    const WorkerCtx wc{cum, bounds, C, NW, W, T, wid, epoch, count_now, cta_count};
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
+    const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kQBytes;
+    const uint32_t wq_a = smem_addr(wq);
     const uint32_t bar_a = smem_addr(bars + warp * ST);
     int4 *wmeta = meta + warp * ST;
 
-    // block-table entry of chunk g (raw; validated when used), 0 past the share
-    auto table_entry = [&](int64_t g) -> int {
-        if (g >= ge) return 0;
-        const ChunkPos q = locate_chunk(cum, N, Hkv, g);
+    // the walk: cut pieces first (see share_order)
+    const ShareOrder order = share_order(cum, N, Hkv, gb, ge);
+
+    // block-table entry of the chunk at walk position i (raw; validated when
+    // used), 0 past the share
+    auto table_entry = [&](int i) -> int {
+        if (i >= n) return 0;
+        const ChunkPos q = locate_chunk(cum, N, Hkv, order.at(i));
         const int lb = chunk_block(q.c, BS, Geo::kRows);
         return __ldg(p.block_tables + (int64_t)q.s * p.max_blocks_per_seq + lb);
     };
-    int64_t win = gb;
-    int tab_cur = table_entry(gb + lane);
-    int tab_nxt = table_entry(gb + 32 + lane);
-    ChunkPos pos = locate_chunk(cum, N, Hkv, gb);  // next chunk to issue
+    int win = 0;
+    int tab_cur = table_entry(lane);
+    int tab_nxt = table_entry(32 + lane);
+    ChunkPos pos;  // chunk being issued
 
     auto issue = [&](int i) {
-        const int64_t g = gb + i;
-        if (g - win >= 32) {
+        const int64_t g = order.at(i);
+        if (order.jumps_at(i))
+            pos = locate_chunk(cum, N, Hkv, g);
+        else
+            next_chunk(pos, cum, N, Hkv);
+        if (i - win >= 32) {
             win += 32;
             tab_cur = tab_nxt;
             tab_nxt = table_entry(win + 32 + lane);
         }
-        int phys = __shfl_sync(kFullMask, tab_cur, (int)(g - win));
+        int phys = __shfl_sync(kFullMask, tab_cur, i - win);
         if (lane == 0) {
             if (phys < 0 || phys >= p.num_blocks) {
                 report(p.status, PKV_ERR_OUT_OF_RANGE);
@@ -407,34 +545,44 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
             const int flags = chunk_flags(pos, g, gb, ge);
             wmeta[stage] = make_int4(pos.s, pos.kvh, rows, flags);
             const uint32_t bar = bar_a + stage * 8;
-            const uint32_t dst = wst_a + stage * Geo::kStageBytes;
-            const uint32_t kv_bytes = (uint32_t)rows * Geo::kRowBytes;
+            const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
+            const uint32_t vdst = kdst + Geo::kTileBytes;
+            // a whole chunk is one box per cache; a last chunk of at most 8 rows
+            // of a 16-row chunk takes one 8-row box per half instead
+            const bool short_box = Geo::kNT == 2 && rows <= 8;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, 2 * kv_bytes + ((flags & kFirst) ? Geo::kQBytes : 0));
-            const int64_t off = chunk_src_offset(phys, pos.kvh, pos.c, Hkv, BS, Geo::kRows, D);
-            bulk_g2s(dst, p.key_cache + off, kv_bytes, bar);
-            bulk_g2s(dst + Geo::kChunkBytes, p.value_cache + off, kv_bytes, bar);
+            mbar_arrive_expect_tx(bar, (short_box ? 2 * Geo::kHalves * Geo::kBoxBytes : 2 * Geo::kTileBytes) +
+                                           ((flags & kFirst) ? Geo::kQBytes : 0));
+            // row of the cache viewed as [num_blocks * Hkv * BS rows]
+            const int y = (int)(((int64_t)phys * Hkv + pos.kvh) * BS + (pos.c * Geo::kRows) % BS);
+            if (!short_box) {
+                tma_load_3d(kdst, &p.tmap_k, 0, y, 0, bar);
+                tma_load_3d(vdst, &p.tmap_v, 0, y, 0, bar);
+            } else {
+#pragma unroll
+                for (int h = 0; h < Geo::kHalves; ++h) {
+                    tma_load_3d(kdst + h * Geo::kHalfBytes, &p.tmap_k8, 0, y, h, bar);
+                    tma_load_3d(vdst + h * Geo::kHalfBytes, &p.tmap_v8, 0, y, h, bar);
+                }
+            }
             if (flags & kFirst)
-                bulk_g2s(dst + 2 * Geo::kChunkBytes,
-                         p.query + ((int64_t)pos.s * p.num_heads + pos.kvh * G) * D, Geo::kQBytes, bar);
+                bulk_g2s(wq_a + stage * Geo::kQBytes, p.query + ((int64_t)pos.s * p.num_heads + pos.kvh * G) * D,
+                         Geo::kQBytes, bar);
         }
     };
 
     int issued = 0;
-    for (; issued < min(ST, n); ++issued) {
-        issue(issued);
-        if (issued + 1 < n) next_chunk(pos, cum, N, Hkv);
-    }
+    for (; issued < min(ST, n); ++issued) issue(issued);
 
-    float q[G][8], m[G], l[G], acc[G][8];
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    uint32_t qa[D / 16][2];
+    float m = -CUDART_INF_F, l = 0.f;
+    float o[D / 8][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -CUDART_INF_F;
-        l[g] = 0.f;
+    for (int kk = 0; kk < D / 16; ++kk) qa[kk][0] = qa[kk][1] = 0u;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) q[g][e] = acc[g][e] = 0.f;
-    }
-    const int cl = lane % Geo::kLanesPerRow;
+    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
     for (int i = 0; i < n; ++i) {
         const int stage = i % ST;
@@ -446,35 +594,34 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
             if (lane == 0) report(p.status, PKV_ERR_DEVICE_TIMEOUT);
             for (int j = i; j < issued; ++j)
                 mbar_wait_bounded(bar_a + (j % ST) * 8, (uint32_t)(j / ST) & 1u, p.wait_limit_ns);
+            exit_warp();
             return;
         }
         const int4 md = wmeta[stage];
-        const unsigned char *sk = wst + stage * Geo::kStageBytes;
         if (md.w & kFirst) {
-            const unsigned char *sq = sk + 2 * Geo::kChunkBytes;
+            // query rows of the group as mma A fragments (rows g >= G stay 0)
+            const unsigned char *sq = wq + stage * Geo::kQBytes;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(sq + g * D * 2 + cl * 16);
-                float f[8];
-                unpack8(raw, f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    q[g][e] = f[e] * p.scale_log2;
-                    acc[g][e] = 0.f;
-                }
-                m[g] = -CUDART_INF_F;
-                l[g] = 0.f;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
+                qa[kk][1] =
+                    gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 8 + 2 * tq) * 2) : 0u;
             }
+            m = -CUDART_INF_F;
+            l = 0.f;
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         }
-        process_chunk<D, BS, G>(sk, sk + Geo::kChunkBytes, md.z, q, m, l, acc, lane);
-        if (md.w & kLast) finish_piece<D, G>(p, wc, md, m, l, acc, lane);
+        if (md.z < Geo::kRows) zero_tail_rows<D, BS, G>(wst + stage * Geo::kStageBytes + Geo::kTileBytes, md.z, lane);
+        const uint32_t kt = wst_a + stage * Geo::kStageBytes;
+        consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
+        // refill the stage first: a piece's finish (and a cut piece's count and
+        // merge) then overlaps the copies in flight instead of draining the ring
         __syncwarp();
-        if (issued < n) {
-            issue(issued);
-            if (issued + 1 < n) next_chunk(pos, cum, N, Hkv);
-            ++issued;
-        }
+        if (issued < n) issue(issued++);
+        if ((md.w & kLast) && finish_piece<D, G>(p, wc, md, m, l, o, lane)) count_in<D, G>(p, wc, md.x, md.y, lane);
     }
+    exit_warp();
 }
 
 }  // namespace pkv

@@ -15,14 +15,24 @@ namespace pkv {
 namespace {
 
 // Warps (workers) per CTA and ring stages per warp.  A stage holds one K
-// chunk, one V chunk (4 KB each at head_dim 128) and the group's query rows.
-constexpr int kWarps = 4;
-constexpr int kStages = (PKV_D == 64) ? 4 : 3;
+// chunk and one V chunk (4 KB each at head_dim 128) plus the group's query
+// rows.  One CTA of 8 workers x 2 stages per SM measured fastest on GB300
+// (more warps per SM hide the per-chunk math; deeper rings did not help).
+#ifdef PKV_DECODE_WARPS
+constexpr int kWarps = PKV_DECODE_WARPS;
+#else
+constexpr int kWarps = 8;
+#endif
+#ifdef PKV_DECODE_STAGES
+constexpr int kStages = PKV_DECODE_STAGES;
+#else
+constexpr int kStages = (PKV_D == 64) ? 4 : 2;
+#endif
 
 template <int BS>
 DecodeKernelInfo info_of() {
     using Geo = DecodeGeometry<PKV_D, BS, PKV_G>;
-    using Smem = DecodeSmem<kWarps, kStages, Geo::kStageBytes>;
+    using Smem = DecodeSmem<kWarps, kStages, PKV_D, BS, PKV_G>;
     DecodeKernelInfo i;
     i.fn = reinterpret_cast<const void *>(&paged_decode_kernel<PKV_D, BS, PKV_G, kWarps, kStages>);
     i.threads = kWarps * 32;
@@ -30,6 +40,7 @@ DecodeKernelInfo info_of() {
     i.rows_per_chunk = Geo::kRows;
     i.smem_fixed = Smem::kFixed;
     i.smem_per_seq = Smem::kPerSeq;
+    i.smem_per_cta = 8;
     return i;
 }
 

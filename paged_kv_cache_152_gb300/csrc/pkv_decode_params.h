@@ -2,6 +2,7 @@
 #ifndef PKV_DECODE_PARAMS_H
 #define PKV_DECODE_PARAMS_H
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -9,6 +10,13 @@
 namespace pkv {
 
 struct DecodeParams {
+    // The caches viewed as 3-D tensors (64 dims, NB*Hkv*BS rows, D/64 halves;
+    // row stride D*2 bytes, half stride 128 bytes) read with the 128-byte
+    // swizzle, so that a box lands as [half][row][64 dims]:
+    CUtensorMap tmap_k;           // box: all halves of one chunk's rows
+    CUtensorMap tmap_v;
+    CUtensorMap tmap_k8;          // box: one half of 8 rows (short last chunks)
+    CUtensorMap tmap_v8;
     __half *out;                  // [N][H][D]
     const __half *query;          // [N][H][D]
     const __half *key_cache;      // [NB][Hkv][BS][D]
@@ -17,7 +25,11 @@ struct DecodeParams {
     const int32_t *context_lens;  // [N]
     float *ws_ml;                 // [W][2][G][2] partial (max, sum)
     float *ws_acc;                // [W][2][G][D] partial unnormalised outputs
-    unsigned long long *ws_count; // [N*Hkv] (call generation << 32 | pieces arrived)
+    // Completion counters, each (epoch << 32 | arrivals): ws_sync[0] is the
+    // epoch word, ws_sync[1 + parity] the per-call exit counters, and ws_count
+    // two arrays (by epoch parity) of N*Hkv per-segment counters.
+    unsigned long long *ws_sync;  // [3]
+    unsigned long long *ws_count; // [2][N*Hkv]
     int32_t *status;              // nullable
     int num_seqs;
     int num_heads;
@@ -25,18 +37,18 @@ struct DecodeParams {
     int max_blocks_per_seq;
     int num_blocks;
     float scale_log2;             // scale * log2(e)
-    uint32_t generation;          // nonzero, distinct for every call
     uint64_t wait_limit_ns;
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
 struct DecodeWorkspace {
-    size_t count, ml, acc, total;
+    size_t sync, count, ml, acc, total;
     static DecodeWorkspace plan(int num_seqs, int num_kv_heads, int64_t workers, int group, int head_dim) {
         auto up = [](size_t x) { return (x + 255) / 256 * 256; };
         DecodeWorkspace w;
-        w.count = 0;
-        w.ml = up(8 * (size_t)num_seqs * num_kv_heads);
+        w.sync = 0;
+        w.count = 256;
+        w.ml = w.count + up(2 * 8 * (size_t)num_seqs * num_kv_heads);
         w.acc = w.ml + up(4 * (size_t)workers * 2 * group * 2);
         w.total = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
         return w;
@@ -51,6 +63,7 @@ struct DecodeKernelInfo {
     int rows_per_chunk;
     size_t smem_fixed;     // dynamic shared memory without the per-sequence arrays
     size_t smem_per_seq;   // bytes per sequence (+ one extra int)
+    size_t smem_per_cta;   // bytes per CTA of the grid (+ one extra)
 };
 
 // Defined in pkv_decode_d{64,128}_g{1,2,4,8}.cu; false if not compiled.

@@ -110,6 +110,104 @@ PKV_HD int partial_slot(int64_t st, int64_t g0) {
     return st < g0 ? 1 : 0;
 }
 
+// Two-level split.  The T chunks are first divided among C CTAs: CTA c's
+// nominal start c*T/C moves to the nearest segment boundary when one lies
+// within snap = min(T/(4C), snap_cap) chunks, so that a segment is normally
+// read by one CTA only (moving a boundary by d chunks costs the CTA's warps
+// d/NW chunks each; a segment cut across CTAs costs two warps a device-wide
+// count and merge, worth a few chunks -- hence a small absolute cap).  Each
+// CTA's range is then divided equally among its NW warps: worker w = c*NW + k.
+PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_t c, int64_t C, int64_t T,
+                                 int64_t snap_cap) {
+    const int64_t nominal = (c * T) / C;
+    if (c == 0 || nominal >= T) return nominal >= T ? T : 0;
+    const ChunkPos p = locate_chunk(cum, n, num_kv_heads, nominal);
+    const int64_t g0 = nominal - p.c;          // segment's first chunk
+    const int64_t g1 = g0 + p.nch;             // one past its last
+    const int64_t snap = T / (4 * C) < snap_cap ? T / (4 * C) : snap_cap;
+    const int64_t left = nominal - g0, right = g1 - nominal;
+    if (left == 0) return nominal;
+    if (left <= right && left <= snap) return g0;
+    if (right < left && right <= snap) return g1;
+    return nominal;
+}
+
+// First chunk of worker w given the CTA bounds.
+PKV_HD int64_t worker_start2(const int64_t *bounds, int nw, int64_t w) {
+    const int64_t c = w / nw, k = w % nw;
+    const int64_t a = bounds[c], len = bounds[c + 1] - a;
+    return a + (k * len) / nw;
+}
+
+// Largest w (of C*nw workers) with worker_start2(w) <= g, 0 <= g < T.
+PKV_HD int64_t worker_of2(const int64_t *bounds, int C, int nw, int64_t g) {
+    int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (bounds[mid] <= g) lo = mid; else hi = mid;
+    }
+    const int64_t a = bounds[lo], len = bounds[lo + 1] - a;
+    // largest k with (k * len) / nw <= g - a
+    const int64_t k = ((g - a + 1) * nw + len - 1) / len - 1;
+    return (int64_t)lo * nw + (k < nw - 1 ? k : nw - 1);
+}
+
+// The order in which a worker walks its share [gb, ge): its cut pieces first
+// -- the last piece (when it runs past ge), then the first piece (when it
+// starts before gb) -- then everything between them in chunk order.  The
+// other pieces of a cut segment sit at the starts and ends of neighbouring
+// shares, so with every worker doing the same, cut segments complete early
+// and their merges overlap the rest of the work.  Pieces stay contiguous runs
+// of the walk, so chunk_flags is unchanged.
+struct ShareOrder {
+    int64_t a0, a1;   // range 1: the cut last piece (empty if none)
+    int64_t b0, b1;   // range 2: the cut first piece (empty if none)
+    int64_t c0, c1;   // range 3: the rest, in order
+
+    PKV_HD int64_t size() const { return (a1 - a0) + (b1 - b0) + (c1 - c0); }
+
+    // chunk at position i of the walk (0 <= i < size())
+    PKV_HD int64_t at(int64_t i) const {
+        const int64_t na = a1 - a0, nb = b1 - b0;
+        if (i < na) return a0 + i;
+        if (i < na + nb) return b0 + (i - na);
+        return c0 + (i - na - nb);
+    }
+
+    // true if position i starts a range (the walk jumps there)
+    PKV_HD bool jumps_at(int64_t i) const {
+        const int64_t na = a1 - a0, nb = b1 - b0;
+        return i == 0 || i == na || i == na + nb;
+    }
+};
+
+PKV_HD ShareOrder share_order(const int *cum, int n, int num_kv_heads, int64_t gb, int64_t ge) {
+    ShareOrder o;
+    o.a0 = o.a1 = o.b0 = o.b1 = gb;
+    o.c0 = gb;
+    o.c1 = ge;
+    if (gb >= ge) return o;
+    const ChunkPos first = locate_chunk(cum, n, num_kv_heads, gb);
+    const ChunkPos last = locate_chunk(cum, n, num_kv_heads, ge - 1);
+    const int64_t first_seg_end = gb + (first.nch - first.c);   // one past the first segment
+    const int64_t last_seg_start = (ge - 1) - last.c;           // the last segment's first chunk
+    if (first_seg_end >= ge) return o;  // the share lies inside one segment: one piece
+    const bool last_cut = last.c < last.nch - 1;
+    const bool first_cut = first.c > 0;
+    if (last_cut) {
+        o.a0 = last_seg_start;
+        o.a1 = ge;
+        o.c1 = last_seg_start;
+    }
+    if (first_cut) {
+        o.b0 = gb;
+        o.b1 = first_seg_end;
+        o.c0 = first_seg_end;
+    }
+    if (o.c0 > o.c1) o.c0 = o.c1;
+    return o;
+}
+
 // Element offset, in either cache, of the first row of chunk c of KV head kvh
 // whose block is physical block phys.
 PKV_HD int64_t chunk_src_offset(int phys, int kvh, int c, int num_kv_heads,

@@ -16,7 +16,18 @@ static int fails = 0;
 #define CHECK(c, ...) do { if (!(c)) { std::printf("FAIL %s:%d: ", __FILE__, __LINE__); \
     std::printf(__VA_ARGS__); std::printf("\n"); if (++fails > 5) std::exit(1); } } while (0)
 
+// split 0: equal shares over all W workers; split 1: snapped CTA ranges of
+// nw workers each (W = C * nw).
+static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W, int split,
+                           int nw);
+
 static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W) {
+    run_case_split(ctx, hkv, bs, sr, mb, W, 0, 1);
+    for (int nw : {1, 3, 8}) run_case_split(ctx, hkv, bs, sr, mb, ((W + nw - 1) / nw) * nw, 1, nw);
+}
+
+static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W, int split,
+                           int nw) {
     const int n = (int)ctx.size();
     std::vector<int> cum(n + 1, 0);
     for (int s = 0; s < n; ++s) cum[s + 1] = cum[s] + hkv * chunks_for(ctx[s], sr);
@@ -29,17 +40,42 @@ static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int m
                 truth.push_back({s, h, c, chunks_for(ctx[s], sr)});
     CHECK((int64_t)truth.size() == T, "T");
     if (T == 0) return;
+    const int C = (int)(W / nw);
+    const int64_t snap_cap = 3 * nw;
+    std::vector<int64_t> bounds(C + 1);
+    if (split == 1) {
+        for (int c = 0; c <= C; ++c)
+            bounds[c] = c == C ? T : snapped_cta_start(cum.data(), n, hkv, c, C, T, snap_cap);
+        for (int c = 0; c < C; ++c) CHECK(bounds[c] <= bounds[c + 1], "cta bounds not monotonic");
+        // a CTA boundary inside a segment could not snap: both ends are far
+        for (int c = 1; c < C; ++c) {
+            const int64_t b = bounds[c];
+            if (b <= 0 || b >= T) continue;
+            const ChunkPos p = locate_chunk(cum.data(), n, hkv, b);
+            if (p.c == 0) continue;
+            const int64_t snap = std::min<int64_t>(T / (4 * (int64_t)C), snap_cap);
+            CHECK(p.c > snap && p.nch - p.c > snap, "boundary left inside a short segment");
+        }
+    }
+    auto wstart = [&](int64_t w) -> int64_t {
+        if (split == 0) return worker_start(w, W, T);
+        return w >= W ? T : worker_start2(bounds.data(), nw, w);
+    };
+    auto wof = [&](int64_t g) -> int64_t {
+        if (split == 0) return worker_of(g, W, T);
+        return worker_of2(bounds.data(), C, nw, g);
+    };
     // ranges partition [0, T)
     std::vector<int> owner(T, -1);
     for (int64_t w = 0; w < W; ++w) {
-        const int64_t st = worker_start(w, W, T), en = worker_start(w + 1, W, T);
+        const int64_t st = wstart(w), en = wstart(w + 1);
         CHECK(st <= en, "range order");
         for (int64_t g = st; g < en; ++g) { CHECK(owner[g] == -1, "overlap"); owner[g] = (int)w; }
     }
     for (int64_t g = 0; g < T; ++g) {
         CHECK(owner[g] >= 0, "uncovered chunk %lld", (long long)g);
-        CHECK(worker_of(g, W, T) == owner[g], "worker_of(%lld)=%lld want %d", (long long)g,
-              (long long)worker_of(g, W, T), owner[g]);
+        CHECK(wof(g) == owner[g], "worker_of(%lld)=%lld want %d (split %d)", (long long)g, (long long)wof(g),
+              owner[g], split);
         const ChunkPos p = locate_chunk(cum.data(), n, hkv, g);
         CHECK(p.s == truth[g].s && p.kvh == truth[g].kvh && p.c == truth[g].c && p.nch == truth[g].nch,
               "locate %lld", (long long)g);
@@ -61,7 +97,7 @@ static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int m
     std::map<std::pair<int, int>, std::vector<std::pair<int64_t, int>>> partials;  // seg -> (worker, slot)
     std::set<std::pair<int, int>> whole_done;
     for (int64_t w = 0; w < W; ++w) {
-        const int64_t gb = worker_start(w, W, T), ge = worker_start(w + 1, W, T);
+        const int64_t gb = wstart(w), ge = wstart(w + 1);
         if (gb == ge) continue;
         ChunkPos p = locate_chunk(cum.data(), n, hkv, gb);
         bool in_piece = false;
@@ -101,6 +137,39 @@ static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int m
         }
         CHECK(!in_piece, "unterminated piece");
     }
+    // the reordered walk visits every chunk of the share once, keeps each piece
+    // a contiguous run that starts with its kFirst chunk and ends with its
+    // kLast chunk, and puts cut pieces before whole ones
+    for (int64_t w = 0; w < W; ++w) {
+        const int64_t gb = wstart(w), ge = wstart(w + 1);
+        const ShareOrder so = share_order(cum.data(), n, hkv, gb, ge);
+        CHECK(so.size() == ge - gb, "order size");
+        std::vector<int> seen(ge - gb + 1, 0);
+        bool in_piece = false, seen_whole = false;
+        for (int64_t i = 0; i < so.size(); ++i) {
+            const int64_t g = so.at(i);
+            CHECK(g >= gb && g < ge, "order outside share");
+            if (g < gb || g >= ge) break;
+            CHECK(seen[g - gb] == 0, "chunk visited twice");
+            seen[g - gb] = 1;
+            const ChunkPos p = locate_chunk(cum.data(), n, hkv, g);
+            const int f = chunk_flags(p, g, gb, ge);
+            if (i > 0 && !so.jumps_at(i)) {
+                const ChunkPos q = locate_chunk(cum.data(), n, hkv, so.at(i - 1));
+                ChunkPos nx = q;
+                next_chunk(nx, cum.data(), n, hkv);
+                CHECK(nx.s == p.s && nx.kvh == p.kvh && nx.c == p.c, "walk step");
+            }
+            if (f & kFirst) { CHECK(!in_piece, "piece not contiguous"); in_piece = true; }
+            CHECK(in_piece, "chunk before its piece's first");
+            if (f & kLast) {
+                in_piece = false;
+                if (f & kWhole) seen_whole = true;
+                else CHECK(!seen_whole, "cut piece after a whole one");
+            }
+        }
+        CHECK(!in_piece, "order ends inside a piece");
+    }
     // the merge kernel finds exactly the stored partials of every cut segment
     for (int s = 0; s < n; ++s) {
         const int nch = chunks_for(ctx[s], sr);
@@ -108,12 +177,12 @@ static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int m
             const auto seg = std::make_pair(s, h);
             if (nch == 0) { CHECK(!partials.count(seg) && !whole_done.count(seg), "empty seg touched"); continue; }
             const int64_t g0 = cum[s] + (int64_t)h * nch, g1 = g0 + nch;
-            const int64_t wa = worker_of(g0, W, T), wb = worker_of(g1 - 1, W, T);
+            const int64_t wa = wof(g0), wb = wof(g1 - 1);
             if (wa == wb) { CHECK(whole_done.count(seg) && !partials.count(seg), "uncut seg %d,%d", s, h); continue; }
             CHECK(!whole_done.count(seg), "cut seg written whole");
             std::vector<std::pair<int64_t, int>> found;
             for (int64_t w = wa; w <= wb; ++w) {
-                const int64_t st = worker_start(w, W, T), en = worker_start(w + 1, W, T);
+                const int64_t st = wstart(w), en = wstart(w + 1);
                 if (st == en) continue;
                 found.push_back({w, partial_slot(st, g0)});
             }

@@ -61,10 +61,10 @@ def test_noalloc_matches_regular_entry_point_twice(pkv):
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch(pkv):
-    case = Case(W.make("tiny"))
+    case = Case(W.make("gqa", num_seqs=4))
     out = torch.empty_like(case.out)
     wl = case.wl
-    huge = 200_000   # CTAs: the partial-result scratch would far exceed 16 MiB
+    huge = 4096      # CTAs (the most a call may ask for): partial results far beyond 16 MiB
     need = pkv.decode_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim,
                                      wl.block_size, huge)
     assert need > 16 * 1024 * 1024

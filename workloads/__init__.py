@@ -115,7 +115,7 @@ def tiny():
 
 def decode_7b(num_seqs=64, block_size=16):
     rng = np.random.default_rng(BASE_SEED + 1)
-    lens = rng.integers(50, 901, size=64)[:num_seqs]
+    lens = rng.integers(50, 901, size=max(64, num_seqs))[:num_seqs]
     return _simple("7b", 1, lens, 32, 32, 128, block_size)
 
 
