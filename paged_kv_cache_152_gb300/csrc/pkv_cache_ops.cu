@@ -11,6 +11,7 @@
 
 #include "../../include/pkv.h"
 #include "pkv_device.cuh"
+#include "pkv_launch.h"
 
 namespace pkv {
 
@@ -21,6 +22,8 @@ __global__ void __launch_bounds__(256)
                              uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
                              const int64_t *__restrict__ slot_mapping, int64_t num_vecs, int heads_x_vecs,
                              int vecs_per_row, int block_size, int64_t num_slots, int32_t *status) {
+    grid_dependency_wait();
+    launch_dependents();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < num_vecs; i += stride) {
         const int64_t t = i / heads_x_vecs;
@@ -48,6 +51,8 @@ __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
                        const int64_t *__restrict__ pairs, int num_pairs, int64_t vecs_per_block,
                        int num_blocks, int32_t *status) {
+    grid_dependency_wait();
+    launch_dependents();
     uint4 *cache = blockIdx.z ? value_cache : key_cache;
     for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
         const int64_t src = __ldg(pairs + 2 * (int64_t)pi);
@@ -125,11 +130,19 @@ extern "C" int pkv_reshape_and_cache(const void *key, const void *value, void *k
     const int64_t num_vecs = (int64_t)num_tokens * heads_x_vecs;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((num_vecs + threads - 1) / threads, 65536);
-    reshape_and_cache_kernel<<<(unsigned)blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), static_cast<uint4 *>(key_cache),
-        static_cast<uint4 *>(value_cache), slot_mapping, num_vecs, (int)heads_x_vecs, vpr, block_size,
-        (int64_t)num_blocks * block_size, dev_status);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    // kernel arguments (non-const locals: launch_pdl takes their addresses)
+    const uint4 *k4 = static_cast<const uint4 *>(key), *v4 = static_cast<const uint4 *>(value);
+    uint4 *kc4 = static_cast<uint4 *>(key_cache), *vc4 = static_cast<uint4 *>(value_cache);
+    const int64_t *slots = slot_mapping;
+    int64_t nv = num_vecs, num_slots = (int64_t)num_blocks * block_size;
+    int hxv = (int)heads_x_vecs, vr = vpr, bsz = block_size;
+    int32_t *st = dev_status;
+    void *args[] = {&k4, &v4, &kc4, &vc4, &slots, &nv, &hxv, &vr, &bsz, &num_slots, &st};
+    if (launch_pdl(reinterpret_cast<const void *>(&reshape_and_cache_kernel), dim3((unsigned)blocks), dim3(threads),
+                   0, stream, args) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
     return PKV_OK;
 }
 
@@ -144,12 +157,17 @@ extern "C" int pkv_copy_blocks(void *key_cache, void *value_cache, const int64_t
     // about 4 vectors per thread per pair, at most 64 CTAs per block
     const int64_t gx = std::max<int64_t>(1, std::min<int64_t>(64, (vpb + 4 * threads - 1) / (4 * threads)));
     const int gy = std::min(num_pairs, 65535);
-    copy_blocks_kernel<<<dim3((unsigned)gx, (unsigned)gy, 2), threads, 0,
-                         reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<uint4 *>(key_cache),
-                                                                    static_cast<uint4 *>(value_cache),
-                                                                    block_pairs, num_pairs, vpb, num_blocks,
-                                                                    dev_status);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    uint4 *kc4 = static_cast<uint4 *>(key_cache), *vc4 = static_cast<uint4 *>(value_cache);
+    const int64_t *pairs = block_pairs;
+    int64_t vpb_arg = vpb;
+    int np = num_pairs, nb = num_blocks;
+    int32_t *st = dev_status;
+    void *args[] = {&kc4, &vc4, &pairs, &np, &vpb_arg, &nb, &st};
+    if (launch_pdl(reinterpret_cast<const void *>(&copy_blocks_kernel), dim3((unsigned)gx, (unsigned)gy, 2),
+                   dim3(threads), 0, stream, args) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
     return PKV_OK;
 }
 

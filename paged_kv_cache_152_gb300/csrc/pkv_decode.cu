@@ -13,6 +13,7 @@
 
 #include "../../include/pkv.h"
 #include "pkv_decode_impl.cuh"
+#include "pkv_launch.h"
 
 namespace pkv {
 
@@ -242,9 +243,8 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.wait_limit_ns = kWaitLimitNs;
 
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     void *args[] = {&p};
-    if (cudaLaunchKernel(r.info.fn, dim3(r.ctas), dim3(r.info.threads), args, r.smem, st) != cudaSuccess) {
+    if (launch_pdl(r.info.fn, dim3(r.ctas), dim3(r.info.threads), r.smem, stream, args) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }

@@ -408,6 +408,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         prefetch_tensormap(&p.tmap_k8);
         prefetch_tensormap(&p.tmap_v8);
     }
+    grid_dependency_wait();
+    launch_dependents();
 
     // ---- prologue: chunk counts per sequence and their prefix sums ----------
     const int per = (N + NW * 32 - 1) / (NW * 32);

@@ -157,6 +157,14 @@ __device__ __forceinline__ float2 unpack_half2(uint32_t v) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&v));
 }
 
+// Programmatic dependent launch: kernels of this library are launched so that
+// they may start while the previous kernel on the stream finishes; each calls
+// grid_dependency_wait() before its first global-memory access, which waits
+// for that kernel to complete and its writes to be visible -- the same
+// ordering as a plain stream, minus the launch gap.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 8 fp16 values packed in 16 bytes -> 8 floats.
 __device__ __forceinline__ void unpack8(const uint4 &raw, float (&f)[8]) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
