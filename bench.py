@@ -72,9 +72,13 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     p.add_argument("--config", choices=list(WORKLOAD_TEXT), default="7b")
     p.add_argument("--num-ctas", type=int, default=0)
+    p.add_argument("--block-size", type=int, default=0,
+                   help="override the workload's block size (8, 16, 32, 64, 128): the block-size sweep")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--fused-append", action="store_true",
+                   help="one launch per step: the decode launch writes the new tokens itself")
     p.add_argument("--no-graph", action="store_true",
                    help="launch every step directly instead of replaying captured CUDA graphs")
     p.add_argument("--identity-tables", action="store_true",
@@ -228,14 +232,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the product arm
 
-def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0):
+def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0, block_size=0):
     """Allocator + device tensors of a workload at its decode step."""
     import numpy as np
     import torch
     import paged_kv_cache_152_gb300 as pkv
     import workloads as W
 
-    wl = W.make(cfg)
+    wl = W.make(cfg, block_size=block_size) if block_size else W.make(cfg)
     n = wl.num_seqs
     extra = n * (-(-e2e_headroom_steps // wl.block_size) + 1) if e2e_headroom_steps else 0
     nb = wl.num_blocks + extra
@@ -268,16 +272,23 @@ def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0):
 
 
 def write_step(pkv, st):
-    """copy_blocks (if the step has copy-on-write pairs), then reshape_and_cache."""
+    """copy_blocks (if the step has copy-on-write pairs), then reshape_and_cache
+    (unless the decode launch appends the new tokens itself)."""
     t = st["t"]
     if st["pairs"].shape[0]:
         pkv.copy_blocks(t["key_cache"], t["value_cache"], st["pairs"], status=st["status"])
-    pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"], st["slots"],
-                          status=st["status"])
+    if not st.get("fused"):
+        pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"], st["slots"],
+                              status=st["status"])
 
 
 def decode_step(pkv, st, ws, num_ctas):
     t = st["t"]
+    if st.get("fused"):
+        pkv.paged_attention_decode_append(st["out"], t["query"], t["key"], t["value"], t["key_cache"],
+                                          t["value_cache"], st["tables"], st["lens"], st["wl"].scale,
+                                          num_ctas=num_ctas, workspace=ws, status=st["status"])
+        return
     pkv.paged_attention_decode(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"],
                                st["lens"], st["wl"].scale, num_ctas=num_ctas, workspace=ws,
                                status=st["status"])
@@ -367,7 +378,11 @@ def run_pkv(args):
     pkv.load()
 
     e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-    st = build_state(args.config, device, args.identity_tables, e2e_headroom_steps=e2e_steps)
+    st = build_state(args.config, device, args.identity_tables, e2e_headroom_steps=e2e_steps,
+                     block_size=args.block_size)
+    if args.fused_append:
+        st["fused"] = True
+        st["launches_per_step"] -= 1
     wl = st["wl"]
     ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
                            args.num_ctas, device)
@@ -385,14 +400,18 @@ def run_pkv(args):
     stream = torch.cuda.current_stream()
     graphs = None
     if not args.no_graph:
-        g_write, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_write, capture_error_mode="relaxed"):
-            write_step(pkv, st)
+        # (with --fused-append and no copy-on-write pairs there is no cache-write launch)
+        has_write = not (st.get("fused") and not st["pairs"].shape[0])
+        g_write, g_dec = (torch.cuda.CUDAGraph() if has_write else None), torch.cuda.CUDAGraph()
+        if has_write:
+            with torch.cuda.graph(g_write, capture_error_mode="relaxed"):
+                write_step(pkv, st)
         with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
             decode_step(pkv, st, ws, args.num_ctas)
         graphs = (g_write, g_dec)
         for _ in range(3):
-            g_write.replay()
+            if g_write is not None:
+                g_write.replay()
             g_dec.replay()
         torch.cuda.synchronize()
 
@@ -410,7 +429,8 @@ def run_pkv(args):
         if graphs is None:
             launches += device_step(pkv, st, ws, args.num_ctas, dec_ev[i])
         else:
-            graphs[0].replay()
+            if graphs[0] is not None:
+                graphs[0].replay()
             dec_ev[i][0].record(stream)
             graphs[1].replay()
             dec_ev[i][1].record(stream)
@@ -458,6 +478,8 @@ def run_pkv(args):
                    "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": st["nb"],
                    "sum_context": int(sum(wl.context_lens)), "kv_bytes_per_step": kv_bytes,
+                   "paged_waste_pct": round(100 * (1 - sum(wl.context_lens) / (wl.block_size * sum(
+                       -(-c // wl.block_size) for c in wl.context_lens))), 2),
                    "tables": "identity (contiguous, in order)" if args.identity_tables else "shuffled pool",
                    "num_ctas": args.num_ctas or pkv.decode_default_ctas(wl.num_heads, wl.num_kv_heads,
                                                                         wl.head_dim, wl.block_size),
@@ -466,8 +488,10 @@ def run_pkv(args):
         "seqs_per_s_per_layer": round(world * wl.num_seqs * args.steps / (ms_total / 1e3), 1),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches * world,
-        "launch_mode": "direct binding calls" if args.no_graph else
-                       "CUDA graphs (cache write graph + decode graph replayed per step)",
+        "launch_mode": ("direct binding calls" if args.no_graph else
+                        "CUDA graphs (cache write graph + decode graph replayed per step)") +
+                       ("; decode launch appends the new tokens (no separate cache write)" if args.fused_append
+                        else ""),
         "host_us_per_step": round(host_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

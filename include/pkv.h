@@ -135,6 +135,36 @@ int pkv_paged_attention_decode(void *out, const void *query,
                                void *workspace, size_t workspace_bytes,
                                int32_t *dev_status, pkv_stream_t stream);
 
+/*
+ * pkv_paged_attention_decode_append
+ *
+ * One decode step in one launch: what pkv_reshape_and_cache of each
+ * sequence's new token followed by pkv_paged_attention_decode computes ([P1]
+ * "How PagedAttention works", steps 2-4: write the token into the next slot
+ * of the last block, then attend over the whole table).  For every sequence s
+ * with L = context_lens[s] > 0, the new token is position L-1: key[s] and
+ * value[s] ([num_kv_heads][head_dim] each) are written to that position's
+ * slot (block block_tables[s][(L-1)/block_size], offset (L-1)%block_size) of
+ * key_cache / value_cache, and attention covers positions 0..L-1 with them.
+ * No slot mapping is needed: the slot follows from the table.  Outputs and
+ * cache contents are identical to the two-call sequence.  Copy-on-write
+ * copies (pkv_copy_blocks) must still run before it.
+ *
+ *   key, value   fp16 [num_seqs][num_kv_heads][head_dim] (device)
+ *   key_cache, value_cache  written at the new tokens' slots (device)
+ * Other arguments, workspace and errors as pkv_paged_attention_decode.
+ */
+int pkv_paged_attention_decode_append(void *out, const void *query,
+                                      const void *key, const void *value,
+                                      void *key_cache, void *value_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens,
+                                      int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks,
+                                      float scale, int num_ctas,
+                                      void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, pkv_stream_t stream);
+
 /* Bytes of workspace pkv_paged_attention_decode needs (host call; queries the
  * current device's SM count when num_ctas == 0).  Returns 0 for unsupported
  * shapes. */
@@ -248,6 +278,34 @@ int pkv_copy_blocks(void *key_cache, void *value_cache,
                     const int64_t *block_pairs, int num_pairs,
                     size_t block_bytes, int num_blocks,
                     int32_t *dev_status, pkv_stream_t stream);
+
+/*
+ * Multi-layer cache ops.  [P2] "How PagedAttention works": a block holds its
+ * tokens for all layers and heads, so one slot mapping (and one list of
+ * copy-on-write pairs) serves every layer.  These do, in ONE launch, what
+ * num_layers calls of pkv_reshape_and_cache / pkv_copy_blocks would do, one
+ * per layer, with every layer's pool shaped alike.
+ *
+ *   keys, values            HOST arrays [num_layers] of device pointers, each
+ *                           fp16 [num_tokens][num_kv_heads][head_dim]
+ *   key_caches, value_caches HOST arrays [num_layers] of device pointers to
+ *                           each layer's pool (layout above)
+ *   slot_mapping, block_pairs, dev_status: device, as for the one-layer calls
+ * 1 <= num_layers <= PKV_MAX_LAYERS.  The pointer arrays are copied into the
+ * kernel's parameters; nothing is allocated.  Same errors as the one-layer
+ * calls; a NULL or misaligned pointer in an array is PKV_ERR_INVALID_ARG.
+ */
+#define PKV_MAX_LAYERS 128
+int pkv_reshape_and_cache_layers(const void *const *keys, const void *const *values,
+                                 void *const *key_caches, void *const *value_caches,
+                                 int num_layers, const int64_t *slot_mapping,
+                                 int num_tokens, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, int32_t *dev_status,
+                                 pkv_stream_t stream);
+int pkv_copy_blocks_layers(void *const *key_caches, void *const *value_caches,
+                           int num_layers, const int64_t *block_pairs, int num_pairs,
+                           size_t block_bytes, int num_blocks, int32_t *dev_status,
+                           pkv_stream_t stream);
 
 /* Host check of a pair list for pkv_copy_blocks: ids in range, destinations
  * distinct, no destination also a source.  PKV_OK or PKV_ERR_INVALID_ARG. */

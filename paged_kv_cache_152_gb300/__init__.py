@@ -44,6 +44,9 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
                                             _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size,
                                             _vp, _vp]),
+    "pkv_paged_attention_decode_append": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int,
+                                                   _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_float,
+                                                   _c_int, _vp, _c_size, _vp, _vp]),
     "pkv_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int,
                                                     _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _c_int,
@@ -53,6 +56,9 @@ SIGNATURES = {
                                        _vp, _vp]),
     "pkv_copy_blocks": (_c_int, [_vp, _vp, _vp, _c_int, _c_size, _c_int, _vp, _vp]),
     "pkv_validate_block_pairs": (_c_int, [_i64p, _c_int, _c_int]),
+    "pkv_reshape_and_cache_layers": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int,
+                                              _c_int, _vp, _vp]),
+    "pkv_copy_blocks_layers": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _c_size, _c_int, _vp, _vp]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),
     "pkv_alloc_destroy": (None, [_vp]),
     "pkv_seq_new": (_c_int, [_vp, _intp]),
@@ -191,6 +197,35 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
     return out
 
 
+def paged_attention_decode_append(out, query, key, value, key_cache, value_cache, block_tables, context_lens,
+                                  scale, num_ctas=0, workspace=None, status=None, stream=None):
+    """pkv_paged_attention_decode_append: write each sequence's new token
+    (key/value fp16 [N][Hkv][D], position context_len - 1) and attend, in one
+    launch."""
+    torch = _need(query, __import__("torch").float16, "query", 3)
+    _need(key, torch.float16, "key", 3)
+    _need(value, torch.float16, "value", 3)
+    _need(out, torch.float16, "out", 3)
+    _need(key_cache, torch.float16, "key_cache", 4)
+    _need(value_cache, torch.float16, "value_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    n, h, d = query.shape
+    nb, hkv, bs, d2 = key_cache.shape
+    if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
+            or tuple(key.shape) != (n, hkv, d) or tuple(value.shape) != (n, hkv, d) \
+            or block_tables.shape[0] != n or context_lens.shape[0] != n:
+        raise ValueError("inconsistent shapes")
+    if workspace is None:
+        workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+    rc = load().pkv_paged_attention_decode_append(
+        _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale), int(num_ctas),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_append")
+    return out
+
+
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None, stream=None):
     """pkv_reshape_and_cache: key/value fp16 [T][Hkv][D], slot_mapping int64 [T]."""
     torch = _need(key, __import__("torch").float16, "key", 3)
@@ -217,6 +252,49 @@ def copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None):
     rc = load().pkv_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_pairs), block_pairs.shape[0],
                                 block_bytes, nb, _ptr(status), _stream(stream))
     _check(rc, "pkv_copy_blocks")
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+    return arr
+
+
+def reshape_and_cache_layers(keys, values, key_caches, value_caches, slot_mapping, status=None, stream=None):
+    """pkv_reshape_and_cache_layers: lists (one entry per layer) of key/value
+    fp16 [T][Hkv][D] and pools fp16 [NB][Hkv][bs][D]; one slot mapping."""
+    torch = __import__("torch")
+    n = len(keys)
+    if not (len(values) == len(key_caches) == len(value_caches) == n) or n == 0:
+        raise ValueError("one key, value, key_cache and value_cache per layer")
+    for t in list(keys) + list(values):
+        _need(t, torch.float16, "key/value", 3)
+    for t in list(key_caches) + list(value_caches):
+        _need(t, torch.float16, "cache", 4)
+        if tuple(t.shape) != tuple(key_caches[0].shape):
+            raise ValueError("every layer's pool must have the same shape")
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    t_, hkv, d = keys[0].shape
+    nb, _, bs, _ = key_caches[0].shape
+    ka, va, kca, vca = _ptr_array(keys), _ptr_array(values), _ptr_array(key_caches), _ptr_array(value_caches)
+    rc = load().pkv_reshape_and_cache_layers(ka, va, kca, vca, n, _ptr(slot_mapping), t_, hkv, d, bs, nb,
+                                             _ptr(status), _stream(stream))
+    _check(rc, "pkv_reshape_and_cache_layers")
+
+
+def copy_blocks_layers(key_caches, value_caches, block_pairs, status=None, stream=None):
+    """pkv_copy_blocks_layers: the same (src, dst) pairs in every layer's pool."""
+    torch = __import__("torch")
+    n = len(key_caches)
+    if len(value_caches) != n or n == 0:
+        raise ValueError("one key_cache and value_cache per layer")
+    for t in list(key_caches) + list(value_caches):
+        _need(t, torch.float16, "cache", 4)
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    nb = key_caches[0].shape[0]
+    block_bytes = key_caches[0][0].numel() * key_caches[0].element_size()
+    rc = load().pkv_copy_blocks_layers(_ptr_array(key_caches), _ptr_array(value_caches), n, _ptr(block_pairs),
+                                       block_pairs.shape[0], block_bytes, nb, _ptr(status), _stream(stream))
+    _check(rc, "pkv_copy_blocks_layers")
 
 
 def validate_block_pairs(pairs, num_blocks):

@@ -181,13 +181,16 @@ extern "C" int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head
     return r.ctas;
 }
 
-extern "C" int pkv_paged_attention_decode(void *out, const void *query, const void *key_cache,
-                                          const void *value_cache, const int32_t *block_tables,
-                                          int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                                          int num_heads, int num_kv_heads, int head_dim, int block_size,
-                                          int num_blocks, float scale, int num_ctas, void *workspace,
-                                          size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream) {
+namespace {
+
+int decode_impl(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
+                const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                int32_t *dev_status, pkv_stream_t stream) {
     if (num_seqs == 0) return PKV_OK;
+    if ((new_key == nullptr) != (new_value == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (new_key && (!aligned16(new_key) || !aligned16(new_value))) return PKV_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks_per_seq < 1 || num_blocks < 1 || num_ctas < 0)
         return PKV_ERR_INVALID_ARG;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens || !workspace)
@@ -228,6 +231,10 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     p.query = static_cast<const __half *>(query);
     p.key_cache = static_cast<const __half *>(key_cache);
     p.value_cache = static_cast<const __half *>(value_cache);
+    p.new_key = static_cast<const __half *>(new_key);
+    p.new_value = static_cast<const __half *>(new_value);
+    p.key_cache_w = static_cast<__half *>(const_cast<void *>(key_cache));
+    p.value_cache_w = static_cast<__half *>(const_cast<void *>(value_cache));
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml);
@@ -250,4 +257,31 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
     }
 
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_attention_decode(void *out, const void *query, const void *key_cache,
+                                          const void *value_cache, const int32_t *block_tables,
+                                          int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                          int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, int num_ctas, void *workspace,
+                                          size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream) {
+    return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                       num_ctas, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" int pkv_paged_attention_decode_append(void *out, const void *query, const void *key,
+                                                 const void *value, void *key_cache, void *value_cache,
+                                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                                 const int32_t *context_lens, int num_seqs, int num_heads,
+                                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                                 float scale, int num_ctas, void *workspace,
+                                                 size_t workspace_bytes, int32_t *dev_status,
+                                                 pkv_stream_t stream) {
+    if (num_seqs > 0 && (!key || !value)) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                       num_ctas, workspace, workspace_bytes, dev_status, stream);
 }

@@ -73,6 +73,8 @@ struct DecodeGeometry {
     static constexpr int kTileBytes = kHalves * kHalfBytes;  // K (or V) rows of a chunk
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = G * D * 2;         // query rows of a KV group
+    static constexpr int kRowBytes = D * 2;           // one K (or V) row
+    static constexpr int kSlotBytes = kQBytes + 2 * kRowBytes;  // + the new token's K and V rows
     static constexpr int kKSteps = D / 16;            // mma K steps of Q.K^T
     static constexpr int kDTiles = D / 8;             // mma N tiles of P.V
     static constexpr int kBoxBytes = 8 * 128;         // one TMA box: 8 rows x 64 fp16
@@ -83,14 +85,14 @@ struct DecodeGeometry {
 };
 
 // Dynamic shared memory (from a 1024-byte aligned base):
-// [stages][query slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)].
+// [stages][query + new-row slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)].
 template <int NW, int ST, int D, int BS, int G>
 struct DecodeSmem {
     using Geo = DecodeGeometry<D, BS, G>;
     static constexpr size_t kQ = (size_t)NW * ST * Geo::kStageBytes;
-    static constexpr size_t kBars = kQ + (size_t)NW * ST * Geo::kQBytes;
+    static constexpr size_t kBars = kQ + (size_t)NW * ST * Geo::kSlotBytes;
     static constexpr size_t kMeta = kBars + (size_t)NW * ST * 8;
-    static constexpr size_t kCum = kMeta + (size_t)NW * ST * 16;
+    static constexpr size_t kCum = kMeta + (size_t)NW * ST * 32;  // two int4 per stage
     static constexpr size_t kAlign = 1024;              // slack for aligning the base
     static constexpr size_t kFixed = kCum + kAlign;
     static constexpr size_t kPerSeq = 8;
@@ -504,10 +506,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
-    const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kQBytes;
+    const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kSlotBytes;
     const uint32_t wq_a = smem_addr(wq);
     const uint32_t bar_a = smem_addr(bars + warp * ST);
-    int4 *wmeta = meta + warp * ST;
+    int4 *wmeta = meta + 2 * warp * ST;
+    const bool append = p.new_key != nullptr;
 
     // the walk: cut pieces first (see share_order)
     const ShareOrder order = share_order(cum, N, Hkv, gb, ge);
@@ -544,19 +547,23 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             }
             const int stage = i % ST;
             const int rows = chunk_rows(pos.c, ctx[pos.s], Geo::kRows);
-            const int flags = chunk_flags(pos, g, gb, ge);
-            wmeta[stage] = make_int4(pos.s, pos.kvh, rows, flags);
+            // the decode step's new token is the last row of the segment's last chunk
+            const bool new_row = append && pos.c == pos.nch - 1;
+            const int flags = chunk_flags(pos, g, gb, ge) | (new_row ? kAppendRow : 0);
             const uint32_t bar = bar_a + stage * 8;
             const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
             const uint32_t vdst = kdst + Geo::kTileBytes;
             // a whole chunk is one box per cache; a last chunk of at most 8 rows
             // of a 16-row chunk takes one 8-row box per half instead
             const bool short_box = Geo::kNT == 2 && rows <= 8;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, (short_box ? 2 * Geo::kHalves * Geo::kBoxBytes : 2 * Geo::kTileBytes) +
-                                           ((flags & kFirst) ? Geo::kQBytes : 0));
             // row of the cache viewed as [num_blocks * Hkv * BS rows]
             const int y = (int)(((int64_t)phys * Hkv + pos.kvh) * BS + (pos.c * Geo::kRows) % BS);
+            wmeta[2 * stage] = make_int4(pos.s, pos.kvh, rows, flags);
+            wmeta[2 * stage + 1] = make_int4(y, 0, 0, 0);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, (short_box ? 2 * Geo::kHalves * Geo::kBoxBytes : 2 * Geo::kTileBytes) +
+                                           ((flags & kFirst) ? Geo::kQBytes : 0) +
+                                           (new_row ? 2 * Geo::kRowBytes : 0));
             if (!short_box) {
                 tma_load_3d(kdst, &p.tmap_k, 0, y, 0, bar);
                 tma_load_3d(vdst, &p.tmap_v, 0, y, 0, bar);
@@ -568,8 +575,14 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
                 }
             }
             if (flags & kFirst)
-                bulk_g2s(wq_a + stage * Geo::kQBytes, p.query + ((int64_t)pos.s * p.num_heads + pos.kvh * G) * D,
-                         Geo::kQBytes, bar);
+                bulk_g2s(wq_a + stage * Geo::kSlotBytes,
+                         p.query + ((int64_t)pos.s * p.num_heads + pos.kvh * G) * D, Geo::kQBytes, bar);
+            if (new_row) {
+                const int64_t src = ((int64_t)pos.s * Hkv + pos.kvh) * D;
+                bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
+                bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes + Geo::kRowBytes, p.new_value + src,
+                         Geo::kRowBytes, bar);
+            }
         }
     };
 
@@ -599,10 +612,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             exit_warp();
             return;
         }
-        const int4 md = wmeta[stage];
+        const int4 md = wmeta[2 * stage];
         if (md.w & kFirst) {
             // query rows of the group as mma A fragments (rows g >= G stay 0)
-            const unsigned char *sq = wq + stage * Geo::kQBytes;
+            const unsigned char *sq = wq + stage * Geo::kSlotBytes;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
@@ -615,6 +628,24 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         }
         if (md.z < Geo::kRows) zero_tail_rows<D, BS, G>(wst + stage * Geo::kStageBytes + Geo::kTileBytes, md.z, lane);
+        if (md.w & kAppendRow) {
+            // the new token (row md.z - 1): into the swizzled tiles for this
+            // step, and into the cache for the steps after it
+            constexpr int kVecs = D / 8;  // 16-byte pieces of a row
+            const int r = md.z - 1;
+            if (lane < 2 * kVecs) {
+                const int v = lane % kVecs;
+                const bool is_v = lane >= kVecs;
+                const uint4 val = *reinterpret_cast<const uint4 *>(wq + stage * Geo::kSlotBytes + Geo::kQBytes +
+                                                                   (is_v ? Geo::kRowBytes : 0) + v * 16);
+                unsigned char *tile = wst + stage * Geo::kStageBytes + (is_v ? Geo::kTileBytes : 0);
+                *reinterpret_cast<uint4 *>(tile + (v >> 3) * Geo::kHalfBytes + r * 128 + (((v & 7) ^ (r & 7)) << 4)) =
+                    val;
+                __half *cache = is_v ? p.value_cache_w : p.key_cache_w;
+                *reinterpret_cast<uint4 *>(cache + ((int64_t)wmeta[2 * stage + 1].x + r) * D + v * 8) = val;
+            }
+            __syncwarp();
+        }
         const uint32_t kt = wst_a + stage * Geo::kStageBytes;
         consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
         // refill the stage first: a piece's finish (and a cut piece's count and

@@ -21,6 +21,10 @@ struct DecodeParams {
     const __half *query;          // [N][H][D]
     const __half *key_cache;      // [NB][Hkv][BS][D]
     const __half *value_cache;    // [NB][Hkv][BS][D]
+    const __half *new_key;        // [N][Hkv][D] new token per sequence (NULL: no append)
+    const __half *new_value;      // [N][Hkv][D]
+    __half *key_cache_w;          // the caches, for writing the new tokens' rows
+    __half *value_cache_w;
     const int32_t *block_tables;  // [N][MB]
     const int32_t *context_lens;  // [N]
     float *ws_ml;                 // [W][2][G][2] partial (max, sum)

@@ -37,7 +37,8 @@ enum ChunkFlags {
     kFirst = 1,   // first chunk of a piece: reset the softmax state, q arrives
     kLast = 2,    // last chunk of a piece: finish it
     kWhole = 4,   // the piece is a whole segment: write the output row directly
-    kSlot1 = 8    // partial goes to slot 1 (else slot 0)
+    kSlot1 = 8,   // partial goes to slot 1 (else slot 0)
+    kAppendRow = 16  // (set by the kernel) the chunk's last row is the decode step's new token
 };
 
 PKV_HD int chunks_for(int ctx, int rows_per_chunk) {

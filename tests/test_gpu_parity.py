@@ -339,3 +339,80 @@ def test_workspace_contents_do_not_matter(pkv):
         torch.cuda.synchronize()
         assert int(case.status.item()) == 0
         assert max_abs_err(out, ref) <= TOL, (g, max_abs_err(out, ref))
+
+
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
+def test_block_size_sweep_full_size(pkv, bs):
+    """The 7B-class workload at every supported block size ([P1] 'Worked
+    example': the block-size trade-off), sampled rows against the oracle."""
+    wl = W.make("7b", block_size=bs)
+    case = Case(wl)
+    _full_check(case, sample_seqs(wl, 8, seed=bs))
+
+
+def test_reshape_and_cache_layers_bit_exact(pkv):
+    """One launch writes every layer's new tokens ([P2]: a block spans all layers)."""
+    rng = np.random.default_rng(12)
+    L, nb, hkv, bs, d, t = 5, 12, 4, 16, 128, 21
+    dev = "cuda"
+    slots = rng.permutation(nb * bs)[:t].astype(np.int64)
+    slots[4] = -1
+    kcs = [rng.standard_normal((nb, hkv, bs, d)).astype(np.float16) for _ in range(L)]
+    vcs = [rng.standard_normal((nb, hkv, bs, d)).astype(np.float16) for _ in range(L)]
+    keys = [rng.standard_normal((t, hkv, d)).astype(np.float16) for _ in range(L)]
+    vals = [rng.standard_normal((t, hkv, d)).astype(np.float16) for _ in range(L)]
+    g_kc = [torch.from_numpy(x).to(dev) for x in kcs]
+    g_vc = [torch.from_numpy(x).to(dev) for x in vcs]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.reshape_and_cache_layers([torch.from_numpy(x).to(dev) for x in keys],
+                                 [torch.from_numpy(x).to(dev) for x in vals], g_kc, g_vc,
+                                 torch.from_numpy(slots).to(dev), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for layer in range(L):
+        OC.reshape_and_cache(keys[layer], vals[layer], kcs[layer], vcs[layer], slots)
+        assert np.array_equal(bits16(g_kc[layer]), bits16(kcs[layer]))
+        assert np.array_equal(bits16(g_vc[layer]), bits16(vcs[layer]))
+
+
+def test_copy_blocks_layers_bit_exact(pkv):
+    rng = np.random.default_rng(13)
+    L, nb, hkv, bs, d = 3, 10, 2, 16, 64
+    dev = "cuda"
+    kcs = [rng.standard_normal((nb, hkv, bs, d)).astype(np.float16) for _ in range(L)]
+    vcs = [rng.standard_normal((nb, hkv, bs, d)).astype(np.float16) for _ in range(L)]
+    pairs = [(1, 7), (3, 0), (5, 9)]
+    assert pkv.validate_block_pairs(pairs, nb)
+    g_kc = [torch.from_numpy(x).to(dev) for x in kcs]
+    g_vc = [torch.from_numpy(x).to(dev) for x in vcs]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.copy_blocks_layers(g_kc, g_vc, torch.tensor(pairs, dtype=torch.int64, device=dev), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for layer in range(L):
+        OC.copy_blocks(kcs[layer], vcs[layer], pairs)
+        assert np.array_equal(bits16(g_kc[layer]), bits16(kcs[layer]))
+        assert np.array_equal(bits16(g_vc[layer]), bits16(vcs[layer]))
+
+
+@pytest.mark.parametrize("name,kw", [("tiny", {}), ("7b", dict(num_seqs=11)), ("gqa", dict(num_seqs=9)),
+                                     ("chat", dict(num_main=5, num_transient=4)), ("7b", {})])
+@pytest.mark.parametrize("num_ctas", [0, 3])
+def test_decode_append_equals_write_then_decode(pkv, name, kw, num_ctas):
+    """The fused append + attend launch gives the same cache bits and the same
+    output bits as reshape_and_cache followed by decode, and matches the oracle."""
+    wl = W.make(name, **kw)
+    fused, split = Case(wl), Case(wl)
+    pkv.paged_attention_decode_append(fused.out, fused.t["query"], fused.t["key"], fused.t["value"],
+                                      fused.t["key_cache"], fused.t["value_cache"], fused.tables, fused.lens,
+                                      wl.scale, num_ctas=num_ctas, status=fused.status)
+    split.write_new_tokens()
+    split.decode(num_ctas)
+    torch.cuda.synchronize()
+    assert int(fused.status.item()) == 0 and int(split.status.item()) == 0
+    assert torch.equal(fused.t["key_cache"].view(torch.int16), split.t["key_cache"].view(torch.int16))
+    assert torch.equal(fused.t["value_cache"].view(torch.int16), split.t["value_cache"].view(torch.int16))
+    assert torch.equal(fused.out.view(torch.int16), split.out.view(torch.int16))
+    seqs = sample_seqs(wl, 8) if wl.num_seqs > 16 else None
+    fused.oracle_write_new_tokens()
+    assert max_abs_err(fused.out, fused.oracle_decode(seqs), seqs) <= TOL

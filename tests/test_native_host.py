@@ -62,7 +62,16 @@ def test_schedule_exhaustive(tmp_path):
     assert "schedule ok" in r.stdout
 
 
-def test_decode_rejects_bad_arguments_on_host(lib):
+@pytest.fixture
+def no_gpu():
+    """Host-validation tests pass fake device pointers that must be rejected
+    before any launch; never run them where a launch could reach a GPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake-pointer host checks run on GPU-less hosts only")
+
+
+def test_decode_rejects_bad_arguments_on_host(lib, no_gpu):
     import ctypes
     vp = ctypes.c_void_p(256)    # never dereferenced: validation fails first
     call = lambda **kw: lib.pkv_paged_attention_decode(  # noqa: E731
@@ -82,7 +91,7 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert call(out=ctypes.c_void_p(258)) == pkv.PKV_ERR_INVALID_ARG  # misaligned
 
 
-def test_cache_ops_reject_bad_arguments_on_host(lib):
+def test_cache_ops_reject_bad_arguments_on_host(lib, no_gpu):
     import ctypes
     import paged_kv_cache_152_gb300 as pkv
     vp = ctypes.c_void_p(256)
@@ -103,3 +112,22 @@ def test_validate_block_pairs(lib):
     assert not pkv.validate_block_pairs([(1, 2), (2, 4)], 8)   # destination is also a source
     assert not pkv.validate_block_pairs([(1, 8)], 8)           # outside the pool
     assert not pkv.validate_block_pairs([(-1, 3)], 8)
+
+
+def test_multi_layer_ops_reject_bad_arguments_on_host(lib, no_gpu):
+    import ctypes
+    import paged_kv_cache_152_gb300 as pkv
+    vp = ctypes.c_void_p(256)
+    good = (ctypes.c_void_p * 2)(256, 512)
+    bad = (ctypes.c_void_p * 2)(256, None)
+    odd = (ctypes.c_void_p * 2)(256, 520)
+    f = lib.pkv_reshape_and_cache_layers
+    assert f(good, good, good, good, 2, vp, 0, 8, 64, 16, 4, None, None) == pkv.PKV_OK   # no tokens
+    assert f(good, good, good, good, 0, vp, 3, 8, 64, 16, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(good, good, good, good, 129, vp, 3, 8, 64, 16, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(good, bad, good, good, 2, vp, 3, 8, 64, 16, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(good, good, odd, good, 2, vp, 3, 8, 64, 16, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    g = lib.pkv_copy_blocks_layers
+    assert g(good, good, 2, vp, 0, 4096, 4, None, None) == pkv.PKV_OK
+    assert g(good, bad, 2, vp, 1, 4096, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert g(good, good, 2, vp, 1, 4001, 4, None, None) == pkv.PKV_ERR_INVALID_ARG

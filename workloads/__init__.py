@@ -108,9 +108,9 @@ def _simple(name, index, lens, heads, kv_heads, head_dim, block_size, pool=None)
                     1.0 / math.sqrt(head_dim), BASE_SEED + index)
 
 
-def tiny():
-    wl = _simple("tiny", 0, [40, 17, 100, 5], 8, 8, 64, 16, pool=64)
-    return wl
+def tiny(block_size=16):
+    pool = 64 if block_size == 16 else None
+    return _simple("tiny", 0, [40, 17, 100, 5], 8, 8, 64, block_size, pool=pool)
 
 
 def decode_7b(num_seqs=64, block_size=16):
