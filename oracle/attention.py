@@ -19,7 +19,7 @@ paged_vs_contiguous.py example on [P1] maps token 37 to logical block 2,
 offset 5).  [P2] "How PagedAttention works": within a block, tokens are laid
 out contiguously.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * cache layout [num_blocks][num_kv_heads][block_size][head_dim];
 * grouped-query attention: query head h reads KV head h // (H / H_kv);
 * context_len == 0 gives an all-zero output row;

@@ -14,6 +14,11 @@ shared block to a fresh block before the writer's token goes in.  The oracle
 copies every byte of the block (all heads, all slots) in both caches; the
 copied fill count travels with the block ([P1] practice listing).
 
+swap_blocks.  [P2] "Why it matters for KV cache", "Swapping and preemption":
+blocks are evicted to CPU memory and fetched back.  The oracle copies every
+byte of each listed block from one pool to the other (both caches); the block
+manager decides which blocks move where.
+
 valid_slot_mask.  The token positions a batch of sequences actually uses; the
 tests poison every other slot of the pool with NaN so that any read outside a
 sequence's context shows up in the output.
@@ -58,6 +63,17 @@ def copy_blocks(key_cache, value_cache, pairs):
             raise ValueError(f"pair ({src}, {dst}) outside the pool")
         key_cache[dst] = key_cache[src]
         value_cache[dst] = value_cache[src]
+
+
+def swap_blocks(src_key, src_value, dst_key, dst_value, pairs):
+    """For each (src, dst) pair copy block src of the source pool over block
+    dst of the destination pool, in place, in order.  Bit-exact copies."""
+    for src, dst in pairs:
+        src, dst = int(src), int(dst)
+        if not (0 <= src < src_key.shape[0] and 0 <= dst < dst_key.shape[0]):
+            raise ValueError(f"pair ({src}, {dst}) outside a pool")
+        dst_key[dst] = src_key[src]
+        dst_value[dst] = src_value[src]
 
 
 def valid_slot_mask(block_tables, context_lens, num_blocks, block_size):
