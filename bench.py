@@ -83,6 +83,8 @@ def parse_args(argv=None):
                    help="launch every step directly instead of replaying captured CUDA graphs")
     p.add_argument("--identity-tables", action="store_true",
                    help="same workload with each sequence's blocks contiguous and in order")
+    p.add_argument("--swap", action="store_true",
+                   help="measure swapping instead: every sequence's blocks device -> pinned host -> device")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -515,6 +517,90 @@ def run_pkv(args):
     return line
 
 
+def run_swap(args):
+    """Swapping, measured on its own: the block manager swaps every sequence
+    of the workload out to a page-locked host pool and back in; the kernel
+    moves the blocks (one launch per direction).  The pair lists of one
+    out/in cycle are replayed K times; the copy engine moving the same bytes
+    as ONE contiguous buffer is timed beside it as the link's reference."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_152_gb300 as pkv
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_152_gb300 import build as b
+    b.build()
+    pkv.load()
+    st = build_state(args.config, device, block_size=args.block_size)
+    wl, alloc, t = st["wl"], st["alloc"], st["t"]
+    kc, vc = t["key_cache"], t["value_cache"]
+    nh = st["nb"]
+    hk = torch.empty_like(kc, device="cpu").pin_memory()
+    hv = torch.empty_like(vc, device="cpu").pin_memory()
+    alloc.host_pool(nh)
+    h0 = time.perf_counter()
+    out_pairs = alloc.swap_out(wl.batch)
+    h1 = time.perf_counter()
+    in_pairs = alloc.swap_in(wl.batch)
+    h2 = time.perf_counter()
+    d_out = torch.from_numpy(out_pairs.astype(np.int64)).to(device)
+    d_in = torch.from_numpy(in_pairs.astype(np.int64)).to(device)
+    block_bytes = kc[0].numel() * kc.element_size()
+    moved = 2 * len(out_pairs) * block_bytes
+    status = st["status"]
+    stream = torch.cuda.current_stream()
+    flat_dev = torch.empty(moved, dtype=torch.uint8, device=device)
+    flat_host = torch.empty(moved, dtype=torch.uint8).pin_memory()
+
+    def timed(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, z in evs:
+            a.record(stream)
+            fn()
+            z.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(z) for a, z in evs]
+
+    ops = {
+        "swap_out_kernel": lambda: pkv.swap_blocks(kc, vc, hk, hv, d_out, status=status),
+        "swap_in_kernel": lambda: pkv.swap_blocks(hk, hv, kc, vc, d_in, status=status),
+        "copy_engine_d2h": lambda: flat_host.copy_(flat_dev, non_blocking=True),
+        "copy_engine_h2d": lambda: flat_dev.copy_(flat_host, non_blocking=True),
+    }
+    steps = max(1, min(args.steps, 50))
+    clocks = ClockSampler(0)
+    res = {}
+    for name, fn in ops.items():
+        timed(fn, max(3, args.warmup))
+        if name == "swap_out_kernel":
+            clocks.start()
+        ms = timed(fn, steps)
+        if name == "swap_in_kernel":
+            clocks.stop()
+        res[name] = {"ms_mean": round(statistics.fmean(ms), 4), "ms_median": round(statistics.median(ms), 4),
+                     "GB/s": round(moved / (statistics.fmean(ms) / 1e3) / 1e9, 2)}
+    assert int(status.item()) == 0, pkv.status_string(int(status.item()))
+    launches = 2 * steps + 2 * max(3, args.warmup)
+    return {
+        "metric": "swap_blocks: device <-> page-locked host block copies, GB/s",
+        "value": round(2 * moved * steps / ((res["swap_out_kernel"]["ms_mean"] + res["swap_in_kernel"]["ms_mean"])
+                                            * steps / 1e3) / 1e9, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config] + "; every sequence swapped out, then in",
+                   "blocks_moved_per_direction": int(len(out_pairs)), "block_bytes_per_cache": block_bytes,
+                   "bytes_per_direction": moved},
+        "kernels": res,
+        "kernel_vs_copy_engine": {
+            "out": round(res["swap_out_kernel"]["GB/s"] / res["copy_engine_d2h"]["GB/s"], 3),
+            "in": round(res["swap_in_kernel"]["GB/s"] / res["copy_engine_h2d"]["GB/s"], 3)},
+        "block_manager_us": {"swap_out": round((h1 - h0) * 1e6, 1), "swap_in": round((h2 - h1) * 1e6, 1)},
+        "gpu_launches": launches,
+        "clocks": clocks.finish(),
+    }
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 
@@ -652,6 +738,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.swap:
+        line = run_swap(args)
     else:
         line = run_pkv(args)
     if line is not None:

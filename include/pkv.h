@@ -65,7 +65,8 @@ typedef enum pkv_status {
     PKV_ERR_DEVICE_TIMEOUT = 4,  /* device: a bounded wait gave up (status word only) */
     PKV_ERR_OUT_OF_RANGE = 5,    /* device: slot / table entry / context outside the pool or table */
     PKV_ERR_NOT_FOUND = 6,       /* block manager: unknown or released sequence id */
-    PKV_ERR_UNSUPPORTED = 7      /* shape not compiled into this build (head_dim, block_size, group) */
+    PKV_ERR_UNSUPPORTED = 7,     /* shape not compiled into this build (head_dim, block_size, group) */
+    PKV_ERR_SWAPPED = 8          /* block manager: the sequence is swapped out (or, for a swap in, resident) */
 } pkv_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -307,6 +308,53 @@ int pkv_copy_blocks_layers(void *const *key_caches, void *const *value_caches,
                            size_t block_bytes, int num_blocks, int32_t *dev_status,
                            pkv_stream_t stream);
 
+/*
+ * pkv_swap_blocks
+ *
+ * [P2] "Why it matters for KV cache", "Swapping and preemption": blocks are
+ * evicted to CPU memory when GPU memory runs short and fetched back when the
+ * request resumes ([P1] "Common misconceptions": a technique separate from
+ * paging itself).  For each pair (src, dst) = block_pairs[2*i],
+ * block_pairs[2*i+1], copy the block_bytes bytes of block src of the SOURCE
+ * pool over block dst of the DESTINATION pool, in the key and the value
+ * pools.  Bit-exact.  Both pools have the cache layout above (block-major,
+ * block_bytes per block); one of them is normally page-locked host memory,
+ * which the kernel reads or writes directly over the CPU-GPU link (no copy
+ * engine, one launch for any number of scattered blocks).
+ *
+ *   src_key, src_value    source pools: device memory of the current device
+ *                         or page-locked host memory (cudaHostAlloc,
+ *                         cudaHostRegister); src_num_blocks blocks each
+ *   dst_key, dst_value    destination pools, same rules; dst_num_blocks
+ *   block_pairs           int64 [num_pairs][2] (device-accessible): (source
+ *                         block, destination block), e.g. the pairs of
+ *                         pkv_swap_out (device -> host) or pkv_swap_in
+ *                         (host -> device)
+ *   block_bytes           bytes of one block in one cache; multiple of 16
+ *   dev_status            a pair outside either pool sets
+ *                         PKV_ERR_OUT_OF_RANGE and is skipped
+ * Pageable (unregistered) host memory, or another device's memory, is
+ * PKV_ERR_INVALID_ARG before anything is launched (the pointer attributes are
+ * queried on the host; on a machine without a GPU that query fails with
+ * PKV_ERR_CUDA).  Destination blocks must be pairwise distinct and must not
+ * overlap the source blocks of the same call.  num_pairs == 0 launches
+ * nothing.
+ */
+int pkv_swap_blocks(const void *src_key, const void *src_value,
+                    void *dst_key, void *dst_value,
+                    const int64_t *block_pairs, int num_pairs, size_t block_bytes,
+                    int src_num_blocks, int dst_num_blocks,
+                    int32_t *dev_status, pkv_stream_t stream);
+
+/* pkv_swap_blocks for every layer in one launch: HOST arrays [num_layers] of
+ * pool pointers (each under the rules above), one pair list for all layers
+ * (a block id spans all layers).  1 <= num_layers <= PKV_MAX_LAYERS. */
+int pkv_swap_blocks_layers(const void *const *src_keys, const void *const *src_values,
+                           void *const *dst_keys, void *const *dst_values, int num_layers,
+                           const int64_t *block_pairs, int num_pairs, size_t block_bytes,
+                           int src_num_blocks, int dst_num_blocks,
+                           int32_t *dev_status, pkv_stream_t stream);
+
 /* Host check of a pair list for pkv_copy_blocks: ids in range, destinations
  * distinct, no destination also a source.  PKV_OK or PKV_ERR_INVALID_ARG. */
 int pkv_validate_block_pairs(const int64_t *host_pairs, int num_pairs,
@@ -342,6 +390,26 @@ int pkv_validate_block_pairs(const int64_t *host_pairs, int num_pairs,
  *   - Sequence ids are handed out 0, 1, 2, ... and never reused.
  * An operation that needs more free blocks than there are returns
  * PKV_ERR_OUT_OF_BLOCKS and changes nothing.  The object is not thread-safe.
+ *
+ * Swapping ([P2] "Why it matters for KV cache", "Swapping and preemption";
+ * [P1] "Common misconceptions").  An optional second pool of host blocks
+ * (pkv_alloc_host_pool) with its own FIFO free list, counts and fills:
+ *   - Swap out of a group of distinct resident sequences: every distinct
+ *     device block the group holds gets one host block, in order of first
+ *     appearance (sequences in the given order, each table in logical order),
+ *     with count = the group members holding it and the block's fill.  The
+ *     device block's count drops by that many; at zero it returns to the
+ *     device free list (same order).  The tables then name host blocks.
+ *   - Swap in: the mirror image, host blocks -> fresh device blocks.
+ *   - Sharing inside a group survives the round trip; sharing with sequences
+ *     outside it does not (each keeps its own copy).
+ *   - A swapped-out sequence can be released (its host blocks go back to the
+ *     host free list) or swapped in; append, fork, export and swap out return
+ *     PKV_ERR_SWAPPED.
+ *   - Each call returns the (source, destination) pairs whose data
+ *     pkv_swap_blocks must move, in allocation order, before the blocks are
+ *     used.  Out of blocks in the destination pool: PKV_ERR_OUT_OF_BLOCKS,
+ *     nothing changed.
  */
 typedef struct pkv_alloc pkv_alloc_t;
 
@@ -392,6 +460,25 @@ int pkv_block_fill(const pkv_alloc_t *a, int block, int *fill);
 int pkv_num_free(const pkv_alloc_t *a, int *num_free);
 /* The free list, front first: out [cap]; *n = its length. */
 int pkv_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n);
+
+/* Give the manager a host pool of num_host_blocks blocks; host_free_order
+ * (nullable) as for pkv_alloc_create.  Allowed while no host block is in use
+ * (replaces the previous host pool). */
+int pkv_alloc_host_pool(pkv_alloc_t *a, int num_host_blocks,
+                        const int32_t *host_free_order);
+/* Swap out / in n distinct sequences seqs[0..n).  pairs_out [cap][2] receives
+ * the (source, destination) pairs, *n_pairs their count; cap must be at least
+ * the total table length of the group (else PKV_ERR_INVALID_ARG, nothing
+ * changed). */
+int pkv_swap_out(pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *pairs_out,
+                 int cap, int *n_pairs);
+int pkv_swap_in(pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *pairs_out,
+                int cap, int *n_pairs);
+int pkv_seq_swapped(const pkv_alloc_t *a, int seq, int *swapped);
+int pkv_host_block_refcount(const pkv_alloc_t *a, int block, int *refs);
+int pkv_host_block_fill(const pkv_alloc_t *a, int block, int *fill);
+int pkv_num_free_host(const pkv_alloc_t *a, int *num_free);
+int pkv_host_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n);
 
 /* ------------------------------------------------------------------------ */
 /* Self-test                                                                 */

@@ -12,8 +12,10 @@ Names mirror the C ABI without its ``pkv_`` prefix:
   context_lens, scale, ...)
 * reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, ...)
 * copy_blocks(key_cache, value_cache, block_pairs, ...)
+* swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, ...)
+* the *_layers variants, one launch for every layer's pool
 * BlockAllocator: pkv_alloc_* / pkv_seq_* / pkv_append_* / pkv_fork /
-  pkv_release / pkv_export_tables.
+  pkv_release / pkv_export_tables / pkv_swap_out / pkv_swap_in.
 """
 
 import ctypes
@@ -32,6 +34,7 @@ PKV_ERR_DEVICE_TIMEOUT = 4
 PKV_ERR_OUT_OF_RANGE = 5
 PKV_ERR_NOT_FOUND = 6
 PKV_ERR_UNSUPPORTED = 7
+PKV_ERR_SWAPPED = 8
 
 # Every symbol include/pkv.h declares, with (restype, argtypes).
 _c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
@@ -76,6 +79,17 @@ SIGNATURES = {
     "pkv_num_free": (_c_int, [_vp, _intp]),
     "pkv_free_list": (_c_int, [_vp, _i32p, _c_int, _intp]),
     "pkv_selftest_wait_timeout": (_c_int, [_vp, ctypes.c_uint64, _vp]),
+    "pkv_swap_blocks": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_size, _c_int, _c_int, _vp, _vp]),
+    "pkv_swap_blocks_layers": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_size, _c_int, _c_int,
+                                        _vp, _vp]),
+    "pkv_alloc_host_pool": (_c_int, [_vp, _c_int, _i32p]),
+    "pkv_swap_out": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
+    "pkv_swap_in": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
+    "pkv_seq_swapped": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_host_block_refcount": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_host_block_fill": (_c_int, [_vp, _c_int, _intp]),
+    "pkv_num_free_host": (_c_int, [_vp, _intp]),
+    "pkv_host_free_list": (_c_int, [_vp, _i32p, _c_int, _intp]),
 }
 
 _lib = None
@@ -88,6 +102,10 @@ class PkvError(RuntimeError):
 
 
 class OutOfBlocks(PkvError):
+    pass
+
+
+class SwappedOut(PkvError):
     pass
 
 
@@ -120,6 +138,8 @@ def status_string(status):
 def _check(status, what):
     if status == PKV_ERR_OUT_OF_BLOCKS:
         raise OutOfBlocks(status, what)
+    if status == PKV_ERR_SWAPPED:
+        raise SwappedOut(status, what)
     if status != PKV_OK:
         raise PkvError(status, what)
 
@@ -297,6 +317,58 @@ def copy_blocks_layers(key_caches, value_caches, block_pairs, status=None, strea
     _check(rc, "pkv_copy_blocks_layers")
 
 
+def _pool(t, name):
+    """A swap pool: fp16 [NB][Hkv][bs][D], contiguous, on the GPU or in
+    page-locked host memory (the library checks the pointer as well)."""
+    torch = _need(t, __import__("torch").float16, name, 4, device=False)
+    if t.device.type == "cpu" and not t.is_pinned():
+        raise ValueError(f"{name}: a host pool must be page-locked (pin_memory)")
+    return torch
+
+
+def swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, status=None, stream=None):
+    """pkv_swap_blocks: copy block src of the source pools over block dst of
+    the destination pools for each (src, dst) in block_pairs (int64 [n][2],
+    device).  One side is normally a pinned host pool."""
+    torch = _pool(src_key, "src_key")
+    for t, name in ((src_value, "src_value"), (dst_key, "dst_key"), (dst_value, "dst_value")):
+        _pool(t, name)
+    if tuple(src_key.shape[1:]) != tuple(dst_key.shape[1:]) or src_key.shape != src_value.shape \
+            or dst_key.shape != dst_value.shape:
+        raise ValueError("source and destination pools must have the same block shape")
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    block_bytes = src_key[0].numel() * src_key.element_size()
+    rc = load().pkv_swap_blocks(_ptr(src_key), _ptr(src_value), _ptr(dst_key), _ptr(dst_value),
+                                _ptr(block_pairs), block_pairs.shape[0], block_bytes, src_key.shape[0],
+                                dst_key.shape[0], _ptr(status), _stream(stream))
+    _check(rc, "pkv_swap_blocks")
+
+
+def swap_blocks_layers(src_keys, src_values, dst_keys, dst_values, block_pairs, status=None, stream=None):
+    """pkv_swap_blocks_layers: swap_blocks for every layer in one launch."""
+    torch = __import__("torch")
+    n = len(src_keys)
+    if not (len(src_values) == len(dst_keys) == len(dst_values) == n) or n == 0:
+        raise ValueError("one source and one destination pool pair per layer")
+    for t in list(src_keys) + list(src_values):
+        _pool(t, "source pool")
+        if tuple(t.shape) != tuple(src_keys[0].shape):
+            raise ValueError("every layer's source pool must have the same shape")
+    for t in list(dst_keys) + list(dst_values):
+        _pool(t, "destination pool")
+        if tuple(t.shape) != tuple(dst_keys[0].shape):
+            raise ValueError("every layer's destination pool must have the same shape")
+    if tuple(src_keys[0].shape[1:]) != tuple(dst_keys[0].shape[1:]):
+        raise ValueError("source and destination pools must have the same block shape")
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    block_bytes = src_keys[0][0].numel() * src_keys[0].element_size()
+    rc = load().pkv_swap_blocks_layers(_ptr_array(src_keys), _ptr_array(src_values), _ptr_array(dst_keys),
+                                       _ptr_array(dst_values), n, _ptr(block_pairs), block_pairs.shape[0],
+                                       block_bytes, src_keys[0].shape[0], dst_keys[0].shape[0], _ptr(status),
+                                       _stream(stream))
+    _check(rc, "pkv_swap_blocks_layers")
+
+
 def validate_block_pairs(pairs, num_blocks):
     """Host check of (src, dst) pairs for copy_blocks; True if valid."""
     a = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
@@ -426,4 +498,59 @@ class BlockAllocator:
         out = np.empty(max(self.num_blocks, 1), np.int32)
         _check(self._lib.pkv_free_list(self._h, out.ctypes.data_as(_i32p), self.num_blocks,
                                        ctypes.byref(self._i)), "pkv_free_list")
+        return out[:self._i.value].tolist()
+
+    # -- swapping ------------------------------------------------------------
+    def host_pool(self, num_host_blocks, host_free_order=None):
+        """Give the manager a pool of host blocks for swapped-out sequences."""
+        order = None
+        if host_free_order is not None:
+            self._host_order = np.ascontiguousarray(np.asarray(host_free_order, dtype=np.int32))
+            if self._host_order.shape != (int(num_host_blocks),):
+                raise ValueError("host_free_order must hold num_host_blocks entries")
+            order = self._host_order.ctypes.data_as(_i32p)
+        _check(self._lib.pkv_alloc_host_pool(self._h, int(num_host_blocks), order), "pkv_alloc_host_pool")
+        self.num_host_blocks = int(num_host_blocks)
+
+    def _move(self, fn, what, seqs):
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        cap = 0
+        for q in s.tolist():
+            _check(self._lib.pkv_seq_num_blocks(self._h, q, ctypes.byref(self._i)), "pkv_seq_num_blocks")
+            cap += self._i.value
+        pairs = np.empty((max(cap, 1), 2), dtype=np.int32)
+        _check(fn(self._h, s.ctypes.data_as(_i32p), s.shape[0], pairs.ctypes.data_as(_i32p), cap,
+                  ctypes.byref(self._i)), what)
+        return pairs[:self._i.value]
+
+    def swap_out(self, seqs):
+        """-> int32 [k][2] (device block, host block) pairs to copy."""
+        return self._move(self._lib.pkv_swap_out, "pkv_swap_out", seqs)
+
+    def swap_in(self, seqs):
+        """-> int32 [k][2] (host block, device block) pairs to copy."""
+        return self._move(self._lib.pkv_swap_in, "pkv_swap_in", seqs)
+
+    def is_swapped(self, seq):
+        _check(self._lib.pkv_seq_swapped(self._h, seq, ctypes.byref(self._i)), "pkv_seq_swapped")
+        return bool(self._i.value)
+
+    def host_refcount(self, block):
+        _check(self._lib.pkv_host_block_refcount(self._h, block, ctypes.byref(self._i)),
+               "pkv_host_block_refcount")
+        return self._i.value
+
+    def host_fill(self, block):
+        _check(self._lib.pkv_host_block_fill(self._h, block, ctypes.byref(self._i)), "pkv_host_block_fill")
+        return self._i.value
+
+    def num_free_host(self):
+        _check(self._lib.pkv_num_free_host(self._h, ctypes.byref(self._i)), "pkv_num_free_host")
+        return self._i.value
+
+    def host_free_list(self):
+        n = getattr(self, "num_host_blocks", 0)
+        out = np.empty(max(n, 1), np.int32)
+        _check(self._lib.pkv_host_free_list(self._h, out.ctypes.data_as(_i32p), n, ctypes.byref(self._i)),
+               "pkv_host_free_list")
         return out[:self._i.value].tolist()

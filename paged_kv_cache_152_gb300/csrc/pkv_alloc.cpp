@@ -7,6 +7,10 @@
 // its exercises (fork, release).  [P2] "What is PagedAttention..." (n4n.ai),
 // "How PagedAttention works": one global pool handed out block by block.
 //
+// Swapping: [P2] "Why it matters for KV cache", "Swapping and preemption";
+// [P1] "Common misconceptions".  A second pool of host blocks; a swapped-out
+// sequence's table names host blocks until it is swapped back in.
+//
 // Every operation first checks that it can complete (free blocks, ids,
 // buffer sizes) and only then mutates, so a failed call changes nothing.
 #include <cstdint>
@@ -25,8 +29,14 @@ struct pkv_alloc {
     std::vector<int32_t> fill;      // token slots written in each block
     struct Seq {
         bool alive = false;
+        bool swapped = false;        // table names host blocks
         std::vector<int32_t> table;  // logical block -> physical block
     };
+    // host pool (swapped-out sequences), same bookkeeping as the device pool
+    int num_host_blocks = 0;
+    std::deque<int32_t> host_free_list;
+    std::vector<int32_t> host_refs;
+    std::vector<int32_t> host_fill;
     std::vector<Seq> seqs;  // indexed by id; ids are never reused
 
     Seq *find(int id) {
@@ -48,7 +58,8 @@ struct pkv_alloc {
 
     int64_t length(const Seq &s) const {
         if (s.table.empty()) return 0;
-        return (int64_t)(s.table.size() - 1) * block_size + fill[s.table.back()];
+        const std::vector<int32_t> &f = s.swapped ? host_fill : fill;
+        return (int64_t)(s.table.size() - 1) * block_size + f[s.table.back()];
     }
 
     // Fresh blocks that appending n tokens to s takes: a copy-on-write of a
@@ -123,6 +134,7 @@ extern "C" int pkv_append_token(pkv_alloc_t *a, int seq, int64_t *slot_out, int3
     if (!a || !slot_out) return PKV_ERR_INVALID_ARG;
     pkv_alloc::Seq *s = a->find(seq);
     if (!s) return PKV_ERR_NOT_FOUND;
+    if (s->swapped) return PKV_ERR_SWAPPED;
     if (a->blocks_needed(*s, 1) > (int64_t)a->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
     int32_t src, dst;
     const bool shared_partial = !s->table.empty() && a->fill[s->table.back()] < a->block_size &&
@@ -141,6 +153,7 @@ extern "C" int pkv_append_tokens(pkv_alloc_t *a, int seq, int n, int64_t *slots_
     if (!a || n < 0) return PKV_ERR_INVALID_ARG;
     pkv_alloc::Seq *s = a->find(seq);
     if (!s) return PKV_ERR_NOT_FOUND;
+    if (s->swapped) return PKV_ERR_SWAPPED;
     if (a->blocks_needed(*s, n) > (int64_t)a->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
     int cows = 0;
     if (cow_pair_out) cow_pair_out[0] = cow_pair_out[1] = -1;
@@ -171,6 +184,7 @@ extern "C" int pkv_append_batch(pkv_alloc_t *a, const int32_t *seqs, int n, int6
     for (int i = 0; i < n; ++i) {
         const pkv_alloc::Seq *s = a->find(seqs[i]);
         if (!s) return PKV_ERR_NOT_FOUND;
+        if (s->swapped) return PKV_ERR_SWAPPED;
         if (seen[seqs[i]]) return PKV_ERR_INVALID_ARG;
         seen[seqs[i]] = 1;
         if (s->table.empty() || a->fill[s->table.back()] == a->block_size) {
@@ -211,6 +225,7 @@ extern "C" int pkv_append_batch(pkv_alloc_t *a, const int32_t *seqs, int n, int6
 extern "C" int pkv_fork(pkv_alloc_t *a, int parent, int *child) {
     if (!a || !child) return PKV_ERR_INVALID_ARG;
     if (!a->find(parent)) return PKV_ERR_NOT_FOUND;
+    if (a->find(parent)->swapped) return PKV_ERR_SWAPPED;
     a->seqs.emplace_back();
     pkv_alloc::Seq &c = a->seqs.back();
     const pkv_alloc::Seq &p = a->seqs[parent];  // after emplace_back: re-read
@@ -225,16 +240,21 @@ extern "C" int pkv_release(pkv_alloc_t *a, int seq, int *n_freed) {
     if (!a) return PKV_ERR_INVALID_ARG;
     pkv_alloc::Seq *s = a->find(seq);
     if (!s) return PKV_ERR_NOT_FOUND;
+    // a swapped-out sequence gives its host blocks back to the host pool
+    std::vector<int32_t> &refs = s->swapped ? a->host_refs : a->refs;
+    std::vector<int32_t> &fill = s->swapped ? a->host_fill : a->fill;
+    std::deque<int32_t> &free_list = s->swapped ? a->host_free_list : a->free_list;
     int freed = 0;
     for (int32_t b : s->table) {
-        a->refs[b] -= 1;
-        if (a->refs[b] == 0) {
-            a->fill[b] = 0;
-            a->free_list.push_back(b);
+        refs[b] -= 1;
+        if (refs[b] == 0) {
+            fill[b] = 0;
+            free_list.push_back(b);
             ++freed;
         }
     }
     s->alive = false;
+    s->swapped = false;
     std::vector<int32_t>().swap(s->table);
     if (n_freed) *n_freed = freed;
     return PKV_OK;
@@ -246,6 +266,7 @@ extern "C" int pkv_export_tables(const pkv_alloc_t *a, const int32_t *seqs, int 
     for (int i = 0; i < n; ++i) {
         const pkv_alloc::Seq *s = a->find(seqs[i]);
         if (!s) return PKV_ERR_NOT_FOUND;
+        if (s->swapped) return PKV_ERR_SWAPPED;
         if ((int64_t)s->table.size() > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
         if (a->length(*s) > INT32_MAX) return PKV_ERR_INVALID_ARG;
     }
@@ -311,6 +332,139 @@ extern "C" int pkv_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n
     if ((int64_t)a->free_list.size() > cap) return PKV_ERR_INVALID_ARG;
     int i = 0;
     for (int32_t b : a->free_list) out[i++] = b;
+    if (n) *n = i;
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Swapping
+// ---------------------------------------------------------------------------
+
+extern "C" int pkv_alloc_host_pool(pkv_alloc_t *a, int num_host_blocks, const int32_t *host_free_order) {
+    if (!a || num_host_blocks < 0) return PKV_ERR_INVALID_ARG;
+    if ((int)a->host_free_list.size() != a->num_host_blocks) return PKV_ERR_INVALID_ARG;  // host blocks in use
+    if (host_free_order) {
+        std::vector<char> seen(num_host_blocks, 0);
+        for (int i = 0; i < num_host_blocks; ++i) {
+            const int32_t b = host_free_order[i];
+            if (b < 0 || b >= num_host_blocks || seen[b]) return PKV_ERR_INVALID_ARG;
+            seen[b] = 1;
+        }
+    }
+    a->num_host_blocks = num_host_blocks;
+    a->host_refs.assign(num_host_blocks, 0);
+    a->host_fill.assign(num_host_blocks, 0);
+    a->host_free_list.clear();
+    for (int i = 0; i < num_host_blocks; ++i) a->host_free_list.push_back(host_free_order ? host_free_order[i] : i);
+    return PKV_OK;
+}
+
+namespace {
+
+// Moves the blocks of a group of sequences from one pool to the other; see
+// the rules in the header.  to_host selects the direction.
+int move_group(pkv_alloc *a, const int32_t *seqs, int n, bool to_host, int32_t *pairs_out, int cap,
+               int *n_pairs) {
+    if (!a || n < 0 || cap < 0 || (n > 0 && !seqs) || (cap > 0 && !pairs_out)) return PKV_ERR_INVALID_ARG;
+    std::vector<char> seen(a->seqs.size(), 0);
+    int64_t entries = 0;
+    for (int i = 0; i < n; ++i) {
+        const pkv_alloc::Seq *s = a->find(seqs[i]);
+        if (!s) return PKV_ERR_NOT_FOUND;
+        if (seen[seqs[i]]) return PKV_ERR_INVALID_ARG;
+        seen[seqs[i]] = 1;
+        if (s->swapped == to_host) return PKV_ERR_SWAPPED;
+        entries += (int64_t)s->table.size();
+    }
+    if (entries > cap) return PKV_ERR_INVALID_ARG;
+    std::vector<int32_t> &src_refs = to_host ? a->refs : a->host_refs;
+    std::vector<int32_t> &src_fill = to_host ? a->fill : a->host_fill;
+    std::deque<int32_t> &src_free = to_host ? a->free_list : a->host_free_list;
+    std::vector<int32_t> &dst_refs = to_host ? a->host_refs : a->refs;
+    std::vector<int32_t> &dst_fill = to_host ? a->host_fill : a->fill;
+    std::deque<int32_t> &dst_free = to_host ? a->host_free_list : a->free_list;
+    // distinct source blocks in order of first appearance, with their holders
+    std::vector<int32_t> order, holders, slot_of(src_refs.size(), -1);
+    for (int i = 0; i < n; ++i)
+        for (int32_t b : a->seqs[seqs[i]].table) {
+            if (slot_of[b] < 0) {
+                slot_of[b] = (int32_t)order.size();
+                order.push_back(b);
+                holders.push_back(0);
+            }
+            holders[slot_of[b]] += 1;
+        }
+    if (order.size() > dst_free.size()) return PKV_ERR_OUT_OF_BLOCKS;
+    std::vector<int32_t> moved(order.size());
+    for (size_t k = 0; k < order.size(); ++k) {
+        const int32_t nb = dst_free.front();
+        dst_free.pop_front();
+        dst_refs[nb] = holders[k];
+        dst_fill[nb] = src_fill[order[k]];
+        moved[k] = nb;
+        pairs_out[2 * k] = order[k];
+        pairs_out[2 * k + 1] = nb;
+    }
+    for (size_t k = 0; k < order.size(); ++k) {
+        const int32_t b = order[k];
+        src_refs[b] -= holders[k];
+        if (src_refs[b] == 0) {
+            src_fill[b] = 0;
+            src_free.push_back(b);
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        pkv_alloc::Seq &s = a->seqs[seqs[i]];
+        for (int32_t &b : s.table) b = moved[slot_of[b]];
+        s.swapped = to_host;
+    }
+    if (n_pairs) *n_pairs = (int)order.size();
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_swap_out(pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *pairs_out, int cap,
+                            int *n_pairs) {
+    return move_group(a, seqs, n, true, pairs_out, cap, n_pairs);
+}
+
+extern "C" int pkv_swap_in(pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *pairs_out, int cap,
+                           int *n_pairs) {
+    return move_group(a, seqs, n, false, pairs_out, cap, n_pairs);
+}
+
+extern "C" int pkv_seq_swapped(const pkv_alloc_t *a, int seq, int *swapped) {
+    if (!a || !swapped) return PKV_ERR_INVALID_ARG;
+    const pkv_alloc::Seq *s = a->find(seq);
+    if (!s) return PKV_ERR_NOT_FOUND;
+    *swapped = s->swapped ? 1 : 0;
+    return PKV_OK;
+}
+
+extern "C" int pkv_host_block_refcount(const pkv_alloc_t *a, int block, int *refs) {
+    if (!a || !refs || block < 0 || block >= a->num_host_blocks) return PKV_ERR_INVALID_ARG;
+    *refs = a->host_refs[block];
+    return PKV_OK;
+}
+
+extern "C" int pkv_host_block_fill(const pkv_alloc_t *a, int block, int *fill) {
+    if (!a || !fill || block < 0 || block >= a->num_host_blocks) return PKV_ERR_INVALID_ARG;
+    *fill = a->host_fill[block];
+    return PKV_OK;
+}
+
+extern "C" int pkv_num_free_host(const pkv_alloc_t *a, int *num_free) {
+    if (!a || !num_free) return PKV_ERR_INVALID_ARG;
+    *num_free = (int)a->host_free_list.size();
+    return PKV_OK;
+}
+
+extern "C" int pkv_host_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n) {
+    if (!a || cap < 0 || (cap > 0 && !out)) return PKV_ERR_INVALID_ARG;
+    if ((int64_t)a->host_free_list.size() > cap) return PKV_ERR_INVALID_ARG;
+    int i = 0;
+    for (int32_t b : a->host_free_list) out[i++] = b;
     if (n) *n = i;
     return PKV_OK;
 }

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from oracle.block_manager import BlockManagerModel, OutOfBlocks
+from oracle.block_manager import BlockManagerModel, OutOfBlocks, SwappedOut
 
 
 @pytest.fixture(scope="module")
@@ -25,9 +25,15 @@ def assert_same_state(model, alloc):
     for b in range(model.num_blocks):
         assert alloc.refcount(b) == model.refs[b], b
         assert alloc.fill(b) == model.fill[b], b
+    if model.num_host_blocks:
+        assert alloc.host_free_list() == list(model.host_free)
+        for b in range(model.num_host_blocks):
+            assert alloc.host_refcount(b) == model.host_refs[b], b
+            assert alloc.host_fill(b) == model.host_fill[b], b
     for seq, table in model.tables.items():
         assert alloc.table(seq) == table
         assert alloc.seq_len(seq) == model.seq_len(seq)
+        assert alloc.is_swapped(seq) == model.is_swapped(seq)
 
 
 def test_practice_run(pkv, golden):
@@ -183,3 +189,82 @@ def test_errors_leave_state_unchanged(pkv):
     with pytest.raises(pkv.PkvError):
         a.append_token(s)               # released
     assert a.num_free() == 4
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_operations_with_swaps_bit_exact(pkv, seed):
+    """Appends, forks, releases and group swaps in both directions; every
+    result, failure and state (both pools) identical to the oracle model."""
+    rng = np.random.default_rng(2000 + seed)
+    nb, nh = int(rng.integers(8, 40)), int(rng.integers(4, 40))
+    bs = int(rng.choice([1, 2, 4, 16]))
+    order, horder = rng.permutation(nb), rng.permutation(nh)
+    model = BlockManagerModel(nb, bs, order, nh, horder)
+    alloc = pkv.BlockAllocator(nb, bs, order)
+    alloc.host_pool(nh, horder)
+    for step in range(400):
+        live = list(model.tables)
+        op = int(rng.integers(0, 9))
+        if op == 0 or not live:
+            assert alloc.new_seq() == model.new_seq()
+            continue
+        s = int(rng.choice(live))
+        group = [int(x) for x in rng.permutation(live)[: int(rng.integers(1, min(4, len(live)) + 1))]]
+        if op <= 3:
+            n = int(rng.integers(1, 2 * bs + 2))
+            try:
+                expect = model.append_tokens(s, n)
+            except (OutOfBlocks, SwappedOut) as e:
+                with pytest.raises(pkv.OutOfBlocks if isinstance(e, OutOfBlocks) else pkv.SwappedOut):
+                    alloc.append_tokens(s, n)
+            else:
+                got = alloc.append_tokens(s, n)
+                assert got[0] == expect[0] and [tuple(c) for c in got[1]] == expect[1]
+        elif op == 4:
+            try:
+                child = model.fork(s)
+            except SwappedOut:
+                with pytest.raises(pkv.SwappedOut):
+                    alloc.fork(s)
+            else:
+                assert alloc.fork(s) == child
+        elif op == 5:
+            assert alloc.release(s) == len(model.release(s))
+        else:
+            fn, mfn = (alloc.swap_out, model.swap_out) if op <= 6 else (alloc.swap_in, model.swap_in)
+            try:
+                expect = mfn(group)
+            except OutOfBlocks:
+                with pytest.raises(pkv.OutOfBlocks):
+                    fn(group)
+            except SwappedOut:
+                with pytest.raises(pkv.SwappedOut):
+                    fn(group)
+            else:
+                assert [tuple(p) for p in fn(group).tolist()] == expect
+        if step % 20 == 0:
+            assert_same_state(model, alloc)
+    assert_same_state(model, alloc)
+
+
+def test_swap_errors(pkv):
+    a = pkv.BlockAllocator(4, 2)
+    s = a.new_seq()
+    a.append_tokens(s, 3)
+    with pytest.raises(pkv.OutOfBlocks):
+        a.swap_out([s])                 # no host pool yet
+    a.host_pool(2)
+    pairs = a.swap_out([s])
+    assert pairs.tolist() == [[0, 0], [1, 1]] and a.num_free() == 4 and a.num_free_host() == 0
+    with pytest.raises(pkv.PkvError):
+        a.host_pool(8)                  # host blocks in use
+    for op in (lambda: a.append_token(s), lambda: a.fork(s), lambda: a.export([s], 4),
+               lambda: a.swap_out([s]), lambda: a.append_batch([s])):
+        with pytest.raises(pkv.SwappedOut):
+            op()
+    with pytest.raises(pkv.PkvError):
+        a.swap_in([s, s])
+    assert a.seq_len(s) == 3 and a.table(s) == [0, 1]
+    assert a.swap_in([s]).tolist() == [[0, 2], [1, 3]] and a.num_free_host() == 2   # FIFO: 0, 1 went to the back
+    a.host_pool(8)                      # none in use: may be replaced
+    assert a.num_free_host() == 8

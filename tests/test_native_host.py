@@ -131,3 +131,27 @@ def test_multi_layer_ops_reject_bad_arguments_on_host(lib, no_gpu):
     assert g(good, good, 2, vp, 0, 4096, 4, None, None) == pkv.PKV_OK
     assert g(good, bad, 2, vp, 1, 4096, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
     assert g(good, good, 2, vp, 1, 4001, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_swap_blocks_reject_bad_arguments_on_host(lib, no_gpu):
+    import ctypes
+    import paged_kv_cache_152_gb300 as pkv
+    vp = ctypes.c_void_p(256)
+    f = lib.pkv_swap_blocks
+    assert f(vp, vp, vp, vp, vp, 0, 4096, 4, 4, None, None) == pkv.PKV_OK           # nothing to move
+    assert f(vp, vp, vp, vp, vp, -1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(vp, vp, vp, vp, vp, 2, 4001, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(vp, vp, vp, vp, vp, 2, 4096, 0, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(vp, vp, None, vp, vp, 2, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(vp, vp, vp, ctypes.c_void_p(264), vp, 2, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert f(vp, vp, vp, vp, None, 2, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    # well-formed arguments reach the pointer-attribute query, which has no
+    # device to ask here: an error status, never a launch
+    assert f(vp, vp, vp, vp, vp, 2, 4096, 4, 4, None, None) == pkv.PKV_ERR_CUDA
+    good = (ctypes.c_void_p * 2)(256, 512)
+    bad = (ctypes.c_void_p * 2)(256, None)
+    g = lib.pkv_swap_blocks_layers
+    assert g(good, good, good, good, 2, vp, 0, 4096, 4, 4, None, None) == pkv.PKV_OK
+    assert g(good, good, good, good, 0, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert g(good, good, good, good, 129, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert g(good, good, bad, good, 2, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
