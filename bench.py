@@ -19,9 +19,10 @@ graphs and replayed every step (--no-graph: direct binding calls).
   synchronize on both sides, max over ranks), inputs resident in HBM.
   The KV read per step (0.57 GB) is larger than L2 (129 MB), so no L2 flush.
 * e2e: the same metric through the public API with host buffers: every step
-  the C++ block manager appends one token per sequence and exports the tables,
-  queries/new K,V/slots/tables/context lengths go host->device from pinned
-  memory, the two kernels run, the output comes back device->host.
+  the C++ block manager appends one token per sequence and exports the tables
+  into the step's pinned staging region (with its queries and new K/V rows),
+  one host->device copy moves it, one DecodePlan launch appends the new
+  tokens and attends, the output comes back device->host, stream sync.
 * roofline: decode launch (both kernels) timed alone with CUDA events on its
   stream over the timed region; algorithmic bytes / mean duration vs the
   measured HBM copy bandwidth.
@@ -308,60 +309,83 @@ def device_step(pkv, st, ws, num_ctas, ev=None):
 
 
 def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
-    """Serving-loop steps through the public API with host buffers."""
+    """Serving-loop steps through the public API with host buffers.
+
+    Every step: the C++ block manager appends one token per sequence and
+    exports the tables and lengths straight into the step's page-locked
+    staging region, which also holds the step's queries and new K/V rows; ONE
+    host->device copy moves the region; copy-on-write pairs (if any) go
+    through copy_blocks; one launch of a DecodePlan (built once: append the
+    new tokens + attend, paged_attention_decode_append) runs the step; the
+    output comes back device->host and the stream is synchronised."""
     import numpy as np
     import torch
     wl, alloc = st["wl"], st["alloc"]
     n, h, hkv, d, mb = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, st["mb"]
-    pin = dict(pin_memory=True)
+    parts = [("q", n * h * d * 2), ("k", n * hkv * d * 2), ("v", n * hkv * d * 2), ("tables", n * mb * 4),
+             ("lens", n * 4)]
+    offs, off = {}, 0
+    for name, nbytes in parts:
+        offs[name] = (off, nbytes)
+        off += -(-nbytes // 256) * 256
+    step_bytes = off
+    h_stage = torch.empty((steps, step_bytes), dtype=torch.uint8).pin_memory()
     rng = np.random.default_rng(wl.seed + 77)
-    h_q = torch.from_numpy(rng.standard_normal((steps, n, h, d)).astype(np.float16))
-    h_k = torch.from_numpy(rng.standard_normal((steps, n, hkv, d)).astype(np.float16))
-    h_v = torch.from_numpy(rng.standard_normal((steps, n, hkv, d)).astype(np.float16))
-    h_q, h_k, h_v = h_q.pin_memory(), h_k.pin_memory(), h_v.pin_memory()
-    h_slots = torch.empty(n, dtype=torch.int64, **pin)
-    h_pairs = torch.empty((n, 2), dtype=torch.int32, **pin)
-    h_tables = torch.empty((n, mb), dtype=torch.int32, **pin)
-    h_lens = torch.empty(n, dtype=torch.int32, **pin)
-    h_out = torch.empty((n, h, d), dtype=torch.float16, **pin)
-    d_q = torch.empty((n, h, d), dtype=torch.float16, device=device)
-    d_k = torch.empty((n, hkv, d), dtype=torch.float16, device=device)
-    d_v = torch.empty_like(d_k)
-    d_slots = torch.empty(n, dtype=torch.int64, device=device)
-    d_pairs = torch.empty((n, 2), dtype=torch.int64, device=device)
-    d_tables = torch.empty((n, mb), dtype=torch.int32, device=device)
-    d_lens = torch.empty(n, dtype=torch.int32, device=device)
+    stage_np = h_stage.numpy()
+    for name in ("q", "k", "v"):
+        o, nbytes = offs[name]
+        stage_np[:, o:o + nbytes].view(np.float16)[:] = rng.standard_normal((steps, nbytes // 2)).astype(np.float16)
+    tab_np = [stage_np[i, offs["tables"][0]:offs["tables"][0] + offs["tables"][1]].view(np.int32).reshape(n, mb)
+              for i in range(steps)]
+    lens_np = [stage_np[i, offs["lens"][0]:offs["lens"][0] + offs["lens"][1]].view(np.int32) for i in range(steps)]
+    h_rows = [h_stage[i] for i in range(steps)]
+    d_stage = torch.empty(step_bytes, dtype=torch.uint8, device=device)
+
+    def dview(name, dtype, shape):
+        o, nbytes = offs[name]
+        return d_stage[o:o + nbytes].view(dtype).view(*shape)
+
+    d_q = dview("q", torch.float16, (n, h, d))
+    d_k = dview("k", torch.float16, (n, hkv, d))
+    d_v = dview("v", torch.float16, (n, hkv, d))
+    d_tables = dview("tables", torch.int32, (n, mb))
+    d_lens = dview("lens", torch.int32, (n,))
     t = st["t"]
+    plan = pkv.DecodePlan(st["out"], d_q, t["key_cache"], t["value_cache"], d_tables, d_lens, wl.scale,
+                          key=d_k, value=d_v, num_ctas=num_ctas, workspace=ws, status=st["status"])
+    h_slots = np.empty(n, dtype=np.int64)
+    h_pairs_t = torch.empty((n, 2), dtype=torch.int64).pin_memory()
+    h_pairs32 = np.empty((n, 2), dtype=np.int32)
+    d_pairs = torch.empty((n, 2), dtype=torch.int64, device=device)
+    h_out = torch.empty((n, h, d), dtype=torch.float16).pin_memory()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
     batch = np.asarray(wl.batch, dtype=np.int32)
+    kv_per_token = 2 * hkv * d * 2
     bytes_total = 0
     h2d = d2h = 0
     barrier(dist, device)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        slots, pairs = alloc.append_batch(batch, slots_out=h_slots.numpy(), pairs_out=h_pairs.numpy())
-        alloc.export(batch, mb, tables_out=h_tables.numpy(), lens_out=h_lens.numpy())
-        bytes_total += 2 * int(h_lens.numpy().sum()) * hkv * d * 2
-        d_q.copy_(h_q[i], non_blocking=True)
-        d_k.copy_(h_k[i], non_blocking=True)
-        d_v.copy_(h_v[i], non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_tables.copy_(h_tables, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
-        h2d += (h_q[i].numel() + h_k[i].numel() + h_v[i].numel()) * 2 + n * 8 + n * mb * 4 + n * 4
+        _, pairs = alloc.append_batch(batch, slots_out=h_slots, pairs_out=h_pairs32)
+        alloc.export(batch, mb, tables_out=tab_np[i], lens_out=lens_np[i])
+        bytes_total += int(lens_np[i].sum()) * kv_per_token
+        d_stage.copy_(h_rows[i], non_blocking=True)
+        h2d += step_bytes
         if len(pairs):
-            d_pairs[:len(pairs)].copy_(h_pairs[:len(pairs)], non_blocking=True)
-            h2d += len(pairs) * 8
+            h_pairs_t.numpy()[:len(pairs)] = pairs
+            d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
+            h2d += len(pairs) * 16
             pkv.copy_blocks(t["key_cache"], t["value_cache"], d_pairs[:len(pairs)], status=st["status"])
-        pkv.reshape_and_cache(d_k, d_v, t["key_cache"], t["value_cache"], d_slots, status=st["status"])
-        pkv.paged_attention_decode(st["out"], d_q, t["key_cache"], t["value_cache"], d_tables, d_lens,
-                                   wl.scale, num_ctas=num_ctas, workspace=ws, status=st["status"])
+        plan.launch_raw(sh)
         h_out.copy_(st["out"], non_blocking=True)
         d2h += h_out.numel() * 2
-        torch.cuda.current_stream().synchronize()
+        stream.synchronize()
     elapsed = time.perf_counter() - t0
     elapsed = max_over_ranks(dist, elapsed, device)
     barrier(dist, device)
+    plan.close()
     return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // steps, "d2h": d2h // steps}
 
 
@@ -508,8 +532,10 @@ def run_pkv(args):
         line["e2e"] = {"value": round(world * e2e["bytes"] / e2e["elapsed"] / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "steps": e2e_steps,
-                       "includes": "host block manager append + table export, H2D from pinned memory, "
-                                   "reshape_and_cache, decode, D2H of the output, stream sync per step"}
+                       "includes": "host block manager append + table export into the step's pinned staging "
+                                   "region (queries, new K/V, tables, lengths), one H2D copy of it, one "
+                                   "DecodePlan launch (append new tokens + attend), D2H of the output, stream "
+                                   "sync per step"}
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
     if dist is not None:

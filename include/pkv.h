@@ -166,6 +166,34 @@ int pkv_paged_attention_decode_append(void *out, const void *query,
                                       void *workspace, size_t workspace_bytes,
                                       int32_t *dev_status, pkv_stream_t stream);
 
+/*
+ * Decode plans: validate once, launch many times.
+ *
+ * A serving loop calls the decode with the same buffers every step; only
+ * their contents (queries, new tokens, tables, lengths) change.
+ * pkv_decode_plan_create checks the arguments, picks the kernel and grid and
+ * encodes the caches' TMA descriptors once; pkv_decode_plan_launch then
+ * launches exactly what pkv_paged_attention_decode_append (key/value
+ * non-NULL) or pkv_paged_attention_decode (both NULL) would, with no host
+ * work but the launch.  Same results, errors and device status as those
+ * calls.  The plan borrows every pointer: the buffers must outlive it, and
+ * must not be moved or freed while it is in use.  A plan is read-only after
+ * creation (launches from several host threads are fine; on one workspace
+ * they must be stream-ordered, as for the direct calls).
+ */
+typedef struct pkv_decode_plan pkv_decode_plan_t;
+int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,
+                           void *key_cache, void *value_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens,
+                           int num_seqs, int num_heads, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks,
+                           float scale, int num_ctas,
+                           void *workspace, size_t workspace_bytes,
+                           int32_t *dev_status, pkv_decode_plan_t **plan);
+int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream);
+void pkv_decode_plan_destroy(pkv_decode_plan_t *plan);
+
 /* Bytes of workspace pkv_paged_attention_decode needs (host call; queries the
  * current device's SM count when num_ctas == 0).  Returns 0 for unsupported
  * shapes. */

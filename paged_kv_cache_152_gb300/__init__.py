@@ -13,6 +13,7 @@ Names mirror the C ABI without its ``pkv_`` prefix:
 * reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, ...)
 * copy_blocks(key_cache, value_cache, block_pairs, ...)
 * swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, ...)
+* DecodePlan: pkv_decode_plan_* (validate once, launch every step)
 * the *_layers variants, one launch for every layer's pool
 * BlockAllocator: pkv_alloc_* / pkv_seq_* / pkv_append_* / pkv_fork /
   pkv_release / pkv_export_tables / pkv_swap_out / pkv_swap_in.
@@ -82,6 +83,11 @@ SIGNATURES = {
     "pkv_swap_blocks": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_size, _c_int, _c_int, _vp, _vp]),
     "pkv_swap_blocks_layers": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_size, _c_int, _c_int,
                                         _vp, _vp]),
+    "pkv_decode_plan_create": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
+                                        _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size, _vp,
+                                        ctypes.POINTER(_vp)]),
+    "pkv_decode_plan_launch": (_c_int, [_vp, _vp]),
+    "pkv_decode_plan_destroy": (None, [_vp]),
     "pkv_alloc_host_pool": (_c_int, [_vp, _c_int, _i32p]),
     "pkv_swap_out": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
     "pkv_swap_in": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
@@ -244,6 +250,69 @@ def paged_attention_decode_append(out, query, key, value, key_cache, value_cache
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     _check(rc, "pkv_paged_attention_decode_append")
     return out
+
+
+class DecodePlan:
+    """pkv_decode_plan_*: a decode call validated once and launched many
+    times with the same tensors (their contents may change between launches).
+    With key/value given, each launch appends the new tokens and attends
+    (paged_attention_decode_append); without, it only attends.  The plan keeps
+    references to every tensor it was built from."""
+
+    def __init__(self, out, query, key_cache, value_cache, block_tables, context_lens, scale, key=None,
+                 value=None, num_ctas=0, workspace=None, status=None):
+        torch = _need(query, __import__("torch").float16, "query", 3)
+        _need(out, torch.float16, "out", 3)
+        _need(key_cache, torch.float16, "key_cache", 4)
+        _need(value_cache, torch.float16, "value_cache", 4)
+        _need(block_tables, torch.int32, "block_tables", 2)
+        _need(context_lens, torch.int32, "context_lens", 1)
+        if (key is None) != (value is None):
+            raise ValueError("key and value go together")
+        n, h, d = query.shape
+        nb, hkv, bs, d2 = key_cache.shape
+        if key is not None:
+            _need(key, torch.float16, "key", 3)
+            _need(value, torch.float16, "value", 3)
+            if tuple(key.shape) != (n, hkv, d) or tuple(value.shape) != (n, hkv, d):
+                raise ValueError("inconsistent shapes")
+        if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
+                or block_tables.shape[0] != n or context_lens.shape[0] != n:
+            raise ValueError("inconsistent shapes")
+        if workspace is None:
+            workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+        self._keep = (out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
+                      status)
+        self._lib = load()
+        handle = ctypes.c_void_p()
+        rc = self._lib.pkv_decode_plan_create(
+            _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale),
+            int(num_ctas), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+            ctypes.byref(handle))
+        _check(rc, "pkv_decode_plan_create")
+        self._h = handle
+        self.out = out
+
+    def launch(self, stream=None):
+        _check(self._lib.pkv_decode_plan_launch(self._h, _stream(stream)), "pkv_decode_plan_launch")
+        return self.out
+
+    def launch_raw(self, stream_handle):
+        """launch() on a stream given as its raw handle (an int), for loops
+        that look the stream up once."""
+        _check(self._lib.pkv_decode_plan_launch(self._h, stream_handle), "pkv_decode_plan_launch")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_decode_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None, stream=None):

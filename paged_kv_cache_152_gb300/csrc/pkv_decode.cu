@@ -10,10 +10,21 @@
 
 #include <math.h>
 #include <mutex>
+#include <new>
 
 #include "../../include/pkv.h"
 #include "pkv_decode_impl.cuh"
 #include "pkv_launch.h"
+
+// A validated decode call, ready to launch again and again (pkv_decode_plan_*).
+struct pkv_decode_plan {
+    pkv::DecodeParams params;
+    const void *fn = nullptr;
+    int ctas = 0;
+    int threads = 0;
+    size_t smem = 0;
+    bool empty = true;
+};
 
 namespace pkv {
 
@@ -53,6 +64,7 @@ struct Resolved {
     size_t smem;
     int ctas;
     int64_t workers;
+    bool smem_partials;  // the grid's shared memory includes the partial slots
 };
 
 bool shape_supported(int num_heads, int num_kv_heads, int head_dim, int block_size) {
@@ -99,7 +111,10 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
     if (num_ctas <= 0) {
         // one full wave; the bounds array grows with the grid, so settle the
         // grid and the shared memory together
-        size_t smem = smem_for(sms * 4);
+        // (the occupancy is taken with the partial slots included when they fit)
+        const size_t part = r->info.smem_partials;
+        size_t smem = smem_for(sms * 4) + part;
+        if (smem + 2 * 1024 > (size_t)optin) smem = smem_for(sms) + part;
         if (smem + 2 * 1024 > (size_t)optin) smem = smem_for(sms);
         if (smem + 2 * 1024 > (size_t)optin) return PKV_ERR_INVALID_ARG;
         int rc0 = ensure_smem_attr(r->info.fn, smem);
@@ -115,6 +130,10 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
         r->smem = smem_for(num_ctas);
     }
     if (r->smem + 2 * 1024 > (size_t)optin) return PKV_ERR_INVALID_ARG;  // + static shared memory
+    // partials of CTA-local merges in shared memory when they fit (else the
+    // workspace holds them; same arithmetic either way)
+    r->smem_partials = r->smem + r->info.smem_partials + 2 * 1024 <= (size_t)optin;
+    if (r->smem_partials) r->smem += r->info.smem_partials;
     const int rc = ensure_smem_attr(r->info.fn, r->smem);
     if (rc != PKV_OK) return rc;
     r->ctas = num_ctas;
@@ -183,11 +202,15 @@ extern "C" int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head
 
 namespace {
 
-int decode_impl(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
-                const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
-                const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
-                int32_t *dev_status, pkv_stream_t stream) {
+// Validates one decode call and fills a launch plan (kernel, grid, shared
+// memory, parameter block with the encoded tensor maps).  plan->empty marks a
+// call with no sequences (nothing to launch).
+int build_plan(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
+               const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+               const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+               int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+               int32_t *dev_status, pkv_decode_plan *plan) {
+    plan->empty = num_seqs == 0;
     if (num_seqs == 0) return PKV_OK;
     if ((new_key == nullptr) != (new_value == nullptr)) return PKV_ERR_INVALID_ARG;
     if (new_key && (!aligned16(new_key) || !aligned16(new_value))) return PKV_ERR_INVALID_ARG;
@@ -212,7 +235,7 @@ int decode_impl(void *out, const void *query, const void *new_key, const void *n
     if (workspace_bytes < ws.total) return PKV_ERR_INVALID_ARG;
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
-    DecodeParams p;
+    DecodeParams &p = plan->params;
     {
         const int chunk_rows = block_size < 16 ? block_size : 16;
         const int halves = head_dim / 64;
@@ -249,14 +272,36 @@ int decode_impl(void *out, const void *query, const void *new_key, const void *n
     p.num_blocks = num_blocks;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.wait_limit_ns = kWaitLimitNs;
+    p.smem_partials = r.smem_partials ? 1 : 0;
 
-    void *args[] = {&p};
-    if (launch_pdl(r.info.fn, dim3(r.ctas), dim3(r.info.threads), r.smem, stream, args) != cudaSuccess) {
+    plan->fn = r.info.fn;
+    plan->ctas = r.ctas;
+    plan->threads = r.info.threads;
+    plan->smem = r.smem;
+    return PKV_OK;
+}
+
+int launch_plan(const pkv_decode_plan &plan, pkv_stream_t stream) {
+    if (plan.empty) return PKV_OK;
+    void *args[] = {const_cast<DecodeParams *>(&plan.params)};
+    if (launch_pdl(plan.fn, dim3(plan.ctas), dim3(plan.threads), plan.smem, stream, args) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
-
     return PKV_OK;
+}
+
+int decode_impl(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
+                const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                int32_t *dev_status, pkv_stream_t stream) {
+    pkv_decode_plan plan;
+    const int rc = build_plan(out, query, new_key, new_value, key_cache, value_cache, block_tables,
+                              max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
+                              block_size, num_blocks, scale, num_ctas, workspace, workspace_bytes, dev_status, &plan);
+    if (rc != PKV_OK) return rc;
+    return launch_plan(plan, stream);
 }
 
 }  // namespace
@@ -285,3 +330,32 @@ extern "C" int pkv_paged_attention_decode_append(void *out, const void *query, c
                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
                        num_ctas, workspace, workspace_bytes, dev_status, stream);
 }
+
+extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,
+                                      void *key_cache, void *value_cache, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                      int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                      float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, pkv_decode_plan_t **plan_out) {
+    if (!plan_out) return PKV_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    if ((key == nullptr) != (value == nullptr)) return PKV_ERR_INVALID_ARG;
+    pkv_decode_plan *plan = new (std::nothrow) pkv_decode_plan;
+    if (!plan) return PKV_ERR_INVALID_ARG;
+    const int rc = build_plan(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                              context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                              scale, num_ctas, workspace, workspace_bytes, dev_status, plan);
+    if (rc != PKV_OK) {
+        delete plan;
+        return rc;
+    }
+    *plan_out = plan;
+    return PKV_OK;
+}
+
+extern "C" int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream) {
+    if (!plan) return PKV_ERR_INVALID_ARG;
+    return launch_plan(*plan, stream);
+}
+
+extern "C" void pkv_decode_plan_destroy(pkv_decode_plan_t *plan) { delete plan; }

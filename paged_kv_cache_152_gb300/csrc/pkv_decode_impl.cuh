@@ -85,7 +85,8 @@ struct DecodeGeometry {
 };
 
 // Dynamic shared memory (from a 1024-byte aligned base):
-// [stages][query + new-row slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)].
+// [stages][query + new-row slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)]
+// [partial slots (optional): NW workers x 2 (first / last piece) x G x (2 + D) fp32].
 template <int NW, int ST, int D, int BS, int G>
 struct DecodeSmem {
     using Geo = DecodeGeometry<D, BS, G>;
@@ -96,6 +97,8 @@ struct DecodeSmem {
     static constexpr size_t kAlign = 1024;              // slack for aligning the base
     static constexpr size_t kFixed = kCum + kAlign;
     static constexpr size_t kPerSeq = 8;
+    static constexpr size_t kSlotFloats = (size_t)G * (2 + D);  // (m, l) per head, then the outputs
+    static constexpr size_t kPartials = (size_t)NW * 2 * kSlotFloats * 4 + 16;  // + alignment slack
 };
 
 // Zeroes V rows [R, kRows) of a ragged chunk's tile (every byte of those rows,
@@ -262,19 +265,65 @@ struct WorkerCtx {
     uint32_t epoch;          // this call's epoch
     unsigned long long *count;  // this call's per-segment counters (global)
     int *cta_count;          // per-worker-slot counters of this CTA (shared)
+    float *part;             // partial slots of this CTA's workers (shared), or NULL
 
     __device__ __forceinline__ int64_t start(int64_t w) const {
         return w >= W ? T : worker_start2(bounds, nw, w);
     }
 };
 
-// One warp merges the pieces of a cut segment, in worker order, combining
-// (max, sum, output) online: M' = max(M, m_p), X' = X 2^(M - M') + x_p 2^(m_p - M').
-// Each piece's (m, l) and output slice are loaded together (one L2 round trip).
+// Which workers hold pieces of segment (s, kvh), and whether they all belong
+// to this CTA.
+struct SegInfo {
+    int64_t g0;      // first chunk of the segment
+    int64_t wa, wb;  // first and last worker whose share meets it
+    bool local;      // wa and wb (and all between) are workers of this CTA
+};
+
+__device__ __forceinline__ SegInfo segment_info(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh) {
+    const int nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
+    SegInfo si;
+    si.g0 = wc.cum[s] + (int64_t)kvh * nch;
+    si.wa = worker_of2(wc.bounds, wc.C, wc.nw, si.g0);
+    si.wb = worker_of2(wc.bounds, wc.C, wc.nw, si.g0 + nch - 1);
+    si.local = (si.wa / wc.nw == blockIdx.x) && (si.wb / wc.nw == blockIdx.x);
+    return si;
+}
+
+// Partial (m, l, outputs) of worker w's piece that starts at chunk st, for
+// head g: in this CTA's shared slots (segments that stay in the CTA, when
+// enabled) or in the workspace.
+struct PartialLoc {
+    float *ml;   // (max, sum)
+    float *acc;  // D outputs
+};
+
+template <int D, int G>
+__device__ __forceinline__ PartialLoc partial_loc(const DecodeParams &p, const WorkerCtx &wc, bool shared_slot,
+                                                  int64_t w, int which, int g) {
+    if (shared_slot) {
+        float *base = wc.part + ((w % wc.nw) * 2 + which) * (G * (2 + D));
+        return {base + 2 * g, base + 2 * G + g * D};
+    }
+    const int64_t b = (w * 2 + which) * G + g;
+    return {p.ws_ml + b * 2, p.ws_acc + b * D};
+}
+
+// One warp merges the pieces of a cut segment, in worker order:
+//     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
+// Up to 32 pieces at a time: lane j fetches piece j's (m, l) -- all in one L2
+// round trip -- and the warp reduces them; the output slices are then summed
+// in piece order with the loads of several pieces in flight together.  A
+// segment with more pieces goes round again, folding each batch into the
+// running (M, L, out) (the same combine, online).  Fixed order throughout:
+// the result does not depend on which piece finished last.
 template <int D, int G>
 __device__ __forceinline__ void merge_segment(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh,
-                                              int64_t g0, int64_t wa, int64_t wb, int lane) {
-    constexpr int PER = D / 32;  // output elements per lane and head
+                                              const SegInfo &si, int lane) {
+    const int64_t g0 = si.g0, wa = si.wa, wb = si.wb;
+    const bool sh = si.local && wc.part != nullptr;  // partials in shared memory
+    constexpr int PER = D / 32;               // output elements per lane and head
+    constexpr int U = G >= 4 ? 1 : 4 / G;     // pieces whose slices are loaded together
     float M[G], L[G], O[G][PER];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -284,28 +333,82 @@ __device__ __forceinline__ void merge_segment(const DecodeParams &p, const Worke
         for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
     }
 #pragma unroll 1
-    for (int64_t w = wa; w <= wb; ++w) {
-        const int64_t st = wc.start(w);
-        if (st == wc.start(w + 1)) continue;
-        const int64_t b = (w * 2 + partial_slot(st, g0)) * G;
-        float2 ml[G];
-        float a[G][PER];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            ml[g] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml) + b + g);
-            const float *src = p.ws_acc + (b + g) * D + lane * PER;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) a[g][k] = __ldcg(src + k);
+    for (int64_t w0 = wa; w0 <= wb; w0 += 32) {
+        const int cnt = (int)(wb - w0 + 1 < 32 ? wb - w0 + 1 : 32);
+        int which = 0;
+        bool has = false;
+        if (lane < cnt) {
+            const int64_t w = w0 + lane;
+            const int64_t st = wc.start(w);
+            has = st < wc.start(w + 1);
+            which = partial_slot(st, g0);
         }
+        // the first U pieces' output slices travel with the (max, sum) loads
+        // (small groups only: for G >= 4 the registers are better spent elsewhere)
+        constexpr bool kEarly = G <= 2;
+        float a0[kEarly ? U : 1][kEarly ? G : 1][kEarly ? PER : 1];
+#pragma unroll
+        for (int u = 0; u < (kEarly ? U : 0); ++u) {
+            const int j = u < cnt ? u : cnt - 1;
+            const int wj = __shfl_sync(kFullMask, which, j);
+            const bool use = u < cnt && __shfl_sync(kFullMask, has, j);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float *src = partial_loc<D, G>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) a0[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
+            }
+        }
+        float wgt[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const float mn = fmaxf(M[g], ml[g].x);
-            const float f_old = exp2f(M[g] - mn);
-            const float f_new = exp2f(ml[g].x - mn);
-            L[g] = L[g] * f_old + ml[g].y * f_new;
+            float2 ml = make_float2(-CUDART_INF_F, 0.f);
+            if (has) {
+                const float2 *src = reinterpret_cast<const float2 *>(
+                    partial_loc<D, G>(p, wc, sh, w0 + lane, which, g).ml);
+                ml = sh ? *src : __ldcg(src);
+            }
+            float mx = ml.x;
 #pragma unroll
-            for (int k = 0; k < PER; ++k) O[g][k] = O[g][k] * f_old + a[g][k] * f_new;
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
+            const float mn = fmaxf(M[g], mx);   // some piece is non-empty: finite
+            const float f_old = exp2f(M[g] - mn);
+            wgt[g] = has ? exp2f(ml.x - mn) : 0.f;
+            float ls = ml.y * wgt[g];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
+            L[g] = L[g] * f_old + ls;
             M[g] = mn;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) O[g][k] *= f_old;
+        }
+#pragma unroll 1
+        for (int j0 = 0; j0 < cnt; j0 += U) {
+            float a[U][G][PER], f[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u < cnt ? j0 + u : cnt - 1;
+                const int wj = __shfl_sync(kFullMask, which, j);
+                const bool use = j0 + u < cnt && __shfl_sync(kFullMask, has, j);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    f[u][g] = __shfl_sync(kFullMask, wgt[g], j);
+                    if (kEarly && j0 == 0) {
+#pragma unroll
+                        for (int k = 0; k < PER; ++k) a[u][g][k] = a0[kEarly ? u : 0][kEarly ? g : 0][kEarly ? k : 0];
+                    } else {
+                        const float *src = partial_loc<D, G>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
+#pragma unroll
+                        for (int k = 0; k < PER; ++k) a[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) O[g][k] += a[u][g][k] * f[u][g];
         }
     }
 #pragma unroll
@@ -321,7 +424,7 @@ __device__ __forceinline__ void merge_segment(const DecodeParams &p, const Worke
 // stored partial; the caller counts it in later (count_in).
 template <int D, int G>
 __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx &wc, const int4 md, float m,
-                                             float l, const float (&o)[D / 8][4], int lane) {
+                                             float l, const float (&o)[D / 8][4], SegInfo &si, int lane) {
     const int g = lane >> 2;
     const int t = lane & 3;
     l += __shfl_xor_sync(kFullMask, l, 1);
@@ -336,15 +439,14 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
         }
         return false;
     }
-    const int64_t base = (wc.wid * 2 + ((flags & kSlot1) ? 1 : 0)) * G;
+    si = segment_info(p, wc, s, kvh);
     if (g < G) {
-        float *dst = p.ws_acc + (base + g) * D + 2 * t;
+        const PartialLoc at = partial_loc<D, G>(p, wc, si.local && wc.part != nullptr, wc.wid,
+                                                (flags & kSlot1) ? 1 : 0, g);
+        float *dst = at.acc + 2 * t;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j) *reinterpret_cast<float2 *>(dst + 8 * j) = make_float2(o[j][0], o[j][1]);
-        if (t == 0) {
-            p.ws_ml[(base + g) * 2] = m;
-            p.ws_ml[(base + g) * 2 + 1] = l;
-        }
+        if (t == 0) *reinterpret_cast<float2 *>(at.ml) = make_float2(m, l);
     }
     return true;
 }
@@ -355,16 +457,13 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
 // spans CTAs (only one longer than the CTA boundary could snap past) meets on
 // the workspace's epoch-tagged counter with GPU-scope ordering.
 template <int D, int G>
-__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh, int lane) {
-    const int nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
-    const int64_t g0 = wc.cum[s] + (int64_t)kvh * nch;
-    const int64_t wa = worker_of2(wc.bounds, wc.C, wc.nw, g0);
-    const int64_t wb = worker_of2(wc.bounds, wc.C, wc.nw, g0 + nch - 1);
+__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh,
+                                         const SegInfo &si, int lane) {
+    const int64_t wa = si.wa, wb = si.wb;
     int pieces = 0;
     for (int64_t w = wa; w <= wb; ++w) pieces += wc.start(w) < wc.start(w + 1);
-    const bool local = (wa / wc.nw == blockIdx.x) && (wb / wc.nw == blockIdx.x);
     int arrived = 0;
-    if (local) {
+    if (si.local) {
         __threadfence_block();  // the partial is visible to this CTA before it is counted
         __syncwarp();
         if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % wc.nw), 1) + 1;
@@ -377,11 +476,16 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx 
         arrived = __shfl_sync(kFullMask, arrived, 0);
         if (arrived == pieces) __threadfence();
     }
-    if (arrived == pieces) merge_segment<D, G>(p, wc, s, kvh, g0, wa, wb, lane);
+    if (arrived == pieces) merge_segment<D, G>(p, wc, s, kvh, si, lane);
 }
 
 template <int D, int BS, int G, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+#ifdef PKV_DECODE_SNAP_CAP
+    constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
+#else
+    constexpr int kSnapCap = 3 * NW;
+#endif
     using Geo = DecodeGeometry<D, BS, G>;
     using Smem = DecodeSmem<NW, ST, D, BS, G>;
     extern __shared__ unsigned char smem_raw[];
@@ -486,7 +590,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     const int64_t T = cum[N];
     const int C = gridDim.x;
     for (int c = tid; c <= C; c += NW * 32)
-        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, 3 * NW);
+        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
     __syncthreads();
     const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
@@ -502,7 +606,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         return;
     }
     const int n = (int)(ge - gb);
-    const WorkerCtx wc{cum, bounds, C, NW, W, T, wid, epoch, count_now, cta_count};
+    // shared partial slots: 16-byte aligned, after the bounds
+    float *part = nullptr;
+    if (p.smem_partials)
+        part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
+    const WorkerCtx wc{cum, bounds, C, NW, W, T, wid, epoch, count_now, cta_count, part};
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
@@ -652,7 +760,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         // merge) then overlaps the copies in flight instead of draining the ring
         __syncwarp();
         if (issued < n) issue(issued++);
-        if ((md.w & kLast) && finish_piece<D, G>(p, wc, md, m, l, o, lane)) count_in<D, G>(p, wc, md.x, md.y, lane);
+        SegInfo si;
+        if ((md.w & kLast) && finish_piece<D, G>(p, wc, md, m, l, o, si, lane))
+            count_in<D, G>(p, wc, md.x, md.y, si, lane);
     }
     exit_warp();
 }

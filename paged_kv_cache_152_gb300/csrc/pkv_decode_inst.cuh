@@ -41,6 +41,7 @@ DecodeKernelInfo info_of() {
     i.smem_fixed = Smem::kFixed;
     i.smem_per_seq = Smem::kPerSeq;
     i.smem_per_cta = 8;
+    i.smem_partials = Smem::kPartials;
     return i;
 }
 

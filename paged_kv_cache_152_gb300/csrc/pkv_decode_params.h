@@ -42,6 +42,9 @@ struct DecodeParams {
     int num_blocks;
     float scale_log2;             // scale * log2(e)
     uint64_t wait_limit_ns;
+    // 1: partials of segments cut between workers of one CTA are kept in the
+    // CTA's shared memory (after the CTA bounds); 0: in ws_ml / ws_acc
+    int smem_partials;
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
@@ -68,6 +71,7 @@ struct DecodeKernelInfo {
     size_t smem_fixed;     // dynamic shared memory without the per-sequence arrays
     size_t smem_per_seq;   // bytes per sequence (+ one extra int)
     size_t smem_per_cta;   // bytes per CTA of the grid (+ one extra)
+    size_t smem_partials;  // bytes of the optional shared-memory partial slots
 };
 
 // Defined in pkv_decode_d{64,128}_g{1,2,4,8}.cu; false if not compiled.

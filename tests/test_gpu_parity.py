@@ -416,3 +416,35 @@ def test_decode_append_equals_write_then_decode(pkv, name, kw, num_ctas):
     seqs = sample_seqs(wl, 8) if wl.num_seqs > 16 else None
     fused.oracle_write_new_tokens()
     assert max_abs_err(fused.out, fused.oracle_decode(seqs), seqs) <= TOL
+
+
+@pytest.mark.parametrize("name,kw", [("7b", dict(num_seqs=11)), ("gqa", dict(num_seqs=9)), ("tiny", {})])
+def test_decode_plan_equals_direct_calls(pkv, name, kw):
+    """A DecodePlan launch gives the bits of the direct call it was built from,
+    launch after launch, with the buffers' contents changing in between."""
+    wl = W.make(name, **kw)
+    direct, planned = Case(wl), Case(wl)
+    plan = pkv.DecodePlan(planned.out, planned.t["query"], planned.t["key_cache"], planned.t["value_cache"],
+                          planned.tables, planned.lens, wl.scale, key=planned.t["key"], value=planned.t["value"],
+                          status=planned.status)
+    read_only = pkv.DecodePlan(torch.empty_like(planned.out), planned.t["query"], planned.t["key_cache"],
+                               planned.t["value_cache"], planned.tables, planned.lens, wl.scale,
+                               status=planned.status)
+    for step in range(3):
+        if step:
+            # new queries for both sides (same values), same tables
+            q = torch.randn_like(direct.t["query"].float()).half()
+            direct.t["query"].copy_(q)
+            planned.t["query"].copy_(q)
+        pkv.paged_attention_decode_append(direct.out, direct.t["query"], direct.t["key"], direct.t["value"],
+                                          direct.t["key_cache"], direct.t["value_cache"], direct.tables,
+                                          direct.lens, wl.scale, status=direct.status)
+        plan.launch()
+        ro = read_only.launch()
+        torch.cuda.synchronize()
+        assert int(direct.status.item()) == 0 and int(planned.status.item()) == 0
+        assert torch.equal(planned.out.view(torch.int16), direct.out.view(torch.int16))
+        assert torch.equal(ro.view(torch.int16), direct.out.view(torch.int16))
+        assert torch.equal(planned.t["key_cache"].view(torch.int16), direct.t["key_cache"].view(torch.int16))
+    plan.close()
+    read_only.close()

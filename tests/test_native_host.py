@@ -155,3 +155,22 @@ def test_swap_blocks_reject_bad_arguments_on_host(lib, no_gpu):
     assert g(good, good, good, good, 0, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
     assert g(good, good, good, good, 129, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
     assert g(good, good, bad, good, 2, vp, 1, 4096, 4, 4, None, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_decode_plan_rejects_bad_arguments_on_host(lib, no_gpu):
+    import ctypes
+    import paged_kv_cache_152_gb300 as pkv
+    vp = ctypes.c_void_p(256)
+    h = ctypes.c_void_p(1)
+
+    def create(**kw):
+        return lib.pkv_decode_plan_create(
+            vp, vp, kw.get("k", None), kw.get("v", None), vp, vp, vp, 4, vp, kw.get("n", 2), 8, 8, 64, 16, 10,
+            ctypes.c_float(0.125), 0, kw.get("ws", vp), 1 << 20, None, kw.get("out", ctypes.byref(h)))
+    assert create(out=None) == pkv.PKV_ERR_INVALID_ARG
+    assert create(k=vp) == pkv.PKV_ERR_INVALID_ARG and h.value is None    # key without value
+    assert create(ws=None) == pkv.PKV_ERR_INVALID_ARG and h.value is None
+    assert create(n=0) == pkv.PKV_OK and h.value is not None               # empty: launches nothing
+    assert lib.pkv_decode_plan_launch(h, None) == pkv.PKV_OK
+    lib.pkv_decode_plan_destroy(h)
+    assert lib.pkv_decode_plan_launch(None, None) == pkv.PKV_ERR_INVALID_ARG
