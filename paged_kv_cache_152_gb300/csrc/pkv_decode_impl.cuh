@@ -254,11 +254,14 @@ __device__ __forceinline__ int count_in_tagged(unsigned long long *cnt, uint32_t
 }
 
 // Where a worker warp is: what finish_piece needs besides the piece itself.
+// NW (workers per CTA) is a compile-time constant, so the share arithmetic
+// divides by a constant.
+template <int NW>
 struct WorkerCtx {
+    static constexpr int nw = NW;
     const int *cum;          // chunk prefix sums (shared memory)
     const int64_t *bounds;   // CTA ranges, [C + 1] (shared memory)
     int C;                   // CTAs in the grid
-    int nw;                  // workers per CTA
     int64_t W;               // workers in the grid
     int64_t T;               // chunks in the batch
     int64_t wid;             // this worker
@@ -268,26 +271,33 @@ struct WorkerCtx {
     float *part;             // partial slots of this CTA's workers (shared), or NULL
 
     __device__ __forceinline__ int64_t start(int64_t w) const {
-        return w >= W ? T : worker_start2(bounds, nw, w);
+        return w >= W ? T : worker_start2(bounds, NW, w);
     }
 };
 
-// Which workers hold pieces of segment (s, kvh), and whether they all belong
-// to this CTA.
+// Where segment (s, kvh) lies, and whether it lies inside this CTA's range
+// (then all its pieces are this CTA's, and they meet in shared memory).
 struct SegInfo {
     int64_t g0;      // first chunk of the segment
-    int64_t wa, wb;  // first and last worker whose share meets it
-    bool local;      // wa and wb (and all between) are workers of this CTA
+    int nch;         // its chunks
+    bool local;      // inside this CTA's range
 };
 
-__device__ __forceinline__ SegInfo segment_info(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh) {
-    const int nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
+template <int NW>
+__device__ __forceinline__ SegInfo segment_info(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh) {
     SegInfo si;
-    si.g0 = wc.cum[s] + (int64_t)kvh * nch;
-    si.wa = worker_of2(wc.bounds, wc.C, wc.nw, si.g0);
-    si.wb = worker_of2(wc.bounds, wc.C, wc.nw, si.g0 + nch - 1);
-    si.local = (si.wa / wc.nw == blockIdx.x) && (si.wb / wc.nw == blockIdx.x);
+    si.nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
+    si.g0 = wc.cum[s] + (int64_t)kvh * si.nch;
+    si.local = si.g0 >= wc.bounds[blockIdx.x] && si.g0 + si.nch <= wc.bounds[blockIdx.x + 1];
     return si;
+}
+
+// First and last worker whose share meets the segment.
+template <int NW>
+__device__ __forceinline__ void segment_workers(const WorkerCtx<NW> &wc, const SegInfo &si, int64_t &wa,
+                                                int64_t &wb) {
+    wa = worker_of2(wc.bounds, wc.C, NW, si.g0);
+    wb = worker_of2(wc.bounds, wc.C, NW, si.g0 + si.nch - 1);
 }
 
 // Partial (m, l, outputs) of worker w's piece that starts at chunk st, for
@@ -298,32 +308,26 @@ struct PartialLoc {
     float *acc;  // D outputs
 };
 
-template <int D, int G>
-__device__ __forceinline__ PartialLoc partial_loc(const DecodeParams &p, const WorkerCtx &wc, bool shared_slot,
+template <int D, int G, int NW>
+__device__ __forceinline__ PartialLoc partial_loc(const DecodeParams &p, const WorkerCtx<NW> &wc, bool shared_slot,
                                                   int64_t w, int which, int g) {
     if (shared_slot) {
-        float *base = wc.part + ((w % wc.nw) * 2 + which) * (G * (2 + D));
+        float *base = wc.part + ((w % NW) * 2 + which) * (G * (2 + D));
         return {base + 2 * g, base + 2 * G + g * D};
     }
     const int64_t b = (w * 2 + which) * G + g;
     return {p.ws_ml + b * 2, p.ws_acc + b * D};
 }
 
-// One warp merges the pieces of a cut segment, in worker order:
-//     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
-// Up to 32 pieces at a time: lane j fetches piece j's (m, l) -- all in one L2
-// round trip -- and the warp reduces them; the output slices are then summed
-// in piece order with the loads of several pieces in flight together.  A
-// segment with more pieces goes round again, folding each batch into the
-// running (M, L, out) (the same combine, online).  Fixed order throughout:
-// the result does not depend on which piece finished last.
-template <int D, int G>
-__device__ __forceinline__ void merge_segment(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh,
-                                              const SegInfo &si, int lane) {
-    const int64_t g0 = si.g0, wa = si.wa, wb = si.wb;
+// One warp merges the pieces of a cut segment, in worker order, combining
+// (max, sum, output) online: M' = max(M, m_p), X' = X 2^(M - M') + x_p 2^(m_p - M').
+// Each piece's (m, l) and output slice are loaded together (one round trip to
+// shared memory or L2 per piece); a segment has only a few pieces.
+template <int D, int G, int NW>
+__device__ __forceinline__ void merge_segment(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
+                                              const SegInfo &si, int64_t wa, int64_t wb, int lane) {
     const bool sh = si.local && wc.part != nullptr;  // partials in shared memory
-    constexpr int PER = D / 32;               // output elements per lane and head
-    constexpr int U = G >= 4 ? 1 : 4 / G;     // pieces whose slices are loaded together
+    constexpr int PER = D / 32;                      // output elements per lane and head
     float M[G], L[G], O[G][PER];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -333,97 +337,46 @@ __device__ __forceinline__ void merge_segment(const DecodeParams &p, const Worke
         for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
     }
 #pragma unroll 1
-    for (int64_t w0 = wa; w0 <= wb; w0 += 32) {
-        const int cnt = (int)(wb - w0 + 1 < 32 ? wb - w0 + 1 : 32);
-        int which = 0;
-        bool has = false;
-        if (lane < cnt) {
-            const int64_t w = w0 + lane;
-            const int64_t st = wc.start(w);
-            has = st < wc.start(w + 1);
-            which = partial_slot(st, g0);
-        }
-        // the first U pieces' output slices travel with the (max, sum) loads
-        // (small groups only: for G >= 4 the registers are better spent elsewhere)
-        constexpr bool kEarly = G <= 2;
-        float a0[kEarly ? U : 1][kEarly ? G : 1][kEarly ? PER : 1];
-#pragma unroll
-        for (int u = 0; u < (kEarly ? U : 0); ++u) {
-            const int j = u < cnt ? u : cnt - 1;
-            const int wj = __shfl_sync(kFullMask, which, j);
-            const bool use = u < cnt && __shfl_sync(kFullMask, has, j);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float *src = partial_loc<D, G>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
-#pragma unroll
-                for (int k = 0; k < PER; ++k) a0[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
-            }
-        }
-        float wgt[G];
+    for (int64_t w = wa; w <= wb; ++w) {
+        const int64_t st = wc.start(w);
+        if (st == wc.start(w + 1)) continue;
+        const int which = partial_slot(st, si.g0);
+        float2 ml[G];
+        float a[G][PER];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            float2 ml = make_float2(-CUDART_INF_F, 0.f);
-            if (has) {
-                const float2 *src = reinterpret_cast<const float2 *>(
-                    partial_loc<D, G>(p, wc, sh, w0 + lane, which, g).ml);
-                ml = sh ? *src : __ldcg(src);
-            }
-            float mx = ml.x;
+            const PartialLoc at = partial_loc<D, G, NW>(p, wc, sh, w, which, g);
+            const float2 *mlp = reinterpret_cast<const float2 *>(at.ml);
+            ml[g] = sh ? *mlp : __ldcg(mlp);
+            const float *src = at.acc + lane * PER;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
-            const float mn = fmaxf(M[g], mx);   // some piece is non-empty: finite
-            const float f_old = exp2f(M[g] - mn);
-            wgt[g] = has ? exp2f(ml.x - mn) : 0.f;
-            float ls = ml.y * wgt[g];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
-            L[g] = L[g] * f_old + ls;
-            M[g] = mn;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) O[g][k] *= f_old;
+            for (int k = 0; k < PER; ++k) a[g][k] = sh ? src[k] : __ldcg(src + k);
         }
-#pragma unroll 1
-        for (int j0 = 0; j0 < cnt; j0 += U) {
-            float a[U][G][PER], f[U][G];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u < cnt ? j0 + u : cnt - 1;
-                const int wj = __shfl_sync(kFullMask, which, j);
-                const bool use = j0 + u < cnt && __shfl_sync(kFullMask, has, j);
+        for (int g = 0; g < G; ++g) {
+            const float mn = fmaxf(M[g], ml[g].x);
+            const float f_old = exp2f(M[g] - mn);
+            const float f_new = exp2f(ml[g].x - mn);
+            L[g] = L[g] * f_old + ml[g].y * f_new;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    f[u][g] = __shfl_sync(kFullMask, wgt[g], j);
-                    if (kEarly && j0 == 0) {
-#pragma unroll
-                        for (int k = 0; k < PER; ++k) a[u][g][k] = a0[kEarly ? u : 0][kEarly ? g : 0][kEarly ? k : 0];
-                    } else {
-                        const float *src = partial_loc<D, G>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
-#pragma unroll
-                        for (int k = 0; k < PER; ++k) a[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int k = 0; k < PER; ++k) O[g][k] += a[u][g][k] * f[u][g];
+            for (int k = 0; k < PER; ++k) O[g][k] = O[g][k] * f_old + a[g][k] * f_new;
+            M[g] = mn;
         }
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
+        const float inv = 1.f / L[g];
 #pragma unroll
-        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] / L[g]);
+        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] * inv);
     }
 }
 
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
 // stored partial; the caller counts it in later (count_in).
-template <int D, int G>
-__device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx &wc, const int4 md, float m,
+template <int D, int G, int NW>
+__device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx<NW> &wc, const int4 md, float m,
                                              float l, const float (&o)[D / 8][4], SegInfo &si, int lane) {
     const int g = lane >> 2;
     const int t = lane & 3;
@@ -433,15 +386,16 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
     if (flags & kWhole) {
         if (g < G) {
             __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + 2 * t;
+            const float inv = 1.f / l;
 #pragma unroll
             for (int j = 0; j < D / 8; ++j)
-                *reinterpret_cast<uint32_t *>(dst + 8 * j) = pack_half2(o[j][0] / l, o[j][1] / l);
+                *reinterpret_cast<uint32_t *>(dst + 8 * j) = pack_half2(o[j][0] * inv, o[j][1] * inv);
         }
         return false;
     }
     si = segment_info(p, wc, s, kvh);
     if (g < G) {
-        const PartialLoc at = partial_loc<D, G>(p, wc, si.local && wc.part != nullptr, wc.wid,
+        const PartialLoc at = partial_loc<D, G, NW>(p, wc, si.local && wc.part != nullptr, wc.wid,
                                                 (flags & kSlot1) ? 1 : 0, g);
         float *dst = at.acc + 2 * t;
 #pragma unroll
@@ -456,17 +410,18 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
 // CTA meet on a shared-memory counter with CTA-scope ordering; a segment that
 // spans CTAs (only one longer than the CTA boundary could snap past) meets on
 // the workspace's epoch-tagged counter with GPU-scope ordering.
-template <int D, int G>
-__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx &wc, int s, int kvh,
+template <int D, int G, int NW>
+__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
                                          const SegInfo &si, int lane) {
-    const int64_t wa = si.wa, wb = si.wb;
+    int64_t wa, wb;
+    segment_workers(wc, si, wa, wb);
     int pieces = 0;
     for (int64_t w = wa; w <= wb; ++w) pieces += wc.start(w) < wc.start(w + 1);
     int arrived = 0;
     if (si.local) {
         __threadfence_block();  // the partial is visible to this CTA before it is counted
         __syncwarp();
-        if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % wc.nw), 1) + 1;
+        if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % NW), 1) + 1;
         arrived = __shfl_sync(kFullMask, arrived, 0);
         if (arrived == pieces) __threadfence_block();
     } else {
@@ -476,7 +431,7 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx 
         arrived = __shfl_sync(kFullMask, arrived, 0);
         if (arrived == pieces) __threadfence();
     }
-    if (arrived == pieces) merge_segment<D, G>(p, wc, s, kvh, si, lane);
+    if (arrived == pieces) merge_segment<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
 }
 
 template <int D, int BS, int G, int NW, int ST>
@@ -586,39 +541,23 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         for (int i = tid; i < p.num_heads * D / 8; i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
     }
 
-    // ---- CTA ranges snapped to segment boundaries, then this warp's share ----
+    // ---- this warp's share: CTA ranges snapped to segment boundaries, each
+    // divided equally among the CTA's warps.  A warp works out its own CTA's
+    // range itself and starts its block-table loads; the CTA-wide array of
+    // ranges (for the merges) is filled after that. ----
     const int64_t T = cum[N];
     const int C = gridDim.x;
-    for (int c = tid; c <= C; c += NW * 32)
-        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
-    __syncthreads();
     const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
-    const int64_t gb = worker_start2(bounds, NW, wid);
-    const int64_t ge = wid + 1 >= W ? T : worker_start2(bounds, NW, wid + 1);
-    // every warp counts itself out at the end; the last one advances the epoch
-    auto exit_warp = [&]() {
-        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
-            atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
-    };
-    if (gb >= ge) {
-        exit_warp();
-        return;
+    int64_t gb, ge;
+    {
+        const int c = (int)blockIdx.x + (lane & 1);
+        const int64_t v = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+        const int64_t lo = __shfl_sync(kFullMask, v, 0), hi = __shfl_sync(kFullMask, v, 1);
+        gb = lo + ((int64_t)warp * (hi - lo)) / NW;        // = worker_start2(bounds, NW, wid)
+        ge = lo + ((int64_t)(warp + 1) * (hi - lo)) / NW;  // = the next worker's start (T past the last)
     }
-    const int n = (int)(ge - gb);
-    // shared partial slots: 16-byte aligned, after the bounds
-    float *part = nullptr;
-    if (p.smem_partials)
-        part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx wc{cum, bounds, C, NW, W, T, wid, epoch, count_now, cta_count, part};
-
-    unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
-    const uint32_t wst_a = smem_addr(wst);
-    const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kSlotBytes;
-    const uint32_t wq_a = smem_addr(wq);
-    const uint32_t bar_a = smem_addr(bars + warp * ST);
-    int4 *wmeta = meta + 2 * warp * ST;
-    const bool append = p.new_key != nullptr;
+    const int n = gb < ge ? (int)(ge - gb) : 0;
 
     // the walk: cut pieces first (see share_order)
     const ShareOrder order = share_order(cum, N, Hkv, gb, ge);
@@ -634,6 +573,33 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     int win = 0;
     int tab_cur = table_entry(lane);
     int tab_nxt = table_entry(32 + lane);
+
+    for (int c = tid; c <= C; c += NW * 32)
+        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+    __syncthreads();
+    // every warp counts itself out at the end; the last one advances the epoch
+    auto exit_warp = [&]() {
+        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
+            atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
+    };
+    if (n == 0) {
+        exit_warp();
+        return;
+    }
+    // shared partial slots: 16-byte aligned, after the bounds
+    float *part = nullptr;
+    if (p.smem_partials)
+        part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
+    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, epoch, count_now, cta_count, part};
+
+    unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
+    const uint32_t wst_a = smem_addr(wst);
+    const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kSlotBytes;
+    const uint32_t wq_a = smem_addr(wq);
+    const uint32_t bar_a = smem_addr(bars + warp * ST);
+    int4 *wmeta = meta + 2 * warp * ST;
+    const bool append = p.new_key != nullptr;
+
     ChunkPos pos;  // chunk being issued
 
     auto issue = [&](int i) {
@@ -761,8 +727,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         __syncwarp();
         if (issued < n) issue(issued++);
         SegInfo si;
-        if ((md.w & kLast) && finish_piece<D, G>(p, wc, md, m, l, o, si, lane))
-            count_in<D, G>(p, wc, md.x, md.y, si, lane);
+        if ((md.w & kLast) && finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane))
+            count_in<D, G, NW>(p, wc, md.x, md.y, si, lane);
     }
     exit_warp();
 }
