@@ -66,7 +66,8 @@ namespace pkv {
 
 template <int D, int BS, int G>
 struct DecodeGeometry {
-    static constexpr int kRows = BS < 16 ? BS : 16;   // rows per chunk
+    static constexpr int kRows = 16;                  // rows per chunk
+    static constexpr int kBPC = BS < 16 ? 16 / BS : 1; // blocks per chunk (2 at block size 8)
     static constexpr int kNT = kRows / 8;             // 8-row groups per chunk (mma N tiles)
     static constexpr int kHalves = D / 64;            // 64-dim (128-byte) swizzle columns
     static constexpr int kHalfBytes = kRows * 128;    // one column of a tile
@@ -79,7 +80,8 @@ struct DecodeGeometry {
     static constexpr int kDTiles = D / 8;             // mma N tiles of P.V
     static constexpr int kBoxBytes = 8 * 128;         // one TMA box: 8 rows x 64 fp16
     static_assert(D == 64 || D == 128, "head_dim");
-    static_assert(BS % kRows == 0 && kRows % 8 == 0, "a chunk is whole 8-row boxes inside one block");
+    static_assert((BS % kRows == 0 || BS == 8) && kRows % 8 == 0,
+                  "a chunk is whole 8-row boxes, inside one block (or one box per block at block size 8)");
     static_assert(G >= 1 && G <= 8, "query heads per KV head");
     static_assert(kHalfBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
 };
@@ -564,15 +566,20 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
 
     // block-table entry of the chunk at walk position i (raw; validated when
     // used), 0 past the share
-    auto table_entry = [&](int i) -> int {
-        if (i >= n) return 0;
+    // (at block size 8 a chunk spans two blocks: the second entry comes in the
+    // high half, 0 when the chunk does not reach it)
+    auto table_entry = [&](int i) -> int2 {
+        if (i >= n) return make_int2(0, 0);
         const ChunkPos q = locate_chunk(cum, N, Hkv, order.at(i));
         const int lb = chunk_block(q.c, BS, Geo::kRows);
-        return __ldg(p.block_tables + (int64_t)q.s * p.max_blocks_per_seq + lb);
+        const int32_t *row = p.block_tables + (int64_t)q.s * p.max_blocks_per_seq;
+        int second = 0;
+        if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[q.s]) second = __ldg(row + lb + 1);
+        return make_int2(__ldg(row + lb), second);
     };
     int win = 0;
-    int tab_cur = table_entry(lane);
-    int tab_nxt = table_entry(32 + lane);
+    int2 tab_cur = table_entry(lane);
+    int2 tab_nxt = table_entry(32 + lane);
 
     for (int c = tid; c <= C; c += NW * 32)
         bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
@@ -613,11 +620,16 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             tab_cur = tab_nxt;
             tab_nxt = table_entry(win + 32 + lane);
         }
-        int phys = __shfl_sync(kFullMask, tab_cur, i - win);
+        int phys = __shfl_sync(kFullMask, tab_cur.x, i - win);
+        int phys2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, tab_cur.y, i - win) : 0;
         if (lane == 0) {
             if (phys < 0 || phys >= p.num_blocks) {
                 report(p.status, PKV_ERR_OUT_OF_RANGE);
                 phys = 0;
+            }
+            if (phys2 < 0 || phys2 >= p.num_blocks) {
+                report(p.status, PKV_ERR_OUT_OF_RANGE);
+                phys2 = 0;
             }
             const int stage = i % ST;
             const int rows = chunk_rows(pos.c, ctx[pos.s], Geo::kRows);
@@ -627,15 +639,20 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             const uint32_t bar = bar_a + stage * 8;
             const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
             const uint32_t vdst = kdst + Geo::kTileBytes;
-            // a whole chunk is one box per cache; a last chunk of at most 8 rows
-            // of a 16-row chunk takes one 8-row box per half instead
-            const bool short_box = Geo::kNT == 2 && rows <= 8;
+            // a whole chunk inside one block is one box per cache; a last chunk
+            // of at most 8 rows takes one 8-row box per half instead, and at
+            // block size 8 each block of the chunk is one 8-row box per half
+            // (the second lands 8 rows down, at +1 KB in each half)
+            const bool short_box = Geo::kBPC == 2 || rows <= 8;
+            const bool second = Geo::kBPC == 2 && rows > 8;
             // row of the cache viewed as [num_blocks * Hkv * BS rows]
             const int y = (int)(((int64_t)phys * Hkv + pos.kvh) * BS + (pos.c * Geo::kRows) % BS);
+            const int y2 = (int)(((int64_t)phys2 * Hkv + pos.kvh) * BS);
             wmeta[2 * stage] = make_int4(pos.s, pos.kvh, rows, flags);
-            wmeta[2 * stage + 1] = make_int4(y, 0, 0, 0);
+            wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, (short_box ? 2 * Geo::kHalves * Geo::kBoxBytes : 2 * Geo::kTileBytes) +
+            mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
+                                                  : 2 * Geo::kTileBytes) +
                                            ((flags & kFirst) ? Geo::kQBytes : 0) +
                                            (new_row ? 2 * Geo::kRowBytes : 0));
             if (!short_box) {
@@ -646,6 +663,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
                 for (int h = 0; h < Geo::kHalves; ++h) {
                     tma_load_3d(kdst + h * Geo::kHalfBytes, &p.tmap_k8, 0, y, h, bar);
                     tma_load_3d(vdst + h * Geo::kHalfBytes, &p.tmap_v8, 0, y, h, bar);
+                    if (second) {
+                        tma_load_3d(kdst + h * Geo::kHalfBytes + Geo::kBoxBytes, &p.tmap_k8, 0, y2, h, bar);
+                        tma_load_3d(vdst + h * Geo::kHalfBytes + Geo::kBoxBytes, &p.tmap_v8, 0, y2, h, bar);
+                    }
                 }
             }
             if (flags & kFirst)
@@ -716,7 +737,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
                 *reinterpret_cast<uint4 *>(tile + (v >> 3) * Geo::kHalfBytes + r * 128 + (((v & 7) ^ (r & 7)) << 4)) =
                     val;
                 __half *cache = is_v ? p.value_cache_w : p.key_cache_w;
-                *reinterpret_cast<uint4 *>(cache + ((int64_t)wmeta[2 * stage + 1].x + r) * D + v * 8) = val;
+                const int4 yy = wmeta[2 * stage + 1];
+                const int64_t crow = (Geo::kBPC == 2 && r >= 8) ? (int64_t)yy.y + (r - 8) : (int64_t)yy.x + r;
+                *reinterpret_cast<uint4 *>(cache + crow * D + v * 8) = val;
             }
             __syncwarp();
         }

@@ -84,13 +84,22 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         CHECK(lb >= 0 && lb < mb, "logical block %d outside table of %d", lb, mb);
         const int rows = chunk_rows(p.c, ctx[p.s], sr);
         CHECK(rows >= 1 && rows <= sr, "rows %d", rows);
-        const int row0 = (p.c * sr) % bs;
-        CHECK(row0 + rows <= bs, "chunk crosses block");
         CHECK(p.c * sr + rows <= ctx[p.s], "chunk past context");
         const int nb = 7;
-        for (int phys : {0, nb - 1}) {
-            const int64_t off = chunk_src_offset(phys, p.kvh, p.c, hkv, bs, sr, 64);
-            CHECK(off >= 0 && off + (int64_t)rows * 64 <= (int64_t)nb * hkv * bs * 64, "src offset");
+        if (bs >= sr) {
+            const int row0 = (p.c * sr) % bs;
+            CHECK(row0 + rows <= bs, "chunk crosses block");
+            for (int phys : {0, nb - 1}) {
+                const int64_t off = chunk_src_offset(phys, p.kvh, p.c, hkv, bs, sr, 64);
+                CHECK(off >= 0 && off + (int64_t)rows * 64 <= (int64_t)nb * hkv * bs * 64, "src offset");
+            }
+        } else {
+            // small blocks: the chunk's rows fill whole blocks lb, lb+1, ... (one
+            // 8-row box each), all inside the table row
+            CHECK(sr % bs == 0 && (p.c * sr) % bs == 0, "chunk not block-aligned");
+            const int last_lb = (p.c * sr + rows - 1) / bs;
+            CHECK(last_lb < mb && last_lb - lb < sr / bs, "chunk's blocks %d..%d outside table of %d", lb,
+                  last_lb, mb);
         }
     }
     // walk every worker as the kernel does; record pieces and partial slots
@@ -197,8 +206,7 @@ int main() {
     const int bss[] = {8, 16, 32, 64, 128};
     for (int it = 0; it < 3000; ++it) {
         const int bs = bss[rng() % 5];
-        const int row_bytes = (rng() % 2) ? 256 : 128;
-        const int sr = (bs * row_bytes <= 4096) ? bs : 4096 / row_bytes;
+        const int sr = 16;  // rows per chunk, as in the decode kernel
         const int n = 1 + (int)(rng() % 40);
         const int hkv = 1 + (int)(rng() % 4);
         const int maxctx = 1 + (int)(rng() % 600);

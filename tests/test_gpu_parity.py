@@ -396,7 +396,9 @@ def test_copy_blocks_layers_bit_exact(pkv):
 
 
 @pytest.mark.parametrize("name,kw", [("tiny", {}), ("7b", dict(num_seqs=11)), ("gqa", dict(num_seqs=9)),
-                                     ("chat", dict(num_main=5, num_transient=4)), ("7b", {})])
+                                     ("chat", dict(num_main=5, num_transient=4)), ("7b", {}),
+                                     ("7b", dict(num_seqs=11, block_size=8)), ("tiny", dict(block_size=8)),
+                                     ("gqa", dict(num_seqs=9, block_size=8))])
 @pytest.mark.parametrize("num_ctas", [0, 3])
 def test_decode_append_equals_write_then_decode(pkv, name, kw, num_ctas):
     """The fused append + attend launch gives the same cache bits and the same
