@@ -374,6 +374,92 @@ __device__ __forceinline__ void merge_segment(const DecodeParams &p, const Worke
     }
 }
 
+// The same merge for a segment cut into many pieces (small batches spread
+// over the whole grid): up to 32 pieces at a time, lane j fetches piece j's
+// (m, l) -- one round trip for all of them -- the warp reduces M and L with
+// shuffles, then sums the output slices in piece order with the loads of
+// several pieces in flight.  More than 32 pieces go round again, folding
+// each batch into the running (M, L, out).  Fixed order: deterministic.
+template <int D, int G, int NW>
+__device__ __forceinline__ void merge_segment_wide(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
+                                                   const SegInfo &si, int64_t wa, int64_t wb, int lane) {
+    const bool sh = si.local && wc.part != nullptr;
+    constexpr int PER = D / 32;
+    constexpr int U = G >= 4 ? 1 : 4 / G;  // pieces whose slices are loaded together
+    float M[G], L[G], O[G][PER];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        M[g] = -CUDART_INF_F;
+        L[g] = 0.f;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
+    }
+#pragma unroll 1
+    for (int64_t w0 = wa; w0 <= wb; w0 += 32) {
+        const int cnt = (int)(wb - w0 + 1 < 32 ? wb - w0 + 1 : 32);
+        int which = 0;
+        bool has = false;
+        if (lane < cnt) {
+            const int64_t st = wc.start(w0 + lane);
+            has = st < wc.start(w0 + lane + 1);
+            which = partial_slot(st, si.g0);
+        }
+        float wgt[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float2 ml = make_float2(-CUDART_INF_F, 0.f);
+            if (has) {
+                const float2 *src =
+                    reinterpret_cast<const float2 *>(partial_loc<D, G, NW>(p, wc, sh, w0 + lane, which, g).ml);
+                ml = sh ? *src : __ldcg(src);
+            }
+            float mx = ml.x;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
+            const float mn = fmaxf(M[g], mx);  // some piece is non-empty: finite
+            const float f_old = exp2f(M[g] - mn);
+            wgt[g] = has ? exp2f(ml.x - mn) : 0.f;
+            float ls = ml.y * wgt[g];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
+            L[g] = L[g] * f_old + ls;
+            M[g] = mn;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) O[g][k] *= f_old;
+        }
+#pragma unroll 1
+        for (int j0 = 0; j0 < cnt; j0 += U) {
+            float a[U][G][PER], f[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u < cnt ? j0 + u : cnt - 1;
+                const int wj = __shfl_sync(kFullMask, which, j);
+                const bool use = j0 + u < cnt && __shfl_sync(kFullMask, has, j);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    f[u][g] = __shfl_sync(kFullMask, wgt[g], j);
+                    const float *src = partial_loc<D, G, NW>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) a[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int k = 0; k < PER; ++k) O[g][k] += a[u][g][k] * f[u][g];
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
+        const float inv = 1.f / L[g];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] * inv);
+    }
+}
+
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
 // stored partial; the caller counts it in later (count_in).
@@ -433,7 +519,13 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
         arrived = __shfl_sync(kFullMask, arrived, 0);
         if (arrived == pieces) __threadfence();
     }
-    if (arrived == pieces) merge_segment<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
+    // a few pieces: one round trip each, in order; many: all at once
+    if (arrived == pieces) {
+        if (wb - wa < 4)
+            merge_segment<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
+        else
+            merge_segment_wide<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
+    }
 }
 
 template <int D, int BS, int G, int NW, int ST>
@@ -442,6 +534,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
 #else
     constexpr int kSnapCap = 3 * NW;
+#endif
+#ifdef PKV_DECODE_MIN_SHARE
+    constexpr int kMinShare = PKV_DECODE_MIN_SHARE;
+#else
+    constexpr int kMinShare = 4;
 #endif
     using Geo = DecodeGeometry<D, BS, G>;
     using Smem = DecodeSmem<NW, ST, D, BS, G>;
@@ -548,7 +645,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     // range itself and starts its block-table loads; the CTA-wide array of
     // ranges (for the merges) is filled after that. ----
     const int64_t T = cum[N];
-    const int C = gridDim.x;
+    // A small batch uses only as many CTAs as give every worker at least
+    // kMinShare chunks: a segment split into one-chunk pieces costs more to
+    // merge than the extra workers save.  The other CTAs have nothing to do.
+    const int C = (int)min((int64_t)gridDim.x, max((int64_t)1, (T + NW * kMinShare - 1) / (NW * kMinShare)));
+    if ((int)blockIdx.x >= C) return;
     const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
     int64_t gb, ge;
