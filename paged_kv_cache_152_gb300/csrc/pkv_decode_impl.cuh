@@ -682,24 +682,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     int2 tab_cur = table_entry(lane);
     int2 tab_nxt = table_entry(32 + lane);
 
-    for (int c = tid; c <= C; c += NW * 32)
-        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
-    __syncthreads();
-    // every warp counts itself out at the end; the last one advances the epoch
-    auto exit_warp = [&]() {
-        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
-            atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
-    };
-    if (n == 0) {
-        exit_warp();
-        return;
-    }
-    // shared partial slots: 16-byte aligned, after the bounds
-    float *part = nullptr;
-    if (p.smem_partials)
-        part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, epoch, count_now, cta_count, part};
-
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
     const unsigned char *wq = smem + Smem::kQ + (size_t)warp * ST * Geo::kSlotBytes;
@@ -784,6 +766,26 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
 
     int issued = 0;
     for (; issued < min(ST, n); ++issued) issue(issued);
+
+    // the CTA-wide ranges are needed only by the merges: fill them while the
+    // first chunks are in flight
+    for (int c = tid; c <= C; c += NW * 32)
+        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+    __syncthreads();
+    // every warp counts itself out at the end; the last one advances the epoch
+    auto exit_warp = [&]() {
+        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
+            atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
+    };
+    if (n == 0) {
+        exit_warp();
+        return;
+    }
+    // shared partial slots: 16-byte aligned, after the bounds
+    float *part = nullptr;
+    if (p.smem_partials)
+        part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
+    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, epoch, count_now, cta_count, part};
 
     const int gq = lane >> 2;
     const int tq = lane & 3;
