@@ -385,7 +385,7 @@ __device__ __forceinline__ void merge_segment_wide(const DecodeParams &p, const 
                                                    const SegInfo &si, int64_t wa, int64_t wb, int lane) {
     const bool sh = si.local && wc.part != nullptr;
     constexpr int PER = D / 32;
-    constexpr int U = G >= 4 ? 1 : 4 / G;  // pieces whose slices are loaded together
+    constexpr int U = G >= 8 ? 1 : (G >= 4 ? 2 : 4 / G);  // pieces whose slices are loaded together
     float M[G], L[G], O[G][PER];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
