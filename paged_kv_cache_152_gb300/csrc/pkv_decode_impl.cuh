@@ -44,7 +44,7 @@
 //    the segment, in worker
 //    order (deterministic, no float atomics, no second kernel).  Counters are
 //    tagged with an epoch kept in the workspace (see count_in_tagged): each
-//    call prepares the next call's counters and the last warp out advances
+//    call prepares the next call's counters and the last CTA out advances
 //    the epoch, so counting in is one atomic, a fresh or half-used workspace
 //    is tolerated, and a launch captured once and replayed works.
 //  * Rows past the context never reach the output: their scores are masked to
@@ -507,17 +507,17 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
     for (int64_t w = wa; w <= wb; ++w) pieces += wc.start(w) < wc.start(w + 1);
     int arrived = 0;
     if (si.local) {
-        __threadfence_block();  // the partial is visible to this CTA before it is counted
+        fence_acq_rel_cta();    // the partial is visible to this CTA before it is counted
         __syncwarp();
         if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % NW), 1) + 1;
         arrived = __shfl_sync(kFullMask, arrived, 0);
-        if (arrived == pieces) __threadfence_block();
+        if (arrived == pieces) fence_acq_rel_cta();
     } else {
-        __threadfence();        // the partial is visible device-wide before it is counted
+        fence_acq_rel_gpu();    // the partial is visible device-wide before it is counted
         __syncwarp();
         if (lane == 0) arrived = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, pieces);
         arrived = __shfl_sync(kFullMask, arrived, 0);
-        if (arrived == pieces) __threadfence();
+        if (arrived == pieces) fence_acq_rel_gpu();
     }
     // a few pieces: one round trip each, in order; many: all at once
     if (arrived == pieces) {
@@ -555,6 +555,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     int *ctx = cum + N + 1;
     int64_t *bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
     __shared__ int cta_count[NW];
+    __shared__ int exit_count;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -599,6 +600,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         epoch_s = (uint32_t)__ldcg(p.ws_sync);
     }
     if (tid < NW) cta_count[tid] = 0;
+    if (tid == 0) exit_count = 0;
     __syncthreads();
     if (warp == 0) {
         const int v = lane < NW ? warp_sums[lane] : 0;
@@ -772,9 +774,12 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     for (int c = tid; c <= C; c += NW * 32)
         bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
     __syncthreads();
-    // every warp counts itself out at the end; the last one advances the epoch
+    // every warp counts itself out at the end
+    // (the CTA's warps count out in shared memory; the last of them counts the
+    // CTA out of the grid, and the last CTA out advances the epoch)
     auto exit_warp = [&]() {
-        if (lane == 0 && count_in_tagged(p.ws_sync + 1 + parity, epoch, (int)W) == (int)W)
+        if (lane == 0 && atomicAdd(&exit_count, 1) == NW - 1 &&
+            count_in_tagged(p.ws_sync + 1 + parity, epoch, C) == C)
             atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
     };
     if (n == 0) {

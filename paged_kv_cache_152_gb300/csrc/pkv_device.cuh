@@ -75,6 +75,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later async-proxy (bulk copy) writes to the same buffer.
+// Acquire-release fences (lighter than the sequentially consistent
+// __threadfence): a release before a relaxed counter update, an acquire after
+// observing the final count.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_acq_rel_cta() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
