@@ -298,8 +298,8 @@ __device__ __forceinline__ SegInfo segment_info(const DecodeParams &p, const Wor
 template <int NW>
 __device__ __forceinline__ void segment_workers(const WorkerCtx<NW> &wc, const SegInfo &si, int64_t &wa,
                                                 int64_t &wb) {
-    wa = worker_of2(wc.bounds, wc.C, NW, si.g0);
-    wb = worker_of2(wc.bounds, wc.C, NW, si.g0 + si.nch - 1);
+    wa = worker_of_cta<NW>(wc.bounds, wc.C, si.g0, blockIdx.x);
+    wb = worker_of_cta<NW>(wc.bounds, wc.C, si.g0 + si.nch - 1, blockIdx.x);
 }
 
 // Partial (m, l, outputs) of worker w's piece that starts at chunk st, for

@@ -153,6 +153,27 @@ PKV_HD int64_t worker_of2(const int64_t *bounds, int C, int nw, int64_t g) {
     return (int64_t)lo * nw + (k < nw - 1 ? k : nw - 1);
 }
 
+// worker_of2 without its 64-bit division, for a compile-time NW: look in CTA
+// `hint` first (where a caller's own segments usually are), else binary-search
+// the CTA, then count the CTA's worker starts at or below g.  Same result as
+// worker_of2.
+template <int NW>
+PKV_HD int64_t worker_of_cta(const int64_t *bounds, int C, int64_t g, int hint) {
+    int c = hint;
+    if (!(bounds[c] <= g && g < bounds[c + 1])) {
+        int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (bounds[mid] <= g) lo = mid; else hi = mid;
+        }
+        c = lo;
+    }
+    const int64_t a = bounds[c], len = bounds[c + 1] - a;
+    int k = 0;
+    for (int j = 1; j < NW; ++j) k += (a + ((int64_t)j * len) / NW <= g) ? 1 : 0;
+    return (int64_t)c * NW + k;
+}
+
 // The order in which a worker walks its share [gb, ge): its cut pieces first
 // -- the last piece (when it runs past ge), then the first piece (when it
 // starts before gb) -- then everything between them in chunk order.  The

@@ -76,6 +76,17 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         CHECK(owner[g] >= 0, "uncovered chunk %lld", (long long)g);
         CHECK(wof(g) == owner[g], "worker_of(%lld)=%lld want %d (split %d)", (long long)g, (long long)wof(g),
               owner[g], split);
+        if (split == 1) {
+            // the constant-divisor search, from every hint CTA
+            for (int hint = 0; hint < C; hint += (C > 16 ? C / 7 : 1)) {
+                int64_t w2 = -1;
+                if (nw == 1) w2 = worker_of_cta<1>(bounds.data(), C, g, hint);
+                if (nw == 3) w2 = worker_of_cta<3>(bounds.data(), C, g, hint);
+                if (nw == 8) w2 = worker_of_cta<8>(bounds.data(), C, g, hint);
+                CHECK(w2 == owner[g], "worker_of_cta(%lld, hint %d)=%lld want %d", (long long)g, hint,
+                      (long long)w2, owner[g]);
+            }
+        }
         const ChunkPos p = locate_chunk(cum.data(), n, hkv, g);
         CHECK(p.s == truth[g].s && p.kvh == truth[g].kvh && p.c == truth[g].c && p.nch == truth[g].nch,
               "locate %lld", (long long)g);
