@@ -38,11 +38,11 @@
 //    in fp32, and splitting P into two fp16 terms keeps P.V at fp32 accuracy.
 //  * A piece that covers a whole (sequence, KV head) is normalised and written
 //    as fp16 by the warp.  A cut piece stores (max, sum, unnormalised output)
-//    in the workspace and counts itself in on its segment's counter -- in
-//    shared memory when the segment stays inside the CTA, else in the
-//    workspace; the warp that brings a count to the number of pieces merges
-//    the segment, in worker
-//    order (deterministic, no float atomics, no second kernel).  Counters are
+//    and adds its chunk count to its segment's counter -- partial and counter
+//    in shared memory when the segment stays inside the CTA, else in the
+//    workspace; the warp that brings the count to the segment's chunk count
+//    merges the segment, in worker order (deterministic, no float atomics,
+//    no second kernel).  Counters are
 //    tagged with an epoch kept in the workspace (see count_in_tagged): each
 //    call prepares the next call's counters and the last CTA out advances
 //    the epoch, so counting in is one atomic, a fresh or half-used workspace
@@ -228,29 +228,31 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     }
 }
 
-// Completion counters hold (epoch << 32 | arrivals).  Every call prepares the
+// Completion counters hold (epoch << 32 | count).  Every call prepares the
 // counters of the NEXT call (the other parity) as (epoch + 1, 0), so counting
 // in is normally a single atomic add.  A counter in any other state (a fresh
-// workspace, or one left by a call that gave up) is swung to (epoch, 1) by the
-// first arrival that sees it.  Returns this arrival's 1-based position out of
-// `total` arrivals.
-__device__ __forceinline__ int count_in_tagged(unsigned long long *cnt, uint32_t epoch, int total) {
+// workspace, or one left by a call that gave up) is swung to (epoch, amount)
+// by the first arrival that sees it.  Adds `amount` (> 0) towards `total` and
+// returns the count after this arrival: the arrival that returns `total` is
+// the last.
+__device__ __forceinline__ int count_in_tagged(unsigned long long *cnt, uint32_t epoch, int total, int amount) {
     const unsigned long long tag = (unsigned long long)epoch << 32;
     const unsigned long long kLow = 0xffffffffull;
+    const unsigned long long add = (unsigned long long)amount;
     auto valid = [&](unsigned long long v) { return (v & ~kLow) == tag && (v & kLow) < (unsigned long long)total; };
-    unsigned long long old = atomicAdd(cnt, 1ull);
-    if (valid(old)) return (int)(old & kLow) + 1;
-    unsigned long long cur = old + 1;
+    unsigned long long old = atomicAdd(cnt, add);
+    if (valid(old)) return (int)(old & kLow) + amount;
+    unsigned long long cur = old + add;
 #pragma unroll 1
     while (true) {
         if (valid(cur)) {
-            old = atomicAdd(cnt, 1ull);
-            if (valid(old)) return (int)(old & kLow) + 1;
-            cur = old + 1;
+            old = atomicAdd(cnt, add);
+            if (valid(old)) return (int)(old & kLow) + amount;
+            cur = old + add;
             continue;
         }
-        const unsigned long long prev = atomicCAS(cnt, cur, tag | 1ull);
-        if (prev == cur) return 1;
+        const unsigned long long prev = atomicCAS(cnt, cur, tag | add);
+        if (prev == cur) return amount;
         cur = prev;
     }
 }
@@ -267,6 +269,7 @@ struct WorkerCtx {
     int64_t W;               // workers in the grid
     int64_t T;               // chunks in the batch
     int64_t wid;             // this worker
+    int64_t gb, ge;          // its share
     uint32_t epoch;          // this call's epoch
     unsigned long long *count;  // this call's per-segment counters (global)
     int *cta_count;          // per-worker-slot counters of this CTA (shared)
@@ -501,26 +504,33 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
 template <int D, int G, int NW>
 __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
                                          const SegInfo &si, int lane) {
-    int64_t wa, wb;
-    segment_workers(wc, si, wa, wb);
-    int pieces = 0;
-    for (int64_t w = wa; w <= wb; ++w) pieces += wc.start(w) < wc.start(w + 1);
-    int arrived = 0;
+    // each piece counts in its chunks; the one that completes the segment's
+    // chunk count merges it (only the merger needs the list of pieces)
+    const int64_t lo = si.g0 > wc.gb ? si.g0 : wc.gb;
+    const int64_t hi = si.g0 + si.nch < wc.ge ? si.g0 + si.nch : wc.ge;
+    const int mine = (int)(hi - lo);
+    int done = 0;
     if (si.local) {
         fence_acq_rel_cta();    // the partial is visible to this CTA before it is counted
         __syncwarp();
-        if (lane == 0) arrived = atomicAdd(wc.cta_count + (wa % NW), 1) + 1;
-        arrived = __shfl_sync(kFullMask, arrived, 0);
-        if (arrived == pieces) fence_acq_rel_cta();
+        // the segment's first worker names its counter (a worker starts at
+        // most one cut segment)
+        if (lane == 0)
+            done = atomicAdd(wc.cta_count + worker_of_cta<NW>(wc.bounds, wc.C, si.g0, blockIdx.x) % NW, mine) + mine;
+        done = __shfl_sync(kFullMask, done, 0);
+        if (done == si.nch) fence_acq_rel_cta();
     } else {
         fence_acq_rel_gpu();    // the partial is visible device-wide before it is counted
         __syncwarp();
-        if (lane == 0) arrived = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, pieces);
-        arrived = __shfl_sync(kFullMask, arrived, 0);
-        if (arrived == pieces) fence_acq_rel_gpu();
+        if (lane == 0)
+            done = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, si.nch, mine);
+        done = __shfl_sync(kFullMask, done, 0);
+        if (done == si.nch) fence_acq_rel_gpu();
     }
-    // a few pieces: one round trip each, in order; many: all at once
-    if (arrived == pieces) {
+    if (done == si.nch) {
+        int64_t wa, wb;
+        segment_workers(wc, si, wa, wb);
+        // a few pieces: one round trip each, in order; many: all at once
         if (wb - wa < 4)
             merge_segment<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
         else
@@ -782,7 +792,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     // CTA out of the grid, and the last CTA out advances the epoch)
     auto exit_warp = [&]() {
         if (lane == 0 && atomicAdd(&exit_count, 1) == NW - 1 &&
-            count_in_tagged(p.ws_sync + 1 + parity, epoch, C) == C)
+            count_in_tagged(p.ws_sync + 1 + parity, epoch, C, 1) == C)
             atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
     };
     if (n == 0) {
@@ -793,7 +803,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     float *part = nullptr;
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, epoch, count_now, cta_count, part};
+    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, part};
 
     const int gq = lane >> 2;
     const int tq = lane & 3;
