@@ -659,10 +659,12 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     const int64_t T = cum[N];
     // A small batch uses only as many CTAs as give every worker at least
     // kMinShare chunks (a segment split into one-chunk pieces costs more to
-    // merge than the extra workers save), and no more CTAs than segments (then
-    // equal segments fall one per CTA and merge in shared memory).  The other
+    // merge than the extra workers save), and, while segments are short (up to
+    // 2 kMinShare chunks per worker), no more CTAs than segments: equal
+    // segments then fall one per CTA and merge in shared memory.  The other
     // CTAs have nothing to do.
-    const int C = (int)min(min((int64_t)gridDim.x, (int64_t)N * Hkv),
+    const int64_t seg_cap = max((int64_t)N * Hkv, (T + NW * 2 * kMinShare - 1) / (NW * 2 * kMinShare));
+    const int C = (int)min(min((int64_t)gridDim.x, seg_cap),
                            max((int64_t)1, (T + NW * kMinShare - 1) / (NW * kMinShare)));
     if ((int)blockIdx.x >= C) return;
     const int64_t W = (int64_t)C * NW;
