@@ -190,7 +190,8 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num
     if (!shape_supported(num_heads, num_kv_heads, head_dim, block_size)) return 0;
     Resolved r;
     if (resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r) != PKV_OK) return 0;
-    return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, num_heads / num_kv_heads, head_dim).total;
+    return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas, num_heads / num_kv_heads, head_dim)
+        .total;
 }
 
 extern "C" int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim, int block_size) {
@@ -231,7 +232,7 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     int rc = resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r);
     if (rc != PKV_OK) return rc;
     const int group = num_heads / num_kv_heads;
-    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, group, head_dim);
+    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas, group, head_dim);
     if (workspace_bytes < ws.total) return PKV_ERR_INVALID_ARG;
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
@@ -262,6 +263,8 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.context_lens = context_lens;
     p.ws_ml = reinterpret_cast<float *>(wsb + ws.ml);
     p.ws_acc = reinterpret_cast<float *>(wsb + ws.acc);
+    p.ws_cml = reinterpret_cast<float *>(wsb + ws.cml);
+    p.ws_cacc = reinterpret_cast<float *>(wsb + ws.cacc);
     p.ws_sync = reinterpret_cast<unsigned long long *>(wsb + ws.sync);
     p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count);
     p.status = dev_status;

@@ -273,6 +273,7 @@ struct WorkerCtx {
     uint32_t epoch;          // this call's epoch
     unsigned long long *count;  // this call's per-segment counters (global)
     int *cta_count;          // per-worker-slot counters of this CTA (shared)
+    int *cta_cross;          // counter of the segment that reaches in from before this CTA (shared)
     float *part;             // partial slots of this CTA's workers (shared), or NULL
 
     __device__ __forceinline__ int64_t start(int64_t w) const {
@@ -283,9 +284,12 @@ struct WorkerCtx {
 // Where segment (s, kvh) lies, and whether it lies inside this CTA's range
 // (then all its pieces are this CTA's, and they meet in shared memory).
 struct SegInfo {
-    int64_t g0;      // first chunk of the segment
-    int nch;         // its chunks
-    bool local;      // inside this CTA's range
+    int64_t g0;          // first chunk of the segment
+    int nch;             // its chunks
+    bool local;          // inside this CTA's range
+    int64_t p_lo, p_hi;  // the part of it in this CTA's range
+    int mine;            // chunks of it in this worker's share
+    int xw;              // 1 if it reaches in from before this CTA's range, else 0
 };
 
 template <int NW>
@@ -293,69 +297,77 @@ __device__ __forceinline__ SegInfo segment_info(const DecodeParams &p, const Wor
     SegInfo si;
     si.nch = (wc.cum[s + 1] - wc.cum[s]) / p.num_kv_heads;
     si.g0 = wc.cum[s] + (int64_t)kvh * si.nch;
-    si.local = si.g0 >= wc.bounds[blockIdx.x] && si.g0 + si.nch <= wc.bounds[blockIdx.x + 1];
+    const int64_t g1 = si.g0 + si.nch;
+    const int64_t c_lo = wc.bounds[blockIdx.x], c_hi = wc.bounds[blockIdx.x + 1];
+    si.local = si.g0 >= c_lo && g1 <= c_hi;
+    si.p_lo = si.g0 > c_lo ? si.g0 : c_lo;
+    si.p_hi = g1 < c_hi ? g1 : c_hi;
+    si.mine = (int)((g1 < wc.ge ? g1 : wc.ge) - (si.g0 > wc.gb ? si.g0 : wc.gb));
+    si.xw = si.g0 < c_lo ? 1 : 0;
     return si;
 }
 
-// First and last worker whose share meets the segment.
-template <int NW>
-__device__ __forceinline__ void segment_workers(const WorkerCtx<NW> &wc, const SegInfo &si, int64_t &wa,
-                                                int64_t &wb) {
-    wa = worker_of_cta<NW>(wc.bounds, wc.C, si.g0, blockIdx.x);
-    wb = worker_of_cta<NW>(wc.bounds, wc.C, si.g0 + si.nch - 1, blockIdx.x);
-}
-
-// Partial (m, l, outputs) of worker w's piece that starts at chunk st, for
-// head g: in this CTA's shared slots (segments that stay in the CTA, when
-// enabled) or in the workspace.
-struct PartialLoc {
-    float *ml;   // (max, sum)
-    float *acc;  // D outputs
+// A piece's partial: (max, sum) of head g at ml[2g], ml[2g + 1] and its
+// unnormalised outputs at acc[g * D ...]; in shared memory or in the workspace.
+struct PieceRef {
+    float *ml;
+    float *acc;
+    bool smem;
+    bool exists;
 };
 
+// Worker w's piece (which: 0 = the first piece of its share, 1 = the last):
+// in this CTA's shared slots when they are enabled (w is then one of this
+// CTA's workers), else in the workspace's worker slots.
 template <int D, int G, int NW>
-__device__ __forceinline__ PartialLoc partial_loc(const DecodeParams &p, const WorkerCtx<NW> &wc, bool shared_slot,
-                                                  int64_t w, int which, int g) {
-    if (shared_slot) {
+__device__ __forceinline__ PieceRef worker_piece(const DecodeParams &p, const WorkerCtx<NW> &wc, int64_t w,
+                                                 int which) {
+    if (wc.part != nullptr) {
         float *base = wc.part + ((w % NW) * 2 + which) * (G * (2 + D));
-        return {base + 2 * g, base + 2 * G + g * D};
+        return {base, base + 2 * G, true, true};
     }
-    const int64_t b = (w * 2 + which) * G + g;
-    return {p.ws_ml + b * 2, p.ws_acc + b * D};
+    const int64_t b = (w * 2 + which) * G;
+    return {p.ws_ml + b * 2, p.ws_acc + b * D, false, true};
 }
 
-// One warp merges the pieces of a cut segment, in worker order, combining
-// (max, sum, output) online: M' = max(M, m_p), X' = X 2^(M - M') + x_p 2^(m_p - M').
-// Each piece's (m, l) and output slice are loaded together (one round trip to
-// shared memory or L2 per piece); a segment has only a few pieces.
-template <int D, int G, int NW>
-__device__ __forceinline__ void merge_segment(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
-                                              const SegInfo &si, int64_t wa, int64_t wb, int lane) {
-    const bool sh = si.local && wc.part != nullptr;  // partials in shared memory
-    constexpr int PER = D / 32;                      // output elements per lane and head
+// CTA c's part of a segment that spans CTAs (which: 1 if the segment started
+// before the CTA's range, else 0 -- a CTA meets at most one of each).
+template <int D, int G>
+__device__ __forceinline__ PieceRef cta_piece(const DecodeParams &p, int64_t c, int which) {
+    const int64_t b = (c * 2 + which) * G;
+    return {p.ws_cml + b * 2, p.ws_cacc + b * D, false, true};
+}
+
+// A merge in progress, combining (max, sum, output) online:
+//     M' = max(M, m_p),  X' = X 2^(M - M') + x_p 2^(m_p - M')  for X = L, O.
+// Lane j holds output dims j*PER .. j*PER + PER - 1 of every head; M and L
+// are the same on all lanes.
+template <int D, int G>
+struct MergeState {
+    static constexpr int PER = D / 32;
     float M[G], L[G], O[G][PER];
+
+    __device__ __forceinline__ void init() {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        M[g] = -CUDART_INF_F;
-        L[g] = 0.f;
+        for (int g = 0; g < G; ++g) {
+            M[g] = -CUDART_INF_F;
+            L[g] = 0.f;
 #pragma unroll
-        for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
+            for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
+        }
     }
-#pragma unroll 1
-    for (int64_t w = wa; w <= wb; ++w) {
-        const int64_t st = wc.start(w);
-        if (st == wc.start(w + 1)) continue;
-        const int which = partial_slot(st, si.g0);
+
+    // Folds in one piece; its (m, l) and output slice are loaded together.
+    __device__ __forceinline__ void add(const PieceRef &r, int lane) {
         float2 ml[G];
         float a[G][PER];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const PartialLoc at = partial_loc<D, G, NW>(p, wc, sh, w, which, g);
-            const float2 *mlp = reinterpret_cast<const float2 *>(at.ml);
-            ml[g] = sh ? *mlp : __ldcg(mlp);
-            const float *src = at.acc + lane * PER;
+            const float2 *mp = reinterpret_cast<const float2 *>(r.ml) + g;
+            ml[g] = r.smem ? *mp : __ldcg(mp);
+            const float *src = r.acc + g * D + lane * PER;
 #pragma unroll
-            for (int k = 0; k < PER; ++k) a[g][k] = sh ? src[k] : __ldcg(src + k);
+            for (int k = 0; k < PER; ++k) a[g][k] = r.smem ? src[k] : __ldcg(src + k);
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -368,82 +380,91 @@ __device__ __forceinline__ void merge_segment(const DecodeParams &p, const Worke
             M[g] = mn;
         }
     }
+
+    // Normalised fp16 output rows of the KV group (s, kvh).
+    __device__ __forceinline__ void write_out(const DecodeParams &p, int s, int kvh, int lane) const {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
-        const float inv = 1.f / L[g];
+        for (int g = 0; g < G; ++g) {
+            __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
+            const float inv = 1.f / L[g];
 #pragma unroll
-        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] * inv);
+            for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] * inv);
+        }
+    }
+
+    // Stored as a partial, for the next level of the merge.
+    __device__ __forceinline__ void store(const PieceRef &r, int lane) const {
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) reinterpret_cast<float2 *>(r.ml)[g] = make_float2(M[g], L[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int k = 0; k < PER; ++k) r.acc[g * D + lane * PER + k] = O[g][k];
+    }
+};
+
+// Folds pieces 0 .. cnt-1 (ref(i) -> PieceRef) into st, in order, one round
+// trip per piece: for a few pieces, or for pieces in shared memory.
+template <int D, int G, class Ref>
+__device__ __forceinline__ void merge_seq(MergeState<D, G> &st, int cnt, Ref ref, int lane) {
+#pragma unroll 1
+    for (int i = 0; i < cnt; ++i) {
+        const PieceRef r = ref(i);
+        if (r.exists) st.add(r, lane);
     }
 }
 
-// The same merge for a segment cut into many pieces (small batches spread
-// over the whole grid): up to 32 pieces at a time, lane j fetches piece j's
-// (m, l) -- one round trip for all of them -- the warp reduces M and L with
-// shuffles, then sums the output slices in piece order with the loads of
-// several pieces in flight.  More than 32 pieces go round again, folding
-// each batch into the running (M, L, out).  Fixed order: deterministic.
-template <int D, int G, int NW>
-__device__ __forceinline__ void merge_segment_wide(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
-                                                   const SegInfo &si, int64_t wa, int64_t wb, int lane) {
-    const bool sh = si.local && wc.part != nullptr;
+// The same for many pieces, in the same order: up
+// to 32 pieces at a time, lane j fetches piece j's (m, l) -- one round trip
+// for all of them -- the warp reduces M and L with shuffles, then sums the
+// output slices in piece order with the loads of several pieces in flight.
+template <int D, int G, class Ref>
+__device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref ref, int lane) {
     constexpr int PER = D / 32;
     constexpr int U = G >= 8 ? 1 : (G >= 4 ? 2 : 4 / G);  // pieces whose slices are loaded together
-    float M[G], L[G], O[G][PER];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        M[g] = -CUDART_INF_F;
-        L[g] = 0.f;
-#pragma unroll
-        for (int k = 0; k < PER; ++k) O[g][k] = 0.f;
-    }
 #pragma unroll 1
-    for (int64_t w0 = wa; w0 <= wb; w0 += 32) {
-        const int cnt = (int)(wb - w0 + 1 < 32 ? wb - w0 + 1 : 32);
-        int which = 0;
-        bool has = false;
-        if (lane < cnt) {
-            const int64_t st = wc.start(w0 + lane);
-            has = st < wc.start(w0 + lane + 1);
-            which = partial_slot(st, si.g0);
-        }
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+        const int n = cnt - i0 < 32 ? cnt - i0 : 32;
+        PieceRef mine{nullptr, nullptr, false, false};
+        if (lane < n) mine = ref(i0 + lane);
         float wgt[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             float2 ml = make_float2(-CUDART_INF_F, 0.f);
-            if (has) {
-                const float2 *src =
-                    reinterpret_cast<const float2 *>(partial_loc<D, G, NW>(p, wc, sh, w0 + lane, which, g).ml);
-                ml = sh ? *src : __ldcg(src);
+            if (mine.exists) {
+                const float2 *mp = reinterpret_cast<const float2 *>(mine.ml) + g;
+                ml = mine.smem ? *mp : __ldcg(mp);
             }
             float mx = ml.x;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
-            const float mn = fmaxf(M[g], mx);  // some piece is non-empty: finite
-            const float f_old = exp2f(M[g] - mn);
-            wgt[g] = has ? exp2f(ml.x - mn) : 0.f;
+            const float mn = fmaxf(st.M[g], mx);  // some piece exists: finite
+            const float f_old = exp2f(st.M[g] - mn);
+            wgt[g] = mine.exists ? exp2f(ml.x - mn) : 0.f;
             float ls = ml.y * wgt[g];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
-            L[g] = L[g] * f_old + ls;
-            M[g] = mn;
+            st.L[g] = st.L[g] * f_old + ls;
+            st.M[g] = mn;
 #pragma unroll
-            for (int k = 0; k < PER; ++k) O[g][k] *= f_old;
+            for (int k = 0; k < PER; ++k) st.O[g][k] *= f_old;
         }
 #pragma unroll 1
-        for (int j0 = 0; j0 < cnt; j0 += U) {
+        for (int j0 = 0; j0 < n; j0 += U) {
             float a[U][G][PER], f[U][G];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int j = j0 + u < cnt ? j0 + u : cnt - 1;
-                const int wj = __shfl_sync(kFullMask, which, j);
-                const bool use = j0 + u < cnt && __shfl_sync(kFullMask, has, j);
+                const int j = j0 + u < n ? j0 + u : n - 1;
+                const PieceRef r = ref(i0 + j);
+                const bool use = j0 + u < n && r.exists;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     f[u][g] = __shfl_sync(kFullMask, wgt[g], j);
-                    const float *src = partial_loc<D, G, NW>(p, wc, sh, w0 + j, wj, g).acc + lane * PER;
+                    const float *src = r.acc + g * D + lane * PER;
 #pragma unroll
-                    for (int k = 0; k < PER; ++k) a[u][g][k] = use ? (sh ? src[k] : __ldcg(src + k)) : 0.f;
+                    for (int k = 0; k < PER; ++k) a[u][g][k] = use ? (r.smem ? src[k] : __ldcg(src + k)) : 0.f;
                 }
             }
 #pragma unroll
@@ -451,21 +472,14 @@ __device__ __forceinline__ void merge_segment_wide(const DecodeParams &p, const 
 #pragma unroll
                 for (int g = 0; g < G; ++g)
 #pragma unroll
-                    for (int k = 0; k < PER; ++k) O[g][k] += a[u][g][k] * f[u][g];
+                    for (int k = 0; k < PER; ++k) st.O[g][k] += a[u][g][k] * f[u][g];
         }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + lane * PER;
-        const float inv = 1.f / L[g];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(O[g][k] * inv);
     }
 }
 
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
-// stored partial; the caller counts it in later (count_in).
+// stored partial; the caller counts it in (count_in).
 template <int D, int G, int NW>
 __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx<NW> &wc, const int4 md, float m,
                                              float l, const float (&o)[D / 8][4], SegInfo &si, int lane) {
@@ -486,56 +500,89 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
     }
     si = segment_info(p, wc, s, kvh);
     if (g < G) {
-        const PartialLoc at = partial_loc<D, G, NW>(p, wc, si.local && wc.part != nullptr, wc.wid,
-                                                (flags & kSlot1) ? 1 : 0, g);
-        float *dst = at.acc + 2 * t;
+        const PieceRef at = worker_piece<D, G, NW>(p, wc, wc.wid, (flags & kSlot1) ? 1 : 0);
+        float *dst = at.acc + g * D + 2 * t;
 #pragma unroll
         for (int j = 0; j < D / 8; ++j) *reinterpret_cast<float2 *>(dst + 8 * j) = make_float2(o[j][0], o[j][1]);
-        if (t == 0) *reinterpret_cast<float2 *>(at.ml) = make_float2(m, l);
+        if (t == 0) reinterpret_cast<float2 *>(at.ml)[g] = make_float2(m, l);
     }
     return true;
 }
 
-// Counts a stored partial of segment (s, kvh) in; the piece that completes
-// the count merges the segment.  Pieces of a segment that stays inside this
-// CTA meet on a shared-memory counter with CTA-scope ordering; a segment that
-// spans CTAs (only one longer than the CTA boundary could snap past) meets on
-// the workspace's epoch-tagged counter with GPU-scope ordering.
+// Counts a stored partial of segment (s, kvh) in, in two levels.
+//  1. The pieces in this CTA's range (the whole segment, if it stays in the
+//     CTA) count their chunks in on a shared-memory counter; the piece that
+//     completes the CTA's part merges that part -- from shared memory.
+//  2. A segment that spans CTAs: the part goes to the CTA's slot in the
+//     workspace and its chunks count in on the segment's device-wide counter;
+//     the CTA completing the segment merges the parts, in CTA order.
+// A segment cut into many pieces thus merges at most a CTA's pieces from
+// shared memory plus one part per CTA from L2.
 template <int D, int G, int NW>
 __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
                                          const SegInfo &si, int lane) {
-    // each piece counts in its chunks; the one that completes the segment's
-    // chunk count merges it (only the merger needs the list of pieces)
-    const int64_t lo = si.g0 > wc.gb ? si.g0 : wc.gb;
-    const int64_t hi = si.g0 + si.nch < wc.ge ? si.g0 + si.nch : wc.ge;
-    const int mine = (int)(hi - lo);
-    int done = 0;
+    const int64_t g1 = si.g0 + si.nch;
+    const int64_t p_lo = si.p_lo, p_hi = si.p_hi;
+    const int part = (int)(p_hi - p_lo);
+    const int mine = si.mine;
+    const int xw = si.xw;  // this CTA's cross slot for the segment (if it spans CTAs)
+    if (part != mine) {
+        fence_acq_rel_cta();  // the partial is visible to this CTA before it is counted
+        __syncwarp();
+        int done = 0;
+        if (lane == 0) {
+            // a worker starts at most one cut segment inside its CTA, and a CTA
+            // meets at most one segment from before its range
+            int *ctr = xw ? wc.cta_cross : wc.cta_count + (worker_of_cta<NW>(wc.bounds, wc.C, p_lo, blockIdx.x) % NW);
+            done = atomicAdd(ctr, mine) + mine;
+        }
+        done = __shfl_sync(kFullMask, done, 0);
+        if (done != part) return;
+        fence_acq_rel_cta();
+    }
+    const int64_t wa = worker_of_cta<NW>(wc.bounds, wc.C, p_lo, blockIdx.x);
+    const int64_t wb = worker_of_cta<NW>(wc.bounds, wc.C, p_hi - 1, blockIdx.x);
+    auto wref = [&](int i) -> PieceRef {
+        const int64_t w = wa + i;
+        const int64_t st = wc.start(w);
+        PieceRef r = worker_piece<D, G, NW>(p, wc, w, partial_slot(st, si.g0));
+        r.exists = st < wc.start(w + 1);
+        return r;
+    };
+    MergeState<D, G> ms;
+    ms.init();
+    const int cnt = (int)(wb - wa + 1);
+    if (cnt <= 4 || wc.part != nullptr)
+        merge_seq<D, G>(ms, cnt, wref, lane);
+    else
+        merge_wide<D, G>(ms, cnt, wref, lane);
     if (si.local) {
-        fence_acq_rel_cta();    // the partial is visible to this CTA before it is counted
-        __syncwarp();
-        // the segment's first worker names its counter (a worker starts at
-        // most one cut segment)
-        if (lane == 0)
-            done = atomicAdd(wc.cta_count + worker_of_cta<NW>(wc.bounds, wc.C, si.g0, blockIdx.x) % NW, mine) + mine;
-        done = __shfl_sync(kFullMask, done, 0);
-        if (done == si.nch) fence_acq_rel_cta();
-    } else {
-        fence_acq_rel_gpu();    // the partial is visible device-wide before it is counted
-        __syncwarp();
-        if (lane == 0)
-            done = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, si.nch, mine);
-        done = __shfl_sync(kFullMask, done, 0);
-        if (done == si.nch) fence_acq_rel_gpu();
+        ms.write_out(p, s, kvh, lane);
+        return;
     }
-    if (done == si.nch) {
-        int64_t wa, wb;
-        segment_workers(wc, si, wa, wb);
-        // a few pieces: one round trip each, in order; many: all at once
-        if (wb - wa < 4)
-            merge_segment<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
-        else
-            merge_segment_wide<D, G, NW>(p, wc, s, kvh, si, wa, wb, lane);
-    }
+    ms.store(cta_piece<D, G>(p, blockIdx.x, xw), lane);
+    fence_acq_rel_gpu();  // the part is visible device-wide before it is counted
+    __syncwarp();
+    int done = 0;
+    if (lane == 0) done = count_in_tagged(wc.count + (int64_t)s * p.num_kv_heads + kvh, wc.epoch, si.nch, part);
+    done = __shfl_sync(kFullMask, done, 0);
+    if (done != si.nch) return;
+    fence_acq_rel_gpu();
+    const int ca = cta_of(wc.bounds, wc.C, si.g0, blockIdx.x);
+    const int cb = cta_of(wc.bounds, wc.C, g1 - 1, blockIdx.x);
+    auto cref = [&](int i) -> PieceRef {
+        const int64_t c = ca + i;
+        PieceRef r = cta_piece<D, G>(p, c, si.g0 < wc.bounds[c] ? 1 : 0);
+        r.exists = wc.bounds[c] < wc.bounds[c + 1];
+        return r;
+    };
+    MergeState<D, G> ms2;
+    ms2.init();
+    if (cb - ca < 4)
+        merge_seq<D, G>(ms2, cb - ca + 1, cref, lane);
+    else
+        merge_wide<D, G>(ms2, cb - ca + 1, cref, lane);
+    ms2.write_out(p, s, kvh, lane);
 }
 
 template <int D, int BS, int G, int NW, int ST>
@@ -566,6 +613,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     int64_t *bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
     __shared__ int cta_count[NW];
     __shared__ int exit_count;
+    __shared__ int cta_cross;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -610,7 +658,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         epoch_s = (uint32_t)__ldcg(p.ws_sync);
     }
     if (tid < NW) cta_count[tid] = 0;
-    if (tid == 0) exit_count = 0;
+    if (tid == 0) {
+        exit_count = 0;
+        cta_cross = 0;
+    }
     __syncthreads();
     if (warp == 0) {
         const int v = lane < NW ? warp_sums[lane] : 0;
@@ -805,7 +856,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     float *part = nullptr;
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, part};
+    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part};
 
     const int gq = lane >> 2;
     const int tq = lane & 3;

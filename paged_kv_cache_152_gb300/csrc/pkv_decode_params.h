@@ -27,8 +27,10 @@ struct DecodeParams {
     __half *value_cache_w;
     const int32_t *block_tables;  // [N][MB]
     const int32_t *context_lens;  // [N]
-    float *ws_ml;                 // [W][2][G][2] partial (max, sum)
+    float *ws_ml;                 // [W][2][G][2] partial (max, sum) of a worker's piece
     float *ws_acc;                // [W][2][G][D] partial unnormalised outputs
+    float *ws_cml;                // [C][2][G][2] a CTA's part of a segment that spans CTAs
+    float *ws_cacc;               // [C][2][G][D]
     // Completion counters, each (epoch << 32 | arrivals): ws_sync[0] is the
     // epoch word, ws_sync[1 + parity] the per-call exit counters, and ws_count
     // two arrays (by epoch parity) of N*Hkv per-segment counters.
@@ -49,15 +51,18 @@ struct DecodeParams {
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
 struct DecodeWorkspace {
-    size_t sync, count, ml, acc, total;
-    static DecodeWorkspace plan(int num_seqs, int num_kv_heads, int64_t workers, int group, int head_dim) {
+    size_t sync, count, ml, acc, cml, cacc, total;
+    static DecodeWorkspace plan(int num_seqs, int num_kv_heads, int64_t workers, int64_t ctas, int group,
+                                int head_dim) {
         auto up = [](size_t x) { return (x + 255) / 256 * 256; };
         DecodeWorkspace w;
         w.sync = 0;
         w.count = 256;
         w.ml = w.count + up(2 * 8 * (size_t)num_seqs * num_kv_heads);
         w.acc = w.ml + up(4 * (size_t)workers * 2 * group * 2);
-        w.total = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
+        w.cml = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
+        w.cacc = w.cml + up(4 * (size_t)ctas * 2 * group * 2);
+        w.total = w.cacc + up(4 * (size_t)ctas * 2 * group * head_dim);
         return w;
     }
 };

@@ -157,17 +157,21 @@ PKV_HD int64_t worker_of2(const int64_t *bounds, int C, int nw, int64_t g) {
 // `hint` first (where a caller's own segments usually are), else binary-search
 // the CTA, then count the CTA's worker starts at or below g.  Same result as
 // worker_of2.
+// The CTA whose range holds chunk g (0 <= g < T): `hint` when it does, else
+// the largest c with bounds[c] <= g.
+PKV_HD int cta_of(const int64_t *bounds, int C, int64_t g, int hint) {
+    if (bounds[hint] <= g && g < bounds[hint + 1]) return hint;
+    int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (bounds[mid] <= g) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
 template <int NW>
 PKV_HD int64_t worker_of_cta(const int64_t *bounds, int C, int64_t g, int hint) {
-    int c = hint;
-    if (!(bounds[c] <= g && g < bounds[c + 1])) {
-        int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (bounds[mid] <= g) lo = mid; else hi = mid;
-        }
-        c = lo;
-    }
+    const int c = cta_of(bounds, C, g, hint);
     const int64_t a = bounds[c], len = bounds[c + 1] - a;
     int k = 0;
     for (int j = 1; j < NW; ++j) k += (a + ((int64_t)j * len) / NW <= g) ? 1 : 0;
