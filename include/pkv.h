@@ -104,8 +104,12 @@ int pkv_version(void);
  *   context_lens int32 [num_seqs]
  *   scale        softmax scale (host value), usually 1/sqrt(head_dim)
  *   num_ctas     persistent grid size; 0 = one full wave (SM count x CTAs
- *                per SM).  Any value >= 1 gives the same result within
- *                rounding; 1 makes every sequence a single pass.
+ *                per SM).  A small batch leaves some of them idle (every
+ *                worker warp gets at least 4 chunks of 16 rows; while the
+ *                (sequence, KV head) segments are short, no more CTAs work
+ *                than there are segments).  Any value >= 1 gives the same
+ *                result within rounding; 1 makes every sequence a single
+ *                pass.
  *   workspace    device scratch of at least pkv_decode_workspace_size(...)
  *                bytes for the same (num_seqs, num_heads, num_kv_heads,
  *                head_dim, block_size, num_ctas); 256-byte aligned.  It
