@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
 #ifdef PKV_DECODE_SNAP_CAP
     constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
 #else
-    constexpr int kSnapCap = 3 * NW;
+    constexpr int kSnapCap = NW;  // one chunk per warp of the CTA
 #endif
 #ifdef PKV_DECODE_MIN_SHARE
     constexpr int kMinShare = PKV_DECODE_MIN_SHARE;

@@ -113,10 +113,11 @@ PKV_HD int partial_slot(int64_t st, int64_t g0) {
 
 // Two-level split.  The T chunks are first divided among C CTAs: CTA c's
 // nominal start c*T/C moves to the nearest segment boundary when one lies
-// within snap = min(T/(4C), snap_cap) chunks, so that a segment is normally
-// read by one CTA only (moving a boundary by d chunks costs the CTA's warps
-// d/NW chunks each; a segment cut across CTAs costs two warps a device-wide
-// count and merge, worth a few chunks -- hence a small absolute cap).  Each
+// within snap = min(T/(4C), snap_cap) chunks, so that fewer segments are read
+// by two CTAs (moving a boundary by d chunks costs the CTA's warps d/NW
+// chunks each; a segment cut across CTAs costs a device-wide count and a
+// merge of the CTAs' parts, worth about a chunk per warp -- hence a small
+// absolute cap, one chunk per warp in the decode kernel).  Each
 // CTA's range is then divided equally among its NW warps: worker w = c*NW + k.
 PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_t c, int64_t C, int64_t T,
                                  int64_t snap_cap) {

@@ -41,7 +41,7 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
     CHECK((int64_t)truth.size() == T, "T");
     if (T == 0) return;
     const int C = (int)(W / nw);
-    const int64_t snap_cap = 3 * nw;
+    const int64_t snap_cap = nw;  // as in the decode kernel
     std::vector<int64_t> bounds(C + 1);
     if (split == 1) {
         for (int c = 0; c <= C; ++c)
