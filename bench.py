@@ -7,12 +7,15 @@ Prints ONE JSON line (rank 0).  Workload (default): 7B-class decode, one layer
 of 16, context lengths uniform integers in [50, 900], pool 1.25x the blocks
 needed with tables assigned from a shuffled free list (workloads.decode_7b).
 
-One step = one pass of the whole device hot path over the batch:
-reshape_and_cache of the decode step's new token of every sequence, then
-paged decode attention (one kernel; split pieces are merged inside it).  The
-workload has no copy-on-write pair at its decode step, so copy_blocks
-launches nothing.  By default the two launches are captured once as CUDA
-graphs and replayed every step (--no-graph: direct binding calls).
+One step = one pass of the whole device hot path over the batch: the
+decode step's new token of every sequence is written into its slot (the
+block table's position context_len - 1) and paged decode attention runs over
+the whole context, in ONE launch (paged_attention_decode_append; split
+pieces are merged inside it).  --two-launch runs the write as its own
+reshape_and_cache launch before a read-only decode instead.  The workload
+has no copy-on-write pair at its decode step, so copy_blocks launches
+nothing.  The step's launches are captured once as CUDA graphs and replayed
+every step (--no-graph: direct binding calls).
 
 * value: KV bytes the decode reads (2 * sum(ctx) * Hkv * D * 2) per step,
   times K steps, over the device-timed K steps (CUDA events, barrier +
@@ -78,8 +81,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    p.add_argument("--fused-append", action="store_true",
-                   help="one launch per step: the decode launch writes the new tokens itself")
+    p.add_argument("--two-launch", action="store_true",
+                   help="reshape_and_cache, then a decode that only reads (instead of the decode launch "
+                        "that writes the new tokens itself)")
     p.add_argument("--no-graph", action="store_true",
                    help="launch every step directly instead of replaying captured CUDA graphs")
     p.add_argument("--identity-tables", action="store_true",
@@ -406,7 +410,7 @@ def run_pkv(args):
     e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
     st = build_state(args.config, device, args.identity_tables, e2e_headroom_steps=e2e_steps,
                      block_size=args.block_size)
-    if args.fused_append:
+    if not args.two_launch:
         st["fused"] = True
         st["launches_per_step"] -= 1
     wl = st["wl"]
@@ -426,7 +430,7 @@ def run_pkv(args):
     stream = torch.cuda.current_stream()
     graphs = None
     if not args.no_graph:
-        # (with --fused-append and no copy-on-write pairs there is no cache-write launch)
+        # (with the fused launch and no copy-on-write pairs there is no cache-write launch)
         has_write = not (st.get("fused") and not st["pairs"].shape[0])
         g_write, g_dec = (torch.cuda.CUDAGraph() if has_write else None), torch.cuda.CUDAGraph()
         if has_write:
@@ -515,13 +519,16 @@ def run_pkv(args):
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches * world,
         "launch_mode": ("direct binding calls" if args.no_graph else
-                        "CUDA graphs (cache write graph + decode graph replayed per step)") +
-                       ("; decode launch appends the new tokens (no separate cache write)" if args.fused_append
-                        else ""),
+                        "CUDA graphs replayed per step") +
+                       ("; reshape_and_cache launch, then a read-only decode launch" if args.two_launch
+                        else "; one decode launch per step that also writes the new tokens "
+                             "(paged_attention_decode_append)"),
         "host_us_per_step": round(host_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pkv_paged_attention_decode (paged_decode_kernel, merge fused)",
+                     "kernel": ("pkv_paged_attention_decode (paged_decode_kernel, merge fused)" if args.two_launch
+                                else "pkv_paged_attention_decode_append (paged_decode_kernel: writes the new "
+                                     "tokens, merge fused)"),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "decode_ms_mean": round(dec_mean, 5),
