@@ -450,3 +450,24 @@ def test_decode_plan_equals_direct_calls(pkv, name, kw):
         assert torch.equal(planned.t["key_cache"].view(torch.int16), direct.t["key_cache"].view(torch.int16))
     plan.close()
     read_only.close()
+
+
+@pytest.mark.parametrize("d,h,hkv,bs,lens", [
+    (128, 4, 4, 16, [16384]),           # group 1: 1,024-chunk segments over many CTAs, partials in shared memory
+    (128, 16, 4, 32, [9000, 40, 5000]),  # group 4
+    (128, 16, 2, 16, [12000, 7]),        # group 8 at head_dim 128: partials in the workspace
+    (64, 8, 2, 16, [20000]),             # head_dim 64
+])
+@pytest.mark.parametrize("num_ctas", [0, 37, 300])
+def test_segments_spanning_many_ctas(pkv, d, h, hkv, bs, lens, num_ctas):
+    """Long segments cut over many workers and CTAs: pieces merge within each
+    CTA, then the CTAs' parts merge; same result as the oracle, and the same
+    bits from launch to launch."""
+    rng = np.random.default_rng(77 + d + h + len(lens))
+    q, kc, vc, tables, lens_a = _random_case(rng, len(lens), h, hkv, d, bs, lens)
+    scale = d ** -0.5
+    ref = OA.paged_decode_attention(q, kc, vc, tables, lens_a, scale)
+    out, st = _run_gpu(pkv, q, kc, vc, tables, lens_a, scale, num_ctas)
+    assert st == 0 and np.max(np.abs(out - ref)) <= TOL
+    out2, st2 = _run_gpu(pkv, q, kc, vc, tables, lens_a, scale, num_ctas)
+    assert st2 == 0 and np.array_equal(out, out2)
