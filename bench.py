@@ -25,9 +25,10 @@ every step (--no-graph: direct binding calls).
   the C++ block manager appends one token per sequence and exports the tables
   into the step's pinned staging region (with its queries and new K/V rows),
   one host->device copy moves it, one DecodePlan launch appends the new
-  tokens and attends, the output comes back device->host, stream sync.
-* roofline: decode launch (both kernels) timed alone with CUDA events on its
-  stream over the timed region; algorithmic bytes / mean duration vs the
+  tokens and attends, the output comes back device->host, stream sync; the
+  next step's block-manager work overlaps the GPU's work on this step.
+* roofline: the decode launch timed alone with CUDA events on its stream
+  over the timed region; algorithmic bytes / mean duration vs the
   measured HBM copy bandwidth.
 * cpu_baseline: the fp64 oracle on the host cores, on a bounded sample of the
   same workload.
@@ -321,7 +322,9 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     host->device copy moves the region; copy-on-write pairs (if any) go
     through copy_blocks; one launch of a DecodePlan (built once: append the
     new tokens + attend, paged_attention_decode_append) runs the step; the
-    output comes back device->host and the stream is synchronised."""
+    output comes back device->host and the stream is synchronised.  The
+    block-manager work of step i+1 runs on the host while the GPU runs step
+    i (as a serving loop schedules ahead)."""
     import numpy as np
     import torch
     wl, alloc = st["wl"], st["alloc"]
@@ -368,16 +371,22 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     kv_per_token = 2 * hkv * d * 2
     bytes_total = 0
     h2d = d2h = 0
+    def prepare(i):
+        """Host work of step i: the block manager appends one token per
+        sequence and writes the tables and lengths into step i's region."""
+        _, pairs = alloc.append_batch(batch, slots_out=h_slots, pairs_out=h_pairs32)
+        alloc.export(batch, mb, tables_out=tab_np[i], lens_out=lens_np[i])
+        return pairs.copy() if len(pairs) else None
+
     barrier(dist, device)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    pairs = prepare(0)
     for i in range(steps):
-        _, pairs = alloc.append_batch(batch, slots_out=h_slots, pairs_out=h_pairs32)
-        alloc.export(batch, mb, tables_out=tab_np[i], lens_out=lens_np[i])
         bytes_total += int(lens_np[i].sum()) * kv_per_token
         d_stage.copy_(h_rows[i], non_blocking=True)
         h2d += step_bytes
-        if len(pairs):
+        if pairs is not None:
             h_pairs_t.numpy()[:len(pairs)] = pairs
             d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
             h2d += len(pairs) * 16
@@ -385,6 +394,10 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
         plan.launch_raw(sh)
         h_out.copy_(st["out"], non_blocking=True)
         d2h += h_out.numel() * 2
+        # the next step's block-manager work runs on the host while the GPU
+        # runs this step (it does not depend on this step's output values)
+        if i + 1 < steps:
+            pairs = prepare(i + 1)
         stream.synchronize()
     elapsed = time.perf_counter() - t0
     elapsed = max_over_ranks(dist, elapsed, device)
@@ -542,7 +555,8 @@ def run_pkv(args):
                        "includes": "host block manager append + table export into the step's pinned staging "
                                    "region (queries, new K/V, tables, lengths), one H2D copy of it, one "
                                    "DecodePlan launch (append new tokens + attend), D2H of the output, stream "
-                                   "sync per step"}
+                                   "sync per step; the next step's block-manager work overlaps this step's GPU "
+                                   "work"}
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
     if dist is not None:
