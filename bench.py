@@ -89,6 +89,9 @@ def parse_args(argv=None):
                    help="launch every step directly instead of replaying captured CUDA graphs")
     p.add_argument("--identity-tables", action="store_true",
                    help="same workload with each sequence's blocks contiguous and in order")
+    p.add_argument("--layers", type=int, default=0,
+                   help="measure a model step instead: this many layers, each with its own pools, one "
+                        "decode launch per layer, all layers captured as one CUDA graph")
     p.add_argument("--swap", action="store_true",
                    help="measure swapping instead: every sequence's blocks device -> pinned host -> device")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -564,6 +567,86 @@ def run_pkv(args):
     return line
 
 
+def run_layers(args):
+    """A model's decode step over `--layers` layers, each with its own K/V
+    pools (same tables: one block id spans all layers): one decode launch per
+    layer (the one that also writes the layer's new token), all captured as
+    one CUDA graph so that programmatic dependent launch lets each layer's
+    prologue overlap the previous layer's tail.  value = KV bytes read by all
+    layers per step / step time."""
+    import torch
+    import paged_kv_cache_152_gb300 as pkv
+    import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_152_gb300 import build as b
+    b.build()
+    pkv.load()
+    st = build_state(args.config, device, block_size=args.block_size)
+    wl, t = st["wl"], st["t"]
+    L = args.layers
+    shape = tuple(t["key_cache"].shape)
+    caches = [(t["key_cache"], t["value_cache"])]
+    for layer in range(1, L):
+        caches.append((W.normal_fp16_large(shape, wl.seed * 1000 + 100 + 2 * layer, device),
+                       W.normal_fp16_large(shape, wl.seed * 1000 + 101 + 2 * layer, device)))
+    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
+                           args.num_ctas, device)
+    plans = [pkv.DecodePlan(st["out"], t["query"], kc, vc, st["tables"], st["lens"], wl.scale, key=t["key"],
+                            value=t["value"], num_ctas=args.num_ctas, workspace=ws, status=st["status"])
+             for kc, vc in caches]
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        for pl in plans:
+            pl.launch()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for pl in plans:
+            pl.launch()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
+    steps = max(1, min(args.steps, 200))
+    clocks = ClockSampler(0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
+    total_ms = e0.elapsed_time(e1)
+    step_ms = statistics.fmean(a.elapsed_time(z) for a, z in ev)
+    kv = wl.kv_read_bytes() * L
+    peak, peak_kind = measured_hbm_peak()
+    value = kv * steps / (total_ms / 1e3) / 1e9
+    return {
+        "metric": METRIC + " (model step over all layers)",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / steps, 5), "higher_is_better": True, "dtype": "f32",
+        "storage_dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.config] + f"; {L} layers, each with its own pools",
+                   "layers": L, "kv_bytes_per_step": kv, "block_size": wl.block_size,
+                   "launch_mode": "one CUDA graph per step: one decode launch per layer (writes the layer's new "
+                                  "token, then attends), programmatic dependent launch between layers"},
+        "per_layer_us": round(step_ms * 1e3 / L, 3),
+        "seqs_per_s_per_layer": round(wl.num_seqs * L * steps / (total_ms / 1e3), 1),
+        "pct_of_peak": round(100 * value / peak, 2),
+        "peak": peak, "peak_kind": peak_kind,
+        "gpu_launches": L * steps,
+        "clocks": clocks.finish(),
+    }
+
+
 def run_swap(args):
     """Swapping, measured on its own: the block manager swaps every sequence
     of the workload out to a page-locked host pool and back in; the kernel
@@ -787,6 +870,8 @@ def main(argv=None):
         line = run_reference(args)
     elif args.swap:
         line = run_swap(args)
+    elif args.layers:
+        line = run_layers(args)
     else:
         line = run_pkv(args)
     if line is not None:
