@@ -10,12 +10,14 @@
 // table lookup is fused into the attention kernel (no separate gather pass).
 //
 // Design (GB300, HBM-bound: each K/V byte is read once):
-//  * The batch's work is cut into chunks of up to 16 rows of one (sequence, KV
-//    head) (pkv_schedule.h) and split among the CTAs of a persistent grid,
-//    with CTA boundaries moved to segment boundaries where one is near, then
-//    into equal contiguous shares, one per WARP.  Every warp is an
-//    independent worker; there is no CTA-wide synchronisation after the
-//    prologue.  A worker walks the cut
+//  * The batch's work is cut into chunks of 16 rows of one (sequence, KV head)
+//    -- a "segment" -- (pkv_schedule.h; at block size 8 a chunk spans two
+//    blocks) and split among the CTAs of a persistent grid, with CTA
+//    boundaries moved to a segment boundary within one chunk per warp, then
+//    into equal contiguous shares, one per WARP.  A small batch uses fewer
+//    CTAs (at least 4 chunks per warp; while segments are short, at most one
+//    CTA per segment).  Every warp is an independent worker; there is no
+//    CTA-wide synchronisation after the prologue.  A worker walks the cut
 //    pieces at the two ends of its share first, so segments cut between
 //    workers are merged early, under the rest of the stream, not at the tail.
 //  * Each warp owns a ring of ST stages in shared memory.  Lane 0 issues, ST
@@ -23,7 +25,8 @@
 //    swizzle) per cache of the chunk's K and V rows -- the cache is viewed as
 //    [halves][rows][64 dims] so one box lands the whole 16-row chunk in the
 //    swizzled [half][row][128 B] tile; a short last chunk (<= 8 rows) takes
-//    one 8-row box per half; boxes never leave the chunk's block -- plus, at
+//    one 8-row box per half, and at block size 8 every block one 8-row box
+//    per half; boxes never leave a block -- plus, at
 //    the first chunk of each piece, a bulk copy of the KV group's query rows,
 //    all completing on the stage's mbarrier.
 //    Block-table entries for the next 32 chunks are prefetched one per lane.
@@ -36,17 +39,22 @@
 //    layout, so P never leaves registers.  Scores are in log2 units and the
 //    softmax is online, per warp, in fp32.  Products of fp16 inputs are exact
 //    in fp32, and splitting P into two fp16 terms keeps P.V at fp32 accuracy.
-//  * A piece that covers a whole (sequence, KV head) is normalised and written
-//    as fp16 by the warp.  A cut piece stores (max, sum, unnormalised output)
-//    and adds its chunk count to its segment's counter -- partial and counter
-//    in shared memory when the segment stays inside the CTA, else in the
-//    workspace; the warp that brings the count to the segment's chunk count
-//    merges the segment, in worker order (deterministic, no float atomics,
-//    no second kernel).  Counters are
-//    tagged with an epoch kept in the workspace (see count_in_tagged): each
-//    call prepares the next call's counters and the last CTA out advances
-//    the epoch, so counting in is one atomic, a fresh or half-used workspace
-//    is tolerated, and a launch captured once and replayed works.
+//  * A piece that covers a whole segment is normalised and written as fp16
+//    by the warp.  A cut piece stores (max, sum, unnormalised output) and adds
+//    its chunk count to a counter; merges go in two levels (see count_in):
+//    the pieces in one CTA's range meet in shared memory and the one that
+//    completes the CTA's part merges it; a segment that spans CTAs then
+//    counts the CTAs' parts in device-wide, and the CTA completing it merges
+//    the parts.  Fixed order throughout (deterministic, no float atomics, no
+//    second kernel).  The device-wide counters are tagged with an epoch kept
+//    in the workspace (see count_in_tagged): each call prepares the next
+//    call's counters and the last CTA out advances the epoch, so counting in
+//    is one atomic, a fresh or half-used workspace is tolerated, and a launch
+//    captured once and replayed works.
+//  * With new K/V rows given (pkv_paged_attention_decode_append), the last
+//    chunk of each segment also brings the row of the decode step's token:
+//    the warp patches it into the tile before the math and stores it to the
+//    cache.
 //  * Rows past the context never reach the output: their scores are masked to
 //    -inf, and in a ragged chunk the warp zeroes those V rows in shared memory
 //    before P.V (whatever the cache holds there, 0 * it stays 0).
