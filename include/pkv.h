@@ -128,7 +128,14 @@ int pkv_version(void);
  * A context longer than max_blocks_per_seq*block_size, or a table entry
  * outside [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in dev_status; such a
  * context is clamped to its table and such an entry reads block 0.
- * Launches one kernel on `stream`.
+ * Launches one kernel on `stream`, with programmatic dependent launch: it may
+ * start while the preceding kernel in the stream finishes, and reads
+ * context_lens and block_tables before it waits for that kernel (everything
+ * else — the caches, query, workspace, out — only after).  So context_lens
+ * and block_tables must not be written by a kernel that signals its
+ * dependents early (griddepcontrol.launch_dependents /
+ * cudaTriggerProgrammaticLaunchCompletion) before it writes them; memory
+ * copies, ordinary kernels and this library's kernels never do.
  */
 int pkv_paged_attention_decode(void *out, const void *query,
                                const void *key_cache, const void *value_cache,

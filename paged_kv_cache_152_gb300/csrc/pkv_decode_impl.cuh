@@ -635,8 +635,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         prefetch_tensormap(&p.tmap_k8);
         prefetch_tensormap(&p.tmap_v8);
     }
-    grid_dependency_wait();
-    launch_dependents();
+    // Up to the grid-dependency wait below, the kernel reads only the context
+    // lengths and the block tables (inputs of the call, never written by the
+    // library's kernels): with programmatic dependent launch, the prologue,
+    // the shares and the first table loads overlap the tail of the preceding
+    // kernel in the stream.
 
     // ---- prologue: chunk counts per sequence and their prefix sums ----------
     const int per = (N + NW * 32 - 1) / (NW * 32);
@@ -659,11 +662,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         if (lane >= o) incl += y;
     }
     if (lane == 31) warp_sums[warp] = incl;
-    __shared__ uint32_t epoch_s;
     if (tid == 0) {
         for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), 1);
         fence_barrier_init();
-        epoch_s = (uint32_t)__ldcg(p.ws_sync);
     }
     if (tid < NW) cta_count[tid] = 0;
     if (tid == 0) {
@@ -692,24 +693,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         if (tid == 0) cum[N] = grand_total;
     }
     __syncthreads();
-    // this call counts on the counters of its epoch's parity, and prepares the
-    // other parity's counters for the next call
-    const uint32_t epoch = epoch_s;
-    const int parity = epoch & 1;
-    unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;
-    {
-        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * N * Hkv;
-        const unsigned long long next_tag = (unsigned long long)(epoch + 1) << 32;
-        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)gridDim.x * NW * 32)
-            count_next[i] = next_tag;
-        if (blockIdx.x == 0 && tid == 0) p.ws_sync[1 + (parity ^ 1)] = next_tag;
-    }
-    // rows of empty contexts are zero; no worker visits them
-    for (int s = blockIdx.x; s < N; s += gridDim.x) {
-        if (ctx[s] != 0) continue;
-        uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)s * p.num_heads * D);
-        for (int i = tid; i < p.num_heads * D / 8; i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
-    }
 
     // ---- this warp's share: CTA ranges snapped to segment boundaries, each
     // divided equally among the CTA's warps.  A warp works out its own CTA's
@@ -841,13 +824,37 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     };
 
     int issued = 0;
-    for (; issued < min(ST, n); ++issued) issue(issued);
-
-    // the CTA-wide ranges are needed only by the merges: fill them while the
-    // first chunks are in flight
+    // the CTA-wide ranges (needed only by the merges)
     for (int c = tid; c <= C; c += NW * 32)
         bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
     __syncthreads();
+
+    // ---- from here on the kernel reads and writes what the preceding kernel
+    // may write: the caches, the workspace, the output ----
+    grid_dependency_wait();
+    launch_dependents();
+    for (; issued < min(ST, n); ++issued) issue(issued);
+    // this call counts on the counters of its epoch's parity, and prepares the
+    // other parity's counters for the next call (the epoch only changes when
+    // every CTA of a call is out, so every warp of this call reads the same)
+    uint32_t epoch = 0;
+    if (lane == 0) epoch = (uint32_t)__ldcg(p.ws_sync);
+    epoch = __shfl_sync(kFullMask, epoch, 0);
+    const int parity = epoch & 1;
+    unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;
+    {
+        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * N * Hkv;
+        const unsigned long long next_tag = (unsigned long long)(epoch + 1) << 32;
+        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)C * NW * 32)
+            count_next[i] = next_tag;
+        if (blockIdx.x == 0 && tid == 0) p.ws_sync[1 + (parity ^ 1)] = next_tag;
+    }
+    // rows of empty contexts are zero; no worker visits them
+    for (int s = blockIdx.x; s < N; s += C) {
+        if (ctx[s] != 0) continue;
+        uint4 *row = reinterpret_cast<uint4 *>(p.out + (int64_t)s * p.num_heads * D);
+        for (int i = tid; i < p.num_heads * D / 8; i += NW * 32) row[i] = make_uint4(0, 0, 0, 0);
+    }
     // every warp counts itself out at the end
     // (the CTA's warps count out in shared memory; the last of them counts the
     // CTA out of the grid, and the last CTA out advances the epoch)
