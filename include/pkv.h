@@ -164,7 +164,8 @@ int pkv_paged_attention_decode(void *out, const void *query,
  *
  *   key, value   fp16 [num_seqs][num_kv_heads][head_dim] (device)
  *   key_cache, value_cache  written at the new tokens' slots (device)
- * Other arguments, workspace and errors as pkv_paged_attention_decode.
+ * Other arguments, workspace, errors and launch ordering (which inputs are
+ * read before the wait for the preceding kernel) as pkv_paged_attention_decode.
  */
 int pkv_paged_attention_decode_append(void *out, const void *query,
                                       const void *key, const void *value,
