@@ -14,7 +14,10 @@
 //    -- a "segment" -- (pkv_schedule.h; at block size 8 a chunk spans two
 //    blocks) and split among the CTAs of a persistent grid, with CTA
 //    boundaries moved to a segment boundary within one chunk per warp, then
-//    into equal contiguous shares, one per WARP.  A small batch uses fewer
+//    into contiguous shares, one per WARP: equal, except that a warp whose
+//    piece is cut across a CTA boundary (it also counts that piece in
+//    device-wide, and may merge the CTAs' parts) gives up a few chunks to the
+//    CTA's other warps.  A small batch uses fewer
 //    CTAs (at least 4 chunks per warp; while segments are short, at most one
 //    CTA per segment).  Every warp is an independent worker; there is no
 //    CTA-wide synchronisation after the prologue.  A worker walks the cut
@@ -140,11 +143,18 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     const int rr = lane & 7;    // which row of it
 
     // ---- S^T = Q . K^T ------------------------------------------------------
-    float s[Geo::kNT][4];
+    // (even and odd K steps accumulate separately: two dependent mma chains of
+    // half the length, summed at the end -- when K/V come from L2 the warp's
+    // latency per chunk is what bounds it)
+    float s[Geo::kNT][4], s2[Geo::kNT][4];
 #pragma unroll
-    for (int nt = 0; nt < Geo::kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < Geo::kNT; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+    }
 #pragma unroll
     for (int kk = 0; kk < Geo::kKSteps; ++kk) {
+        float(*acc)[4] = (kk & 1) ? s2 : s;
         // matrices: (n-tile mi>>1, dims 16kk + 8(mi&1)); the row's 16-byte chunk
         // c sits at c ^ (row & 7) in the swizzled tile
         const int nt = (Geo::kNT == 2) ? (mi >> 1) : 0;
@@ -154,14 +164,18 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
         if (Geo::kNT == 2) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(addr, b0, b1, b2, b3);
-            mma_16816(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-            mma_16816(s[Geo::kNT - 1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+            mma_16816(acc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_16816(acc[Geo::kNT - 1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
         } else {
             uint32_t b0, b1;
             ldsm_x2(addr, b0, b1);
-            mma_16816(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_16816(acc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < Geo::kNT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[nt][j] += s2[nt][j];
 
     // ---- online softmax (per query head; rows past R masked) ----------------
     float x[Geo::kNT][2];
@@ -283,9 +297,16 @@ struct WorkerCtx {
     int *cta_count;          // per-worker-slot counters of this CTA (shared)
     int *cta_cross;          // counter of the segment that reaches in from before this CTA (shared)
     float *part;             // partial slots of this CTA's workers (shared), or NULL
+    int64_t lo, len;         // this CTA's range [lo, lo + len)
+    int r0, r1;              // chunks its first / last worker give up (cta_share_start)
 
+    // first chunk of worker w, one of this CTA's workers or the next CTA's first
     __device__ __forceinline__ int64_t start(int64_t w) const {
-        return w >= W ? T : worker_start2(bounds, NW, w);
+        return cta_share_start(lo, len, NW, (int)(w - (int64_t)blockIdx.x * NW), r0, r1);
+    }
+    // this CTA's worker whose share holds chunk g (lo <= g < lo + len)
+    __device__ __forceinline__ int64_t worker_of(int64_t g) const {
+        return (int64_t)blockIdx.x * NW + worker_in_cta<NW>(lo, len, g, r0, r1);
     }
 };
 
@@ -541,15 +562,15 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
         if (lane == 0) {
             // a worker starts at most one cut segment inside its CTA, and a CTA
             // meets at most one segment from before its range
-            int *ctr = xw ? wc.cta_cross : wc.cta_count + (worker_of_cta<NW>(wc.bounds, wc.C, p_lo, blockIdx.x) % NW);
+            int *ctr = xw ? wc.cta_cross : wc.cta_count + (wc.worker_of(p_lo) % NW);
             done = atomicAdd(ctr, mine) + mine;
         }
         done = __shfl_sync(kFullMask, done, 0);
         if (done != part) return;
         fence_acq_rel_cta();
     }
-    const int64_t wa = worker_of_cta<NW>(wc.bounds, wc.C, p_lo, blockIdx.x);
-    const int64_t wb = worker_of_cta<NW>(wc.bounds, wc.C, p_hi - 1, blockIdx.x);
+    const int64_t wa = wc.worker_of(p_lo);
+    const int64_t wb = wc.worker_of(p_hi - 1);
     auto wref = [&](int i) -> PieceRef {
         const int64_t w = wa + i;
         const int64_t st = wc.start(w);
@@ -604,6 +625,16 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     constexpr int kMinShare = PKV_DECODE_MIN_SHARE;
 #else
     constexpr int kMinShare = 4;
+#endif
+#ifdef PKV_DECODE_RELIEF
+    constexpr int kRelief = PKV_DECODE_RELIEF;
+#else
+    constexpr int kRelief = 4;  // chunks a worker with a piece cut across CTAs gives up
+#endif
+#ifdef PKV_DECODE_RELIEF_DIV
+    constexpr int kReliefDiv = PKV_DECODE_RELIEF_DIV;
+#else
+    constexpr int kReliefDiv = 16;  // ... at most 1/16 of a nominal share
 #endif
     using Geo = DecodeGeometry<D, BS, G>;
     using Smem = DecodeSmem<NW, ST, D, BS, G>;
@@ -695,7 +726,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     __syncthreads();
 
     // ---- this warp's share: CTA ranges snapped to segment boundaries, each
-    // divided equally among the CTA's warps.  A warp works out its own CTA's
+    // divided among the CTA's warps (cta_share_start).  A warp works out its own CTA's
     // range itself and starts its block-table loads; the CTA-wide array of
     // ranges (for the merges) is filled after that. ----
     const int64_t T = cum[N];
@@ -711,13 +742,20 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     if ((int)blockIdx.x >= C) return;
     const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
-    int64_t gb, ge;
+    int64_t gb, ge, c_lo, c_len;
+    int r0, r1;
     {
+        // lane 0: the CTA range's start, lane 1: its end (and whether each
+        // cuts a segment)
         const int c = (int)blockIdx.x + (lane & 1);
         const int64_t v = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
-        const int64_t lo = __shfl_sync(kFullMask, v, 0), hi = __shfl_sync(kFullMask, v, 1);
-        gb = lo + ((int64_t)warp * (hi - lo)) / NW;        // = worker_start2(bounds, NW, wid)
-        ge = lo + ((int64_t)(warp + 1) * (hi - lo)) / NW;  // = the next worker's start (T past the last)
+        c_lo = __shfl_sync(kFullMask, v, 0);
+        c_len = __shfl_sync(kFullMask, v, 1) - c_lo;
+        const int r = cut_relief(cum, N, Hkv, v, T, c_len, NW, kRelief, kReliefDiv);
+        r0 = __shfl_sync(kFullMask, r, 0);
+        r1 = __shfl_sync(kFullMask, r, 1);
+        gb = cta_share_start(c_lo, c_len, NW, warp, r0, r1);
+        ge = cta_share_start(c_lo, c_len, NW, warp + 1, r0, r1);
     }
     const int n = gb < ge ? (int)(ge - gb) : 0;
 
@@ -871,7 +909,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     float *part = nullptr;
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part};
+    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
+                           c_lo, c_len, r0, r1};
 
     const int gq = lane >> 2;
     const int tq = lane & 3;

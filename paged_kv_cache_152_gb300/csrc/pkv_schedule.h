@@ -141,6 +141,41 @@ PKV_HD int64_t worker_start2(const int64_t *bounds, int nw, int64_t w) {
     return a + (k * len) / nw;
 }
 
+// Start of worker k (0 <= k <= nw) of a CTA whose range is [a, a + len):
+// equal shares, except that the first worker gives up r0 chunks and the last
+// r1, spread evenly over the workers between them (nw >= 3).  A worker whose
+// piece is cut across a CTA boundary also counts that piece in device-wide
+// and may merge the CTAs' parts -- a few round trips to L2 that its share
+// makes up for.  Callers pass r0, r1 <= len / (2 nw) (cut_relief), so starts
+// never decrease.
+PKV_HD int64_t cta_share_start(int64_t a, int64_t len, int nw, int k, int r0, int r1) {
+    const int64_t st = a + ((int64_t)k * len) / nw;
+    if (k == 0 || k == nw || nw < 3) return st;
+    return st - r0 + ((int64_t)(k - 1) * (r0 + r1)) / (nw - 2);
+}
+
+// Relief for one end of a CTA range of len chunks when the CTA boundary at
+// chunk b (0 < b < T) lies inside a segment: `relief` chunks, but at most
+// 1/div of a nominal share (the cut costs a fixed time, so short shares give
+// up less); else 0.  div >= 2.
+PKV_HD int cut_relief(const int *cum, int n, int num_kv_heads, int64_t b, int64_t T, int64_t len, int nw,
+                      int relief, int div) {
+    if (relief <= 0 || nw < 3 || b <= 0 || b >= T) return 0;
+    const int64_t cap = len / ((int64_t)div * nw);
+    const int r = cap < relief ? (int)cap : relief;
+    if (r <= 0) return 0;
+    return locate_chunk(cum, n, num_kv_heads, b).c != 0 ? r : 0;
+}
+
+// The worker k of that CTA (0 <= k < NW) whose share holds chunk g,
+// a <= g < a + len (the last one when empty shares start at g).
+template <int NW>
+PKV_HD int worker_in_cta(int64_t a, int64_t len, int64_t g, int r0, int r1) {
+    int k = 0;
+    for (int j = 1; j < NW; ++j) k += (cta_share_start(a, len, NW, j, r0, r1) <= g) ? 1 : 0;
+    return k;
+}
+
 // Largest w (of C*nw workers) with worker_start2(w) <= g, 0 <= g < T.
 PKV_HD int64_t worker_of2(const int64_t *bounds, int C, int nw, int64_t g) {
     int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]

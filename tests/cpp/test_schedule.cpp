@@ -1,6 +1,7 @@
 // Exhaustive CPU check of the decode kernel's work split (pkv_schedule.h).
 // Built and run by tests/test_native_host.py.  Exits non-zero on the first
 // violation, printing it.
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
@@ -13,21 +14,32 @@
 using namespace pkv;
 
 static int fails = 0;
+static long relieved = 0;  // CTA ends where a relief applied (the test must exercise it)
 #define CHECK(c, ...) do { if (!(c)) { std::printf("FAIL %s:%d: ", __FILE__, __LINE__); \
     std::printf(__VA_ARGS__); std::printf("\n"); if (++fails > 5) std::exit(1); } } while (0)
 
 // split 0: equal shares over all W workers; split 1: snapped CTA ranges of
-// nw workers each (W = C * nw).
+// nw workers each (W = C * nw), divided equally (relief 0) or with the first
+// and last worker giving up `relief` chunks where their CTA boundary cuts a
+// segment.
 static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W, int split,
-                           int nw);
+                           int nw, int relief = 0);
 
 static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W) {
     run_case_split(ctx, hkv, bs, sr, mb, W, 0, 1);
     for (int nw : {1, 3, 8}) run_case_split(ctx, hkv, bs, sr, mb, ((W + nw - 1) / nw) * nw, 1, nw);
+    for (int nw : {3, 8})
+        for (int relief : {1, 2, 1000}) run_case_split(ctx, hkv, bs, sr, mb, ((W + nw - 1) / nw) * nw, 1, nw, relief);
+}
+
+template <int NW>
+static int worker_in_cta_rt(int nw, int64_t a, int64_t len, int64_t g, int r0, int r1) {
+    CHECK(nw == NW, "nw");
+    return worker_in_cta<NW>(a, len, g, r0, r1);
 }
 
 static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W, int split,
-                           int nw) {
+                           int nw, int relief) {
     const int n = (int)ctx.size();
     std::vector<int> cum(n + 1, 0);
     for (int s = 0; s < n; ++s) cum[s + 1] = cum[s] + hkv * chunks_for(ctx[s], sr);
@@ -57,12 +69,50 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
             CHECK(p.c > snap && p.nch - p.c > snap, "boundary left inside a short segment");
         }
     }
+    // reliefs of each CTA's first and last worker
+    std::vector<int> r0(C, 0), r1(C, 0);
+    if (split == 1 && relief > 0) {
+        for (int c = 0; c < C; ++c) {
+            const int64_t a = bounds[c], len = bounds[c + 1] - a;
+            r0[c] = cut_relief(cum.data(), n, hkv, a, T, len, nw, relief, 2);
+            r1[c] = cut_relief(cum.data(), n, hkv, a + len, T, len, nw, relief, 2);
+            relieved += (r0[c] > 0) + (r1[c] > 0);
+            for (int end = 0; end < 2; ++end) {
+                const int r = end ? r1[c] : r0[c];
+                const int64_t b = end ? a + len : a;
+                const bool cuts = b > 0 && b < T && locate_chunk(cum.data(), n, hkv, b).c != 0;
+                const int64_t cap = nw >= 3 ? std::min<int64_t>(relief, len / (2 * nw)) : 0;
+                CHECK(r == (cuts ? cap : 0), "relief %d at boundary %lld", r, (long long)b);
+            }
+            CHECK(cta_share_start(a, len, nw, 0, r0[c], r1[c]) == a &&
+                      cta_share_start(a, len, nw, nw, r0[c], r1[c]) == a + len,
+                  "relief shares do not span the CTA range");
+            // the first and last worker give up exactly their relief
+            if (nw >= 3) {
+                CHECK(cta_share_start(a, len, nw, 1, r0[c], r1[c]) == a + len / nw - r0[c], "first share");
+                CHECK(cta_share_start(a, len, nw, nw - 1, r0[c], r1[c]) == a + ((nw - 1) * len) / nw + r1[c],
+                      "last share");
+            }
+        }
+    }
     auto wstart = [&](int64_t w) -> int64_t {
         if (split == 0) return worker_start(w, W, T);
-        return w >= W ? T : worker_start2(bounds.data(), nw, w);
+        if (w >= W) return T;
+        if (relief > 0) {
+            const int64_t c = w / nw;
+            return cta_share_start(bounds[c], bounds[c + 1] - bounds[c], nw, (int)(w % nw), r0[c], r1[c]);
+        }
+        return worker_start2(bounds.data(), nw, w);
     };
     auto wof = [&](int64_t g) -> int64_t {
         if (split == 0) return worker_of(g, W, T);
+        if (relief > 0) {
+            const int c = cta_of(bounds.data(), C, g, 0);
+            const int64_t a = bounds[c], len = bounds[c + 1] - a;
+            const int k = nw == 3 ? worker_in_cta_rt<3>(nw, a, len, g, r0[c], r1[c])
+                                  : worker_in_cta_rt<8>(nw, a, len, g, r0[c], r1[c]);
+            return (int64_t)c * nw + k;
+        }
         return worker_of2(bounds.data(), C, nw, g);
     };
     // ranges partition [0, T)
@@ -76,7 +126,7 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         CHECK(owner[g] >= 0, "uncovered chunk %lld", (long long)g);
         CHECK(wof(g) == owner[g], "worker_of(%lld)=%lld want %d (split %d)", (long long)g, (long long)wof(g),
               owner[g], split);
-        if (split == 1) {
+        if (split == 1 && relief == 0) {
             // the constant-divisor search, from every hint CTA
             for (int hint = 0; hint < C; hint += (C > 16 ? C / 7 : 1)) {
                 int64_t w2 = -1;
@@ -233,7 +283,8 @@ int main() {
     run_case({1}, 1, 16, 16, 1, 1000);
     run_case({0, 5, 0, 0, 17, 0}, 3, 16, 16, 2, 3);
     run_case({4096, 256, 1000}, 8, 32, 16, 128, 1216);
+    CHECK(relieved > 1000, "relief exercised only %ld times", relieved);
     if (fails) { std::printf("%d failures\n", fails); return 1; }
-    std::printf("schedule ok: %d random cases\n", cases);
+    std::printf("schedule ok: %d random cases (%ld relieved CTA ends)\n", cases, relieved);
     return 0;
 }
