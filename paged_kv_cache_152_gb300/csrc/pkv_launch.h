@@ -1,10 +1,11 @@
 // pkv_launch.h -- kernel launch with programmatic dependent launch enabled.
 //
-// The kernel may begin while the previous kernel on the stream is finishing;
-// every kernel of this library calls grid_dependency_wait() (griddepcontrol.wait)
-// before touching global memory, so results are the same as with plain
-// stream ordering.  After a non-kernel operation (a copy, an event wait) the
-// launch simply waits as usual.
+// The kernel may begin while the previous kernel on the stream is finishing.
+// The cache kernels call grid_dependency_wait() (griddepcontrol.wait) before
+// touching global memory; the decode kernel reads only the context lengths
+// and block tables before it (include/pkv.h states that contract), so results
+// are the same as with plain stream ordering.  After a non-kernel operation
+// (a copy, an event wait) the launch simply waits as usual.
 #ifndef PKV_LAUNCH_H
 #define PKV_LAUNCH_H
 
