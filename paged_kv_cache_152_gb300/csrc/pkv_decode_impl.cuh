@@ -32,7 +32,10 @@
 //    per half; boxes never leave a block -- plus, at
 //    the first chunk of each piece, a bulk copy of the KV group's query rows,
 //    all completing on the stage's mbarrier.
-//    Block-table entries for the next 32 chunks are prefetched one per lane.
+//    Block-table entries are prefetched one per lane a window of 32 chunks
+//    ahead; when a window starts, each lane turns its entry into the chunk's
+//    copy descriptor (rows, flags, cache rows), so issuing a chunk is a few
+//    shuffles and the copies.
 //  * Math on the tensor cores, one warp per chunk: query heads on M (G of the
 //    16 rows used), rows of the chunk on N, head_dim on K:
 //        S^T[16 x rows] = Q[16 x D] . K^T       (mma.sync m16n8k16, fp32 acc)
@@ -763,7 +766,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     const ShareOrder order = share_order(cum, N, Hkv, gb, ge);
 
     // block-table entry of the chunk at walk position i (raw; validated when
-    // used), 0 past the share
+    // its descriptor is built), 0 past the share
     // (at block size 8 a chunk spans two blocks: the second entry comes in the
     // high half, 0 when the chunk does not reach it)
     auto table_entry = [&](int i) -> int2 {
@@ -775,9 +778,38 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[q.s]) second = __ldg(row + lb + 1);
         return make_int2(__ldg(row + lb), second);
     };
+    const bool append = p.new_key != nullptr;
+    // Descriptor of the chunk at walk position i, built by one lane for a
+    // window of 32 positions at a time (lane j: position win + j) from its
+    // table entry `tab`: x = sequence | KV head << 16, y = rows | flags << 8,
+    // z / w = the cache row of its box (of each block's box at block size 8).
+    // Issuing a chunk is then a few shuffles and the copies.
+    auto chunk_desc = [&](int i, int2 tab) -> int4 {
+        if (i >= n) return make_int4(0, 0, 0, 0);
+        const int64_t g = order.at(i);
+        const ChunkPos q = locate_chunk(cum, N, Hkv, g);
+        int phys = tab.x, phys2 = tab.y;
+        if (phys < 0 || phys >= p.num_blocks) {
+            report(p.status, PKV_ERR_OUT_OF_RANGE);
+            phys = 0;
+        }
+        if (phys2 < 0 || phys2 >= p.num_blocks) {
+            report(p.status, PKV_ERR_OUT_OF_RANGE);
+            phys2 = 0;
+        }
+        const int rows = chunk_rows(q.c, ctx[q.s], Geo::kRows);
+        // the decode step's new token is the last row of the segment's last chunk
+        const bool new_row = append && q.c == q.nch - 1;
+        const int flags = chunk_flags(q, g, gb, ge) | (new_row ? kAppendRow : 0);
+        // row of the cache viewed as [num_blocks * Hkv * BS rows]
+        const int y = (int)(((int64_t)phys * Hkv + q.kvh) * BS + (q.c * Geo::kRows) % BS);
+        const int y2 = (int)(((int64_t)phys2 * Hkv + q.kvh) * BS);
+        return make_int4(q.s | (q.kvh << 16), rows | (flags << 8), y, y2);
+    };
     int win = 0;
-    int2 tab_cur = table_entry(lane);
-    int2 tab_nxt = table_entry(32 + lane);
+    const int2 tab0 = table_entry(lane);  // window 0's entries, loading
+    int2 tab_nxt = table_entry(32 + lane);  // window 1's
+    int4 desc;  // descriptors of window win (window 0's are built below)
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
@@ -785,37 +817,25 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     const uint32_t wq_a = smem_addr(wq);
     const uint32_t bar_a = smem_addr(bars + warp * ST);
     int4 *wmeta = meta + 2 * warp * ST;
-    const bool append = p.new_key != nullptr;
-
-    ChunkPos pos;  // chunk being issued
 
     auto issue = [&](int i) {
-        const int64_t g = order.at(i);
-        if (order.jumps_at(i))
-            pos = locate_chunk(cum, N, Hkv, g);
-        else
-            next_chunk(pos, cum, N, Hkv);
-        if (i - win >= 32) {
+        if (i == win + 32) {
+            // next window: its descriptors from the entries loaded one window
+            // ago, then the loads for the window after it
             win += 32;
-            tab_cur = tab_nxt;
+            desc = chunk_desc(win + lane, tab_nxt);
             tab_nxt = table_entry(win + 32 + lane);
         }
-        int phys = __shfl_sync(kFullMask, tab_cur.x, i - win);
-        int phys2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, tab_cur.y, i - win) : 0;
+        const int j = i - win;
+        const int sk = __shfl_sync(kFullMask, desc.x, j);
+        const int rf = __shfl_sync(kFullMask, desc.y, j);
+        const int y = __shfl_sync(kFullMask, desc.z, j);
+        const int y2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, desc.w, j) : 0;
         if (lane == 0) {
-            if (phys < 0 || phys >= p.num_blocks) {
-                report(p.status, PKV_ERR_OUT_OF_RANGE);
-                phys = 0;
-            }
-            if (phys2 < 0 || phys2 >= p.num_blocks) {
-                report(p.status, PKV_ERR_OUT_OF_RANGE);
-                phys2 = 0;
-            }
+            const int s = sk & 0xffff, kvh = sk >> 16;
+            const int rows = rf & 0xff, flags = rf >> 8;
+            const bool new_row = (flags & kAppendRow) != 0;
             const int stage = i % ST;
-            const int rows = chunk_rows(pos.c, ctx[pos.s], Geo::kRows);
-            // the decode step's new token is the last row of the segment's last chunk
-            const bool new_row = append && pos.c == pos.nch - 1;
-            const int flags = chunk_flags(pos, g, gb, ge) | (new_row ? kAppendRow : 0);
             const uint32_t bar = bar_a + stage * 8;
             const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
             const uint32_t vdst = kdst + Geo::kTileBytes;
@@ -825,12 +845,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             // (the second lands 8 rows down, at +1 KB in each half)
             const bool short_box = Geo::kBPC == 2 || rows <= 8;
             const bool second = Geo::kBPC == 2 && rows > 8;
-            // row of the cache viewed as [num_blocks * Hkv * BS rows]
-            const int y = (int)(((int64_t)phys * Hkv + pos.kvh) * BS + (pos.c * Geo::kRows) % BS);
-            const int y2 = (int)(((int64_t)phys2 * Hkv + pos.kvh) * BS);
-            wmeta[2 * stage] = make_int4(pos.s, pos.kvh, rows, flags);
+            wmeta[2 * stage] = make_int4(s, kvh, rows, flags);
             wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
-            fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
                                                   : 2 * Geo::kTileBytes) +
                                            ((flags & kFirst) ? Geo::kQBytes : 0) +
@@ -850,10 +866,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
                 }
             }
             if (flags & kFirst)
-                bulk_g2s(wq_a + stage * Geo::kSlotBytes,
-                         p.query + ((int64_t)pos.s * p.num_heads + pos.kvh * G) * D, Geo::kQBytes, bar);
+                bulk_g2s(wq_a + stage * Geo::kSlotBytes, p.query + ((int64_t)s * p.num_heads + kvh * G) * D,
+                         Geo::kQBytes, bar);
             if (new_row) {
-                const int64_t src = ((int64_t)pos.s * Hkv + pos.kvh) * D;
+                const int64_t src = ((int64_t)s * Hkv + kvh) * D;
                 bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
                 bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes + Geo::kRowBytes, p.new_value + src,
                          Geo::kRowBytes, bar);
@@ -865,6 +881,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     // the CTA-wide ranges (needed only by the merges)
     for (int c = tid; c <= C; c += NW * 32)
         bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+    // window 0's descriptors (the table entries have arrived meanwhile)
+    desc = chunk_desc(lane, tab0);
     __syncthreads();
 
     // ---- from here on the kernel reads and writes what the preceding kernel
@@ -971,6 +989,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             }
             __syncwarp();
         }
+        // The stage's tiles were written through the generic proxy (zeroed tail
+        // rows, the new row): order those writes before the TMA copy that
+        // refills this stage (issued after the __syncwarp below).  Reads need
+        // no fence: every ldmatrix has delivered before the mma that uses it.
+        if (md.z < Geo::kRows || (md.w & kAppendRow)) fence_proxy_async_smem();
         const uint32_t kt = wst_a + stage * Geo::kStageBytes;
         consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
         // refill the stage first: a piece's finish (and a cut piece's count and
