@@ -751,10 +751,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         // lane 0: the CTA range's start, lane 1: its end (and whether each
         // cuts a segment)
         const int c = (int)blockIdx.x + (lane & 1);
-        const int64_t v = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+        bool cuts = false;
+        const int64_t v = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap, &cuts);
         c_lo = __shfl_sync(kFullMask, v, 0);
         c_len = __shfl_sync(kFullMask, v, 1) - c_lo;
-        const int r = cut_relief(cum, N, Hkv, v, T, c_len, NW, kRelief, kReliefDiv);
+        const int r = cut_relief_for(cuts, c_len, NW, kRelief, kReliefDiv);
         r0 = __shfl_sync(kFullMask, r, 0);
         r1 = __shfl_sync(kFullMask, r, 1);
         gb = cta_share_start(c_lo, c_len, NW, warp, r0, r1);
@@ -762,21 +763,33 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     }
     const int n = gb < ge ? (int)(ge - gb) : 0;
 
-    // the walk: cut pieces first (see share_order)
-    const ShareOrder order = share_order(cum, N, Hkv, gb, ge);
+    // the walk: cut pieces first (see share_order); lane 0 locates the
+    // share's first chunk, lane 1 its last
+    ShareOrder order = share_order(cum, N, Hkv, gb, gb);  // empty
+    if (n > 0) {
+        const ChunkPos e = locate_chunk(cum, N, Hkv, (lane & 1) ? ge - 1 : gb);
+        ChunkPos first, last;
+        first.c = __shfl_sync(kFullMask, e.c, 0);
+        first.nch = __shfl_sync(kFullMask, e.nch, 0);
+        last.c = __shfl_sync(kFullMask, e.c, 1);
+        last.nch = __shfl_sync(kFullMask, e.nch, 1);
+        order = share_order_at(first, last, gb, ge);
+    }
 
     // block-table entry of the chunk at walk position i (raw; validated when
     // its descriptor is built), 0 past the share
     // (at block size 8 a chunk spans two blocks: the second entry comes in the
     // high half, 0 when the chunk does not reach it)
-    auto table_entry = [&](int i) -> int2 {
-        if (i >= n) return make_int2(0, 0);
-        const ChunkPos q = locate_chunk(cum, N, Hkv, order.at(i));
+    auto table_entry_at = [&](const ChunkPos &q) -> int2 {
         const int lb = chunk_block(q.c, BS, Geo::kRows);
         const int32_t *row = p.block_tables + (int64_t)q.s * p.max_blocks_per_seq;
         int second = 0;
         if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[q.s]) second = __ldg(row + lb + 1);
         return make_int2(__ldg(row + lb), second);
+    };
+    auto table_entry = [&](int i) -> int2 {
+        if (i >= n) return make_int2(0, 0);
+        return table_entry_at(locate_chunk(cum, N, Hkv, order.at(i)));
     };
     const bool append = p.new_key != nullptr;
     // Descriptor of the chunk at walk position i, built by one lane for a
@@ -784,10 +797,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     // table entry `tab`: x = sequence | KV head << 16, y = rows | flags << 8,
     // z / w = the cache row of its box (of each block's box at block size 8).
     // Issuing a chunk is then a few shuffles and the copies.
-    auto chunk_desc = [&](int i, int2 tab) -> int4 {
-        if (i >= n) return make_int4(0, 0, 0, 0);
-        const int64_t g = order.at(i);
-        const ChunkPos q = locate_chunk(cum, N, Hkv, g);
+    auto chunk_desc_at = [&](int64_t g, const ChunkPos &q, int2 tab) -> int4 {
         int phys = tab.x, phys2 = tab.y;
         if (phys < 0 || phys >= p.num_blocks) {
             report(p.status, PKV_ERR_OUT_OF_RANGE);
@@ -806,9 +816,22 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
         const int y2 = (int)(((int64_t)phys2 * Hkv + q.kvh) * BS);
         return make_int4(q.s | (q.kvh << 16), rows | (flags << 8), y, y2);
     };
+    auto chunk_desc = [&](int i, int2 tab) -> int4 {
+        if (i >= n) return make_int4(0, 0, 0, 0);
+        const int64_t g = order.at(i);
+        return chunk_desc_at(g, locate_chunk(cum, N, Hkv, g), tab);
+    };
+    // windows 0 and 1: each lane locates its two positions in one search and
+    // starts their table loads (window 0's position is kept for its descriptor)
     int win = 0;
-    const int2 tab0 = table_entry(lane);  // window 0's entries, loading
-    int2 tab_nxt = table_entry(32 + lane);  // window 1's
+    ChunkPos q0, q1;
+    int2 tab0 = make_int2(0, 0), tab_nxt = make_int2(0, 0);
+    if (n > 0) {
+        locate_chunk2(cum, N, Hkv, lane < n ? order.at(lane) : gb, 32 + lane < n ? order.at(32 + lane) : gb, q0,
+                      q1);
+        if (lane < n) tab0 = table_entry_at(q0);
+        if (32 + lane < n) tab_nxt = table_entry_at(q1);
+    }
     int4 desc;  // descriptors of window win (window 0's are built below)
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
@@ -882,7 +905,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     for (int c = tid; c <= C; c += NW * 32)
         bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
     // window 0's descriptors (the table entries have arrived meanwhile)
-    desc = chunk_desc(lane, tab0);
+    desc = lane < n ? chunk_desc_at(order.at(lane), q0, tab0) : make_int4(0, 0, 0, 0);
     __syncthreads();
 
     // ---- from here on the kernel reads and writes what the preceding kernel

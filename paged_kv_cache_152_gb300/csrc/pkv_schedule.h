@@ -83,6 +83,29 @@ PKV_HD ChunkPos locate_chunk(const int *cum, int n, int num_kv_heads, int64_t g)
     return p;
 }
 
+// locate_chunk for two chunks at once: the two binary searches run in one
+// loop, so their dependent loads overlap.
+PKV_HD void locate_chunk2(const int *cum, int n, int num_kv_heads, int64_t g0, int64_t g1, ChunkPos &p0,
+                          ChunkPos &p1) {
+    int lo0 = 0, hi0 = n, lo1 = 0, hi1 = n;
+    while (hi0 - lo0 > 1 || hi1 - lo1 > 1) {
+        const int m0 = (lo0 + hi0) >> 1, m1 = (lo1 + hi1) >> 1;
+        const bool d0 = hi0 - lo0 > 1, d1 = hi1 - lo1 > 1;
+        const int c0 = cum[m0], c1 = cum[m1];
+        if (d0) { if (c0 <= g0) lo0 = m0; else hi0 = m0; }
+        if (d1) { if (c1 <= g1) lo1 = m1; else hi1 = m1; }
+    }
+    p0.s = lo0;
+    p1.s = lo1;
+    p0.nch = (cum[lo0 + 1] - cum[lo0]) / num_kv_heads;
+    p1.nch = (cum[lo1 + 1] - cum[lo1]) / num_kv_heads;
+    const int off0 = (int)(g0 - cum[lo0]), off1 = (int)(g1 - cum[lo1]);
+    p0.kvh = off0 / p0.nch;
+    p1.kvh = off1 / p1.nch;
+    p0.c = off0 - p0.kvh * p0.nch;
+    p1.c = off1 - p1.kvh * p1.nch;
+}
+
 // Step to chunk g+1 (which must exist).
 PKV_HD void next_chunk(ChunkPos &p, const int *cum, int n, int num_kv_heads) {
     if (++p.c < p.nch) return;
@@ -119,8 +142,10 @@ PKV_HD int partial_slot(int64_t st, int64_t g0) {
 // merge of the CTAs' parts, worth about a chunk per warp -- hence a small
 // absolute cap, one chunk per warp in the decode kernel).  Each
 // CTA's range is then divided equally among its NW warps: worker w = c*NW + k.
+// *cuts (if given) tells whether the start lies inside a segment.
 PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_t c, int64_t C, int64_t T,
-                                 int64_t snap_cap) {
+                                 int64_t snap_cap, bool *cuts = nullptr) {
+    if (cuts) *cuts = false;
     const int64_t nominal = (c * T) / C;
     if (c == 0 || nominal >= T) return nominal >= T ? T : 0;
     const ChunkPos p = locate_chunk(cum, n, num_kv_heads, nominal);
@@ -131,6 +156,7 @@ PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_
     if (left == 0) return nominal;
     if (left <= right && left <= snap) return g0;
     if (right < left && right <= snap) return g1;
+    if (cuts) *cuts = true;
     return nominal;
 }
 
@@ -158,13 +184,18 @@ PKV_HD int64_t cta_share_start(int64_t a, int64_t len, int nw, int k, int r0, in
 // chunk b (0 < b < T) lies inside a segment: `relief` chunks, but at most
 // 1/div of a nominal share (the cut costs a fixed time, so short shares give
 // up less); else 0.  div >= 2.
+// The same, given whether the boundary cuts a segment (snapped_cta_start
+// tells).
+PKV_HD int cut_relief_for(bool cuts, int64_t len, int nw, int relief, int div) {
+    if (!cuts || relief <= 0 || nw < 3) return 0;
+    const int64_t cap = len / ((int64_t)div * nw);
+    return cap < relief ? (int)cap : relief;
+}
+
 PKV_HD int cut_relief(const int *cum, int n, int num_kv_heads, int64_t b, int64_t T, int64_t len, int nw,
                       int relief, int div) {
     if (relief <= 0 || nw < 3 || b <= 0 || b >= T) return 0;
-    const int64_t cap = len / ((int64_t)div * nw);
-    const int r = cap < relief ? (int)cap : relief;
-    if (r <= 0) return 0;
-    return locate_chunk(cum, n, num_kv_heads, b).c != 0 ? r : 0;
+    return cut_relief_for(locate_chunk(cum, n, num_kv_heads, b).c != 0, len, nw, relief, div);
 }
 
 // The worker k of that CTA (0 <= k < NW) whose share holds chunk g,
@@ -243,14 +274,13 @@ struct ShareOrder {
     }
 };
 
-PKV_HD ShareOrder share_order(const int *cum, int n, int num_kv_heads, int64_t gb, int64_t ge) {
+// The walk of a non-empty share [gb, ge) given where its first chunk (gb)
+// and its last (ge - 1) lie (only c and nch of each are used).
+PKV_HD ShareOrder share_order_at(const ChunkPos &first, const ChunkPos &last, int64_t gb, int64_t ge) {
     ShareOrder o;
     o.a0 = o.a1 = o.b0 = o.b1 = gb;
     o.c0 = gb;
     o.c1 = ge;
-    if (gb >= ge) return o;
-    const ChunkPos first = locate_chunk(cum, n, num_kv_heads, gb);
-    const ChunkPos last = locate_chunk(cum, n, num_kv_heads, ge - 1);
     const int64_t first_seg_end = gb + (first.nch - first.c);   // one past the first segment
     const int64_t last_seg_start = (ge - 1) - last.c;           // the last segment's first chunk
     if (first_seg_end >= ge) return o;  // the share lies inside one segment: one piece
@@ -268,6 +298,18 @@ PKV_HD ShareOrder share_order(const int *cum, int n, int num_kv_heads, int64_t g
     }
     if (o.c0 > o.c1) o.c0 = o.c1;
     return o;
+}
+
+PKV_HD ShareOrder share_order(const int *cum, int n, int num_kv_heads, int64_t gb, int64_t ge) {
+    if (gb >= ge) {
+        ShareOrder o;
+        o.a0 = o.a1 = o.b0 = o.b1 = gb;
+        o.c0 = gb;
+        o.c1 = ge;
+        return o;
+    }
+    return share_order_at(locate_chunk(cum, n, num_kv_heads, gb), locate_chunk(cum, n, num_kv_heads, ge - 1), gb,
+                          ge);
 }
 
 // Element offset, in either cache, of the first row of chunk c of KV head kvh

@@ -59,6 +59,17 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         for (int c = 0; c <= C; ++c)
             bounds[c] = c == C ? T : snapped_cta_start(cum.data(), n, hkv, c, C, T, snap_cap);
         for (int c = 0; c < C; ++c) CHECK(bounds[c] <= bounds[c + 1], "cta bounds not monotonic");
+        // the reported cut, and the relief derived from it, match a fresh look-up
+        for (int c = 0; c <= C; ++c) {
+            bool cuts = true;
+            const int64_t b = c == C ? T : snapped_cta_start(cum.data(), n, hkv, c, C, T, snap_cap, &cuts);
+            if (c == C) cuts = false;
+            const bool want = b > 0 && b < T && locate_chunk(cum.data(), n, hkv, b).c != 0;
+            CHECK(cuts == want, "cut flag of cta %d start %lld", c, (long long)b);
+            for (int64_t len : {(int64_t)0, (int64_t)17, (int64_t)1000})
+                CHECK(cut_relief_for(cuts, len, nw, 3, 4) == cut_relief(cum.data(), n, hkv, b, T, len, nw, 3, 4),
+                      "cut_relief_for");
+        }
         // a CTA boundary inside a segment could not snap: both ends are far
         for (int c = 1; c < C; ++c) {
             const int64_t b = bounds[c];
@@ -136,6 +147,16 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
                 CHECK(w2 == owner[g], "worker_of_cta(%lld, hint %d)=%lld want %d", (long long)g, hint,
                       (long long)w2, owner[g]);
             }
+        }
+        {
+            // the two-key search agrees with two single ones
+            const int64_t g2 = (g * 7919) % T;
+            ChunkPos a2, b2;
+            locate_chunk2(cum.data(), n, hkv, g, g2, a2, b2);
+            const ChunkPos t2 = truth[g2];
+            CHECK(a2.s == truth[g].s && a2.kvh == truth[g].kvh && a2.c == truth[g].c && a2.nch == truth[g].nch &&
+                      b2.s == t2.s && b2.kvh == t2.kvh && b2.c == t2.c && b2.nch == t2.nch,
+                  "locate_chunk2(%lld, %lld)", (long long)g, (long long)g2);
         }
         const ChunkPos p = locate_chunk(cum.data(), n, hkv, g);
         CHECK(p.s == truth[g].s && p.kvh == truth[g].kvh && p.c == truth[g].c && p.nch == truth[g].nch,
