@@ -327,11 +327,11 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
 
     Every step: the C++ block manager appends one token per sequence and
     exports the tables and lengths straight into the step's page-locked
-    staging region, which also holds the step's queries and new K/V rows; ONE
-    host->device copy moves the region; copy-on-write pairs (if any) go
-    through copy_blocks; one launch of a DecodePlan (built once: append the
-    new tokens + attend, paged_attention_decode_append) runs the step; the
-    output comes back device->host and the stream is synchronised.  The
+    staging region, which also holds the step's queries and new K/V rows;
+    copy-on-write pairs (if any) go through copy_blocks; then ONE library call
+    (pkv_decode_plan_step of a DecodePlan built once: append the new tokens +
+    attend) copies the region host->device, launches the step and copies the
+    output device->host; the stream is synchronised.  The
     block-manager work of step i+1 runs on the host while the GPU runs step
     i (as a serving loop schedules ahead)."""
     import numpy as np
@@ -376,6 +376,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     h_out = torch.empty((n, h, d), dtype=torch.float16).pin_memory()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
+    d_stage_ptr, h_out_ptr = d_stage.data_ptr(), h_out.data_ptr()
+    h_row_ptrs = [r.data_ptr() for r in h_rows]
     batch = np.asarray(wl.batch, dtype=np.int32)
     kv_per_token = 2 * hkv * d * 2
     bytes_total = 0
@@ -392,16 +394,15 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     t0 = time.perf_counter()
     pairs = prepare(0)
     for i in range(steps):
-        bytes_total += int(lens_np[i].sum()) * kv_per_token
-        d_stage.copy_(h_rows[i], non_blocking=True)
-        h2d += step_bytes
         if pairs is not None:
             h_pairs_t.numpy()[:len(pairs)] = pairs
             d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
             h2d += len(pairs) * 16
             pkv.copy_blocks(t["key_cache"], t["value_cache"], d_pairs[:len(pairs)], status=st["status"])
-        plan.launch_raw(sh)
-        h_out.copy_(st["out"], non_blocking=True)
+        # one library call: the region host -> device, the launch, the output device -> host
+        plan.step_raw(d_stage_ptr, h_row_ptrs[i], step_bytes, h_out_ptr, sh)
+        bytes_total += int(lens_np[i].sum()) * kv_per_token
+        h2d += step_bytes
         d2h += h_out.numel() * 2
         # the next step's block-manager work runs on the host while the GPU
         # runs this step (it does not depend on this step's output values)
@@ -562,10 +563,10 @@ def run_pkv(args):
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "steps": e2e_steps,
                        "includes": "host block manager append + table export into the step's pinned staging "
-                                   "region (queries, new K/V, tables, lengths), one H2D copy of it, one "
-                                   "DecodePlan launch (append new tokens + attend), D2H of the output, stream "
-                                   "sync per step; the next step's block-manager work overlaps this step's GPU "
-                                   "work"}
+                                   "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
+                                   "per step: H2D copy of the region, the launch (append new tokens + attend), "
+                                   "D2H of the output; stream sync per step; the next step's block-manager work "
+                                   "overlaps this step's GPU work"}
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
     if dist is not None:

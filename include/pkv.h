@@ -204,6 +204,21 @@ int pkv_decode_plan_create(void *out, const void *query, const void *key, const 
                            void *workspace, size_t workspace_bytes,
                            int32_t *dev_status, pkv_decode_plan_t **plan);
 int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream);
+
+/*
+ * pkv_decode_plan_step: one serving step in one call, all on `stream`:
+ * in_bytes from host_in to dev_in (the step's inputs -- queries, new K/V,
+ * tables, lengths -- staged in one region that the plan's device pointers
+ * lie in), then the plan's launch, then the plan's output (fp16
+ * [num_seqs][num_heads][head_dim]) to host_out.  in_bytes == 0 skips the
+ * first copy and host_out == NULL the last.  host_in / host_out should be
+ * page-locked for the copies to be asynchronous.  The caller synchronises the
+ * stream before reading host_out or reusing host_in.  PKV_ERR_INVALID_ARG for
+ * a NULL plan or a missing pointer; PKV_ERR_CUDA when a copy or the launch
+ * fails to enqueue (nothing after it is enqueued).
+ */
+int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void *host_in, size_t in_bytes,
+                         void *host_out, pkv_stream_t stream);
 void pkv_decode_plan_destroy(pkv_decode_plan_t *plan);
 
 /* Bytes of workspace pkv_paged_attention_decode needs (host call; queries the

@@ -87,6 +87,7 @@ SIGNATURES = {
                                         _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size, _vp,
                                         ctypes.POINTER(_vp)]),
     "pkv_decode_plan_launch": (_c_int, [_vp, _vp]),
+    "pkv_decode_plan_step": (_c_int, [_vp, _vp, _vp, _c_size, _vp, _vp]),
     "pkv_decode_plan_destroy": (None, [_vp]),
     "pkv_alloc_host_pool": (_c_int, [_vp, _c_int, _i32p]),
     "pkv_swap_out": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
@@ -302,6 +303,33 @@ class DecodePlan:
         """launch() on a stream given as its raw handle (an int), for loops
         that look the stream up once."""
         _check(self._lib.pkv_decode_plan_launch(self._h, stream_handle), "pkv_decode_plan_launch")
+
+    def step(self, dev_in=None, host_in=None, host_out=None, stream=None):
+        """One serving step (pkv_decode_plan_step): host_in -> dev_in (same
+        byte size; the region the plan's inputs live in), the launch, then
+        out -> host_out.  Host tensors should be pinned; the caller
+        synchronises the stream before reading host_out."""
+        nbytes = 0
+        if host_in is not None:
+            if dev_in is None or host_in.numel() * host_in.element_size() != dev_in.numel() * dev_in.element_size():
+                raise ValueError("host_in and dev_in must have the same byte size")
+            if host_in.is_cuda or not dev_in.is_cuda or not host_in.is_contiguous() or not dev_in.is_contiguous():
+                raise ValueError("host_in must be a contiguous host tensor and dev_in a contiguous CUDA tensor")
+            nbytes = host_in.numel() * host_in.element_size()
+        if host_out is not None:
+            if host_out.is_cuda or not host_out.is_contiguous() or \
+                    host_out.numel() * host_out.element_size() != self.out.numel() * self.out.element_size():
+                raise ValueError("host_out must be a contiguous host tensor the size of out")
+        _check(self._lib.pkv_decode_plan_step(self._h, _ptr(dev_in) if nbytes else None,
+                                              _ptr(host_in) if nbytes else None, nbytes,
+                                              _ptr(host_out), _stream(stream)), "pkv_decode_plan_step")
+        return host_out
+
+    def step_raw(self, dev_in_ptr, host_in_ptr, nbytes, host_out_ptr, stream_handle):
+        """step() with raw pointers (ints) and a raw stream handle, unchecked
+        beyond what the library checks, for loops that resolve them once."""
+        _check(self._lib.pkv_decode_plan_step(self._h, dev_in_ptr, host_in_ptr, nbytes, host_out_ptr,
+                                              stream_handle), "pkv_decode_plan_step")
 
     def close(self):
         if getattr(self, "_h", None):

@@ -23,6 +23,7 @@ struct pkv_decode_plan {
     int ctas = 0;
     int threads = 0;
     size_t smem = 0;
+    size_t out_bytes = 0;  // fp16 [num_seqs][num_heads][head_dim]
     bool empty = true;
 };
 
@@ -277,6 +278,7 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.wait_limit_ns = kWaitLimitNs;
     p.smem_partials = r.smem_partials ? 1 : 0;
 
+    plan->out_bytes = (size_t)num_seqs * num_heads * head_dim * 2;
     plan->fn = r.info.fn;
     plan->ctas = r.ctas;
     plan->threads = r.info.threads;
@@ -359,6 +361,24 @@ extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *
 extern "C" int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream) {
     if (!plan) return PKV_ERR_INVALID_ARG;
     return launch_plan(*plan, stream);
+}
+
+extern "C" int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void *host_in,
+                                    size_t in_bytes, void *host_out, pkv_stream_t stream) {
+    if (!plan || (in_bytes && (!dev_in || !host_in))) return PKV_ERR_INVALID_ARG;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (in_bytes && cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    const int rc = launch_plan(*plan, stream);
+    if (rc != PKV_OK) return rc;
+    if (host_out && plan->out_bytes &&
+        cudaMemcpyAsync(host_out, plan->params.out, plan->out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
 }
 
 extern "C" void pkv_decode_plan_destroy(pkv_decode_plan_t *plan) { delete plan; }

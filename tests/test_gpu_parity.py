@@ -452,6 +452,65 @@ def test_decode_plan_equals_direct_calls(pkv, name, kw):
     read_only.close()
 
 
+@pytest.mark.gpu
+def test_decode_plan_step_stages_inputs_and_output(pkv):
+    """pkv_decode_plan_step: the step's inputs staged in one host region go in
+    with one copy, the plan runs, the output comes back to the host; the same
+    bits as the direct call on the same inputs, step after step."""
+    wl = W.make("tiny")
+    direct = Case(wl)
+    n, h, d = direct.t["query"].shape
+    hkv = direct.t["key"].shape[1]
+    mb = direct.tables.shape[1]
+    # staging layout: query | key | value | tables | lengths, each 256-byte aligned
+    parts = [("q", n * h * d * 2), ("k", n * hkv * d * 2), ("v", n * hkv * d * 2), ("tab", n * mb * 4), ("len", n * 4)]
+    offs, off = {}, 0
+    for nm, nb in parts:
+        offs[nm] = (off, nb)
+        off += -(-nb // 256) * 256
+    dev = torch.empty(off, dtype=torch.uint8, device="cuda")
+    host = torch.zeros(off, dtype=torch.uint8).pin_memory()
+
+    def view(buf, nm, dtype, shape):
+        o, nb = offs[nm]
+        return buf[o:o + nb].view(dtype).view(*shape)
+
+    staged = Case(wl)  # its caches; inputs come from the staging region
+    out = torch.empty_like(direct.out)
+    plan = pkv.DecodePlan(out, view(dev, "q", torch.float16, (n, h, d)), staged.t["key_cache"],
+                          staged.t["value_cache"], view(dev, "tab", torch.int32, (n, mb)),
+                          view(dev, "len", torch.int32, (n,)), wl.scale, key=view(dev, "k", torch.float16, (n, hkv, d)),
+                          value=view(dev, "v", torch.float16, (n, hkv, d)), status=staged.status)
+    host_out = torch.empty(out.shape, dtype=torch.float16).pin_memory()
+    view(host, "tab", torch.int32, (n, mb)).copy_(direct.tables.cpu())
+    view(host, "len", torch.int32, (n,)).copy_(direct.lens.cpu())
+    for step in range(3):
+        q = torch.randn_like(direct.t["query"].float()).half()
+        k = torch.randn_like(direct.t["key"].float()).half()
+        v = torch.randn_like(direct.t["value"].float()).half()
+        direct.t["query"].copy_(q)
+        direct.t["key"].copy_(k)
+        direct.t["value"].copy_(v)
+        view(host, "q", torch.float16, (n, h, d)).copy_(q.cpu())
+        view(host, "k", torch.float16, (n, hkv, d)).copy_(k.cpu())
+        view(host, "v", torch.float16, (n, hkv, d)).copy_(v.cpu())
+        pkv.paged_attention_decode_append(direct.out, direct.t["query"], direct.t["key"], direct.t["value"],
+                                          direct.t["key_cache"], direct.t["value_cache"], direct.tables,
+                                          direct.lens, wl.scale, status=direct.status)
+        plan.step(dev, host, host_out)
+        torch.cuda.synchronize()
+        assert int(direct.status.item()) == 0 and int(staged.status.item()) == 0
+        assert torch.equal(host_out.view(torch.int16), direct.out.cpu().view(torch.int16))
+        assert torch.equal(staged.t["key_cache"].view(torch.int16), direct.t["key_cache"].view(torch.int16))
+    # no input copy, no output copy: a plain launch
+    plan.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), direct.out.view(torch.int16))
+    with pytest.raises(ValueError):
+        plan.step(dev[:16], host)
+    plan.close()
+
+
 @pytest.mark.parametrize("d,h,hkv,bs,lens", [
     (128, 4, 4, 16, [16384]),           # group 1: 1,024-chunk segments over many CTAs, partials in shared memory
     (128, 16, 4, 32, [9000, 40, 5000]),  # group 4

@@ -172,5 +172,10 @@ def test_decode_plan_rejects_bad_arguments_on_host(lib, no_gpu):
     assert create(ws=None) == pkv.PKV_ERR_INVALID_ARG and h.value is None
     assert create(n=0) == pkv.PKV_OK and h.value is not None               # empty: launches nothing
     assert lib.pkv_decode_plan_launch(h, None) == pkv.PKV_OK
+    # a step of the empty plan without copies enqueues nothing; missing pointers are refused
+    assert lib.pkv_decode_plan_step(h, None, None, 0, None, None) == pkv.PKV_OK
+    assert lib.pkv_decode_plan_step(h, None, vp, 64, None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_plan_step(h, vp, None, 64, None, None) == pkv.PKV_ERR_INVALID_ARG
     lib.pkv_decode_plan_destroy(h)
     assert lib.pkv_decode_plan_launch(None, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.pkv_decode_plan_step(None, None, None, 0, None, None) == pkv.PKV_ERR_INVALID_ARG
