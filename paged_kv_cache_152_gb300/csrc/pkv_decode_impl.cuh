@@ -36,13 +36,17 @@
 //    ahead; when a window starts, each lane turns its entry into the chunk's
 //    copy descriptor (rows, flags, cache rows), so issuing a chunk is a few
 //    shuffles and the copies.
-//  * Math on the tensor cores, one warp per chunk: query heads on M (G of the
-//    16 rows used), rows of the chunk on N, head_dim on K:
-//        S^T[16 x rows] = Q[16 x D] . K^T       (mma.sync m16n8k16, fp32 acc)
-//        O[16 x D]     += P[16 x rows] . V       (P as fp16 hi + lo parts)
-//    K and V fragments come from the swizzled tiles through ldmatrix (.trans
-//    for V) without bank conflicts; the S accumulator layout is P's operand
-//    layout, so P never leaves registers.  Scores are in log2 units and the
+//  * Math on the tensor cores, one warp per chunk (mma.sync m16n8k16, fp32
+//    accumulate):
+//        S^T[16 x rows] = Q[16 x D] . K^T     query heads on M (G of 16 used),
+//                                               rows on N, head_dim on K
+//        O^T[D x 8]    += V^T[D x rows] . P^T  head_dim on M, heads on N (G of
+//                                               8 used), rows on K; P as fp16
+//                                               hi + lo parts
+//    K and V^T fragments come from the swizzled tiles through ldmatrix
+//    (.trans for V) without bank conflicts; the S accumulator layout is P^T's
+//    B-operand layout, so P never leaves registers, and the transposed P.V
+//    takes half the mma of P.V with heads on M.  Scores are in log2 units and the
 //    softmax is online, per warp, in fp32.  Products of fp16 inputs are exact
 //    in fp32, and splitting P into two fp16 terms keeps P.V at fp32 accuracy.
 //  * A piece that covers a whole segment is normalised and written as fp16
@@ -91,7 +95,7 @@ struct DecodeGeometry {
     static constexpr int kRowBytes = D * 2;           // one K (or V) row
     static constexpr int kSlotBytes = kQBytes + 2 * kRowBytes;  // + the new token's K and V rows
     static constexpr int kKSteps = D / 16;            // mma K steps of Q.K^T
-    static constexpr int kDTiles = D / 8;             // mma N tiles of P.V
+    static constexpr int kDTiles = D / 16;            // mma M tiles of O^T = V^T . P^T
     static constexpr int kBoxBytes = 8 * 128;         // one TMA box: 8 rows x 64 fp16
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert((BS % kRows == 0 || BS == 8) && kRows % 8 == 0,
@@ -134,11 +138,13 @@ __device__ __forceinline__ void zero_tail_rows(unsigned char *vt, int R, int lan
 }
 
 // One chunk of R valid rows: tiles at kt / vt (shared-memory addresses).
-// Lane (g, t) = (lane / 4, lane % 4) owns query head g (valid if g < G), rows
-// 2t, 2t+1 (+8) of the scores and output dims 8j + 2t, 8j + 2t + 1.
+// Lane (g, t) = (lane / 4, lane % 4) owns query head g (valid if g < G) and
+// rows 2t, 2t+1 (+8) of the scores; the output is kept transposed, O^T
+// [dims x heads]: o[i] holds dims 16i + g and 16i + g + 8 of heads 2t and
+// 2t + 1 (o[i][0] / o[i][2] head 2t, o[i][1] / o[i][3] head 2t + 1).
 template <int D, int BS, int G>
 __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, const uint32_t (&qa)[D / 16][2],
-                                              float scale_log2, float &m, float &l, float (&o)[D / 8][4],
+                                              float scale_log2, float &m, float &l, float (&o)[D / 16][4],
                                               int lane) {
     using Geo = DecodeGeometry<D, BS, G>;
     const int t = lane & 3;
@@ -197,10 +203,16 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     const float corr = exp2f(m - mn);       // m = -inf at a piece's start -> 0
     m = mn;
     l *= corr;
+    // the output columns are heads 2t and 2t + 1: their factors come from
+    // the lanes that own those heads' rows
+    const float corr_e = __shfl_sync(kFullMask, corr, 8 * t);
+    const float corr_o = __shfl_sync(kFullMask, corr, 8 * t + 4);
 #pragma unroll
-    for (int j = 0; j < Geo::kDTiles; ++j) {
-        o[j][0] *= corr;
-        o[j][1] *= corr;
+    for (int i = 0; i < D / 16; ++i) {
+        o[i][0] *= corr_e;
+        o[i][1] *= corr_o;
+        o[i][2] *= corr_e;
+        o[i][3] *= corr_o;
     }
     float pr[Geo::kNT][2];
 #pragma unroll
@@ -221,35 +233,21 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
         lo2 = pack_half2(pr[Geo::kNT - 1][0] - f2.x, pr[Geo::kNT - 1][1] - f2.y);
     }
 
-    // ---- O += P . V ----------------------------------------------------------
-    if (Geo::kNT == 2) {
+    // ---- O^T += V^T . P^T -----------------------------------------------------
+    // M = 16 dims per tile, N = 8 heads, K = the chunk's 16 rows.  P's score
+    // layout (head g, rows 2t, 2t+1 and 2t+8, 2t+9) is exactly the B operand
+    // of P^T, and V^T comes from the V tile through ldmatrix.trans: matrices
+    // (rows 8(mi>>1).., dims 16i + 8(mi&1)).
+    static_assert(Geo::kNT == 2, "16-row chunks");
 #pragma unroll
-        for (int dp = 0; dp < Geo::kDTiles / 2; ++dp) {
-            // matrices: (rows 8(mi&1).., dims 16dp + 8(mi>>1))
-            const int row = rr + 8 * (mi & 1);
-            const int c = (2 * dp + (mi >> 1)) & 7;
-            const uint32_t addr = vt + (dp >> 2) * Geo::kHalfBytes + row * 128 + ((c ^ rr) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_trans(addr, b0, b1, b2, b3);
-            mma_16816(o[2 * dp], h0, 0u, h2, 0u, b0, b1);
-            mma_16816(o[2 * dp], lo0, 0u, lo2, 0u, b0, b1);
-            mma_16816(o[2 * dp + 1], h0, 0u, h2, 0u, b2, b3);
-            mma_16816(o[2 * dp + 1], lo0, 0u, lo2, 0u, b2, b3);
-        }
-    } else {
-#pragma unroll
-        for (int dq = 0; dq < Geo::kDTiles / 4; ++dq) {
-            // matrices: (rows 0-7, dims 32dq + 8mi); rows 8-15 of P are zero
-            const int c = (4 * dq + mi) & 7;
-            const uint32_t addr = vt + (dq >> 1) * Geo::kHalfBytes + rr * 128 + ((c ^ rr) << 4);
-            uint32_t b[4];
-            ldsm_x4_trans(addr, b[0], b[1], b[2], b[3]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                mma_16816(o[4 * dq + j], h0, 0u, 0u, 0u, b[j], 0u);
-                mma_16816(o[4 * dq + j], lo0, 0u, 0u, 0u, b[j], 0u);
-            }
-        }
+    for (int i = 0; i < D / 16; ++i) {
+        const int row = rr + 8 * (mi >> 1);
+        const int c = (2 * i + (mi & 1)) & 7;
+        const uint32_t addr = vt + (i >> 2) * Geo::kHalfBytes + row * 128 + ((c ^ rr) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(addr, a0, a1, a2, a3);
+        mma_16816(o[i], a0, a1, a2, a3, h0, h2);
+        mma_16816(o[i], a0, a1, a2, a3, lo0, lo2);
     }
 }
 
@@ -511,33 +509,52 @@ __device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref re
 
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
-// stored partial; the caller counts it in (count_in).
+// stored partial; the caller counts it in (count_in).  The output is held
+// transposed (see consume_chunk): each lane pairs its values with lane ^ 4's
+// so that it stores two neighbouring dims of one head, hh = 2t + (g & 1).
 template <int D, int G, int NW>
 __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx<NW> &wc, const int4 md, float m,
-                                             float l, const float (&o)[D / 8][4], SegInfo &si, int lane) {
+                                             float l, const float (&o)[D / 16][4], SegInfo &si, int lane) {
     const int g = lane >> 2;
     const int t = lane & 3;
     l += __shfl_xor_sync(kFullMask, l, 1);
     l += __shfl_xor_sync(kFullMask, l, 2);
     const int s = md.x, kvh = md.y, flags = md.w;
+    const int hh = 2 * t + (g & 1);  // the head this lane stores
+    const int d0 = g & ~1;           // its first dim in each 8-dim group
+    // (even g: its own head-2t value and lane ^ 4's; odd g: lane ^ 4's
+    // head-(2t+1) value and its own)
+    auto pair = [&](float own_e, float own_o) -> float2 {
+        const float y = __shfl_xor_sync(kFullMask, (g & 1) ? own_e : own_o, 4);
+        return (g & 1) ? make_float2(y, own_o) : make_float2(own_e, y);
+    };
     if (flags & kWhole) {
-        if (g < G) {
-            __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + g) * D + 2 * t;
-            const float inv = 1.f / l;
+        const float inv = 1.f / __shfl_sync(kFullMask, l, 4 * hh);  // l of head hh
+        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + hh) * D + d0;
 #pragma unroll
-            for (int j = 0; j < D / 8; ++j)
-                *reinterpret_cast<uint32_t *>(dst + 8 * j) = pack_half2(o[j][0] * inv, o[j][1] * inv);
+        for (int i = 0; i < D / 16; ++i) {
+            const float2 a = pair(o[i][0], o[i][1]);
+            const float2 b = pair(o[i][2], o[i][3]);
+            if (hh < G) {
+                *reinterpret_cast<uint32_t *>(dst + 16 * i) = pack_half2(a.x * inv, a.y * inv);
+                *reinterpret_cast<uint32_t *>(dst + 16 * i + 8) = pack_half2(b.x * inv, b.y * inv);
+            }
         }
         return false;
     }
     si = segment_info(p, wc, s, kvh);
-    if (g < G) {
-        const PieceRef at = worker_piece<D, G, NW>(p, wc, wc.wid, (flags & kSlot1) ? 1 : 0);
-        float *dst = at.acc + g * D + 2 * t;
+    const PieceRef at = worker_piece<D, G, NW>(p, wc, wc.wid, (flags & kSlot1) ? 1 : 0);
+    float *dst = at.acc + hh * D + d0;
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) *reinterpret_cast<float2 *>(dst + 8 * j) = make_float2(o[j][0], o[j][1]);
-        if (t == 0) reinterpret_cast<float2 *>(at.ml)[g] = make_float2(m, l);
+    for (int i = 0; i < D / 16; ++i) {
+        const float2 a = pair(o[i][0], o[i][1]);
+        const float2 b = pair(o[i][2], o[i][3]);
+        if (hh < G) {
+            *reinterpret_cast<float2 *>(dst + 16 * i) = a;
+            *reinterpret_cast<float2 *>(dst + 16 * i + 8) = b;
+        }
     }
+    if (t == 0 && g < G) reinterpret_cast<float2 *>(at.ml)[g] = make_float2(m, l);
     return true;
 }
 
@@ -618,7 +635,7 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
 }
 
 template <int D, int BS, int G, int NW, int ST>
-__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #ifdef PKV_DECODE_SNAP_CAP
     constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
 #else
@@ -957,11 +974,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
     const int tq = lane & 3;
     uint32_t qa[D / 16][2];
     float m = -CUDART_INF_F, l = 0.f;
-    float o[D / 8][4];
+    float o[D / 16][4];  // O^T: dims 16i + g (+8) of heads 2t, 2t + 1
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) qa[kk][0] = qa[kk][1] = 0u;
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
     for (int i = 0; i < n; ++i) {
         const int stage = i % ST;
@@ -989,7 +1006,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const __grid_cons
             m = -CUDART_INF_F;
             l = 0.f;
 #pragma unroll
-            for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+            for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         }
         if (md.z < Geo::kRows) zero_tail_rows<D, BS, G>(wst + stage * Geo::kStageBytes + Geo::kTileBytes, md.z, lane);
         if (md.w & kAppendRow) {
