@@ -51,11 +51,13 @@
 //    in fp32, and splitting P into two fp16 terms keeps P.V at fp32 accuracy.
 //  * A piece that covers a whole segment is normalised and written as fp16
 //    by the warp.  A cut piece stores (max, sum, unnormalised output) and adds
-//    its chunk count to a counter; merges go in two levels (see count_in):
-//    the pieces in one CTA's range meet in shared memory and the one that
-//    completes the CTA's part merges it; a segment that spans CTAs then
-//    counts the CTAs' parts in device-wide, and the CTA completing it merges
-//    the parts.  Fixed order throughout (deterministic, no float atomics, no
+//    its chunk count to a counter; merges go in two levels (count_piece,
+//    merge_part): the pieces in one CTA's range meet in shared memory, and
+//    the CTA's part, once complete, is merged -- right away by the completing
+//    warp when shares are short, else through a per-CTA queue by a warp that
+//    has finished its own share (so no warp ends late for having merged); a
+//    segment that spans CTAs then counts the CTAs' parts in device-wide, and
+//    the CTA completing it merges the parts.  Fixed order throughout (deterministic, no float atomics, no
 //    second kernel).  The device-wide counters are tagged with an epoch kept
 //    in the workspace (see count_in_tagged): each call prepares the next
 //    call's counters and the last CTA out advances the epoch, so counting in
@@ -560,21 +562,22 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
 
 // Counts a stored partial of segment (s, kvh) in, in two levels.
 //  1. The pieces in this CTA's range (the whole segment, if it stays in the
-//     CTA) count their chunks in on a shared-memory counter; the piece that
-//     completes the CTA's part merges that part -- from shared memory.
-//  2. A segment that spans CTAs: the part goes to the CTA's slot in the
-//     workspace and its chunks count in on the segment's device-wide counter;
-//     the CTA completing the segment merges the parts, in CTA order.
+//     CTA) count their chunks in on a shared-memory counter (count_piece);
+//     the piece that completes the CTA's part queues the segment for merging
+//     in the CTA's merge queue (it does not merge: see merge_part).
+//  2. merge_part, run by a warp of the CTA that has finished its own share,
+//     merges the CTA's part from shared memory.  A segment that spans CTAs:
+//     the part goes to the CTA's slot in the workspace and its chunks count
+//     in on the segment's device-wide counter; the CTA completing the segment
+//     merges the parts, in CTA order.
 // A segment cut into many pieces thus merges at most a CTA's pieces from
-// shared memory plus one part per CTA from L2.
+// shared memory plus one part per CTA from L2, and the merges fall to warps
+// with nothing else to do instead of delaying a warp's own chunks.
+// Returns true when this warp completed the CTA's part of the segment.
 template <int D, int G, int NW>
-__device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
-                                         const SegInfo &si, int lane) {
-    const int64_t g1 = si.g0 + si.nch;
-    const int64_t p_lo = si.p_lo, p_hi = si.p_hi;
-    const int part = (int)(p_hi - p_lo);
+__device__ __forceinline__ bool count_piece(const WorkerCtx<NW> &wc, const SegInfo &si, int lane) {
+    const int part = (int)(si.p_hi - si.p_lo);
     const int mine = si.mine;
-    const int xw = si.xw;  // this CTA's cross slot for the segment (if it spans CTAs)
     if (part != mine) {
         fence_acq_rel_cta();  // the partial is visible to this CTA before it is counted
         __syncwarp();
@@ -582,15 +585,25 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
         if (lane == 0) {
             // a worker starts at most one cut segment inside its CTA, and a CTA
             // meets at most one segment from before its range
-            int *ctr = xw ? wc.cta_cross : wc.cta_count + (wc.worker_of(p_lo) % NW);
+            int *ctr = si.xw ? wc.cta_cross : wc.cta_count + (wc.worker_of(si.p_lo) % NW);
             done = atomicAdd(ctr, mine) + mine;
         }
         done = __shfl_sync(kFullMask, done, 0);
-        if (done != part) return;
+        if (done != part) return false;
         fence_acq_rel_cta();
     }
-    const int64_t wa = wc.worker_of(p_lo);
-    const int64_t wb = wc.worker_of(p_hi - 1);
+    return true;
+}
+
+// Merges this CTA's part of cut segment (s, kvh) (see count_piece); si is
+// its segment_info (only the CTA-level fields are used).
+template <int D, int G, int NW>
+__device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
+                                           const SegInfo &si, int lane) {
+    const int64_t g1 = si.g0 + si.nch;
+    const int part = (int)(si.p_hi - si.p_lo);
+    const int64_t wa = wc.worker_of(si.p_lo);
+    const int64_t wb = wc.worker_of(si.p_hi - 1);
     auto wref = [&](int i) -> PieceRef {
         const int64_t w = wa + i;
         const int64_t st = wc.start(w);
@@ -609,7 +622,7 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
         ms.write_out(p, s, kvh, lane);
         return;
     }
-    ms.store(cta_piece<D, G>(p, blockIdx.x, xw), lane);
+    ms.store(cta_piece<D, G>(p, blockIdx.x, si.xw), lane);
     fence_acq_rel_gpu();  // the part is visible device-wide before it is counted
     __syncwarp();
     int done = 0;
@@ -634,6 +647,17 @@ __device__ __forceinline__ void count_in(const DecodeParams &p, const WorkerCtx<
     ms2.write_out(p, s, kvh, lane);
 }
 
+// The CTA's merge queue (shared memory): segments whose CTA part is complete
+// and waits for merge_part.  At most NW + 1 parts complete in a CTA (a cut
+// segment holds a warp or CTA boundary of the range), so kMergeQueue entries
+// never run out; a push that would still overflow merges at once.
+constexpr int kMergeQueue = 32;
+struct MergeQueue {
+    int entry[kMergeQueue];  // sequence | KV head << 16, -1 until written
+    int tail;                // entries claimed by producers
+    int head;                // entries taken by consumers
+};
+
 template <int D, int BS, int G, int NW, int ST>
 __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #ifdef PKV_DECODE_SNAP_CAP
@@ -650,6 +674,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     constexpr int kRelief = PKV_DECODE_RELIEF;
 #else
     constexpr int kRelief = 4;  // chunks a worker with a piece cut across CTAs gives up
+#endif
+#ifdef PKV_DECODE_DEFER_MIN
+    constexpr int kDeferMin = PKV_DECODE_DEFER_MIN;
+#else
+    constexpr int kDeferMin = 24;  // CTAs whose warps' shares are shorter merge at once
 #endif
 #ifdef PKV_DECODE_RELIEF_DIV
     constexpr int kReliefDiv = PKV_DECODE_RELIEF_DIV;
@@ -673,6 +702,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     __shared__ int cta_count[NW];
     __shared__ int exit_count;
     __shared__ int cta_cross;
+    __shared__ MergeQueue mq;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -718,9 +748,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         fence_barrier_init();
     }
     if (tid < NW) cta_count[tid] = 0;
+    if (tid < kMergeQueue) mq.entry[tid] = -1;
     if (tid == 0) {
         exit_count = 0;
         cta_cross = 0;
+        mq.tail = mq.head = 0;
     }
     __syncthreads();
     if (warp == 0) {
@@ -959,16 +991,68 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             count_in_tagged(p.ws_sync + 1 + parity, epoch, C, 1) == C)
             atomicExch(p.ws_sync, (unsigned long long)(epoch + 1));
     };
-    if (n == 0) {
-        exit_warp();
-        return;
-    }
     // shared partial slots: 16-byte aligned, after the bounds
     float *part = nullptr;
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
     const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
                            c_lo, c_len, r0, r1};
+
+    // the CTA's merge queue (count_piece / merge_part)
+    auto vload = [](const int *a) { return *reinterpret_cast<const volatile int *>(a); };
+    auto push = [&](int s, int kvh) {  // (an overflowing push merges at once: see MergeQueue)
+        int idx = 0;
+        if (lane == 0) {
+            idx = atomicAdd(&mq.tail, 1);
+            if (idx < kMergeQueue) *reinterpret_cast<volatile int *>(&mq.entry[idx]) = s | (kvh << 16);
+        }
+        idx = __shfl_sync(kFullMask, idx, 0);
+        if (idx >= kMergeQueue) merge_part<D, G, NW>(p, wc, s, kvh, segment_info(p, wc, s, kvh), lane);
+    };
+    // After its own share a warp merges queued parts until the queue is empty.
+    // No entry is left behind: a warp pushes only during its own share and
+    // drains after it, so whatever it pushed is either taken by another warp
+    // or by itself.  Warps that finish early thus take the parts queued early
+    // (the cut pieces come first in every share).
+    auto drain = [&]() {
+        const uint64_t t0 = global_ns();
+        while (true) {
+            int e = -1;
+            if (lane == 0) {
+                int h = vload(&mq.head);
+                while (h < vload(&mq.tail)) {
+                    const int prev = atomicCAS(&mq.head, h, h + 1);
+                    if (prev == h) {
+                        e = h;
+                        break;
+                    }
+                    h = prev;
+                }
+            }
+            e = __shfl_sync(kFullMask, e, 0);
+            if (e < 0) return;               // empty
+            if (e >= kMergeQueue) continue;  // merged by its producer
+            int v = -1;
+            if (lane == 0)  // written by its producer right after the claim
+                while ((v = vload(&mq.entry[e])) < 0 && global_ns() - t0 < p.wait_limit_ns) {
+                }
+            v = __shfl_sync(kFullMask, v, 0);
+            if (v < 0) {
+                if (lane == 0) report(p.status, PKV_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            fence_acq_rel_cta();
+            merge_part<D, G, NW>(p, wc, v & 0xffff, v >> 16, segment_info(p, wc, v & 0xffff, v >> 16), lane);
+        }
+    };
+    // whether this CTA queues its merges (the same for all its warps): when
+    // its warps' shares are long enough for the merging warp to end late
+    const bool defer = c_len >= (int64_t)kDeferMin * NW;
+    if (n == 0) {
+        if (defer) drain();
+        exit_warp();
+        return;
+    }
 
     const int gq = lane >> 2;
     const int tq = lane & 3;
@@ -1041,9 +1125,21 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         __syncwarp();
         if (issued < n) issue(issued++);
         SegInfo si;
-        if ((md.w & kLast) && finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane))
-            count_in<D, G, NW>(p, wc, md.x, md.y, si, lane);
+        if ((md.w & kLast) && finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane) &&
+            count_piece<D, G, NW>(wc, si, lane)) {
+            // with long shares the merge goes to a warp that is done with its
+            // own (the merging warp would otherwise end late); with short ones
+            // every warp ends at about the same time, and merging at once
+            // overlaps the copies still in flight
+            if (defer) {
+                fence_acq_rel_cta();  // the part's pieces are visible to whoever merges it
+                push(md.x, md.y);
+            } else {
+                merge_part<D, G, NW>(p, wc, md.x, md.y, si, lane);
+            }
+        }
     }
+    if (defer) drain();
     exit_warp();
 }
 
