@@ -322,7 +322,10 @@ def device_step(pkv, st, ws, num_ctas, ev=None):
     return st["launches_per_step"]
 
 
-def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
+E2E_WARMUP = 20  # untimed serving steps before the timed ones (first-use costs on the host)
+
+
+def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
     """Serving-loop steps through the public API with host buffers.
 
     Every step: the C++ block manager appends one token per sequence and
@@ -345,6 +348,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
         offs[name] = (off, nbytes)
         off += -(-nbytes // 256) * 256
     step_bytes = off
+    timed = steps
+    steps = warmup + timed  # every step has its own staging row
     h_stage = torch.empty((steps, step_bytes), dtype=torch.uint8).pin_memory()
     rng = np.random.default_rng(wl.seed + 77)
     stage_np = h_stage.numpy()
@@ -378,6 +383,7 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     sh = stream.cuda_stream
     d_stage_ptr, h_out_ptr = d_stage.data_ptr(), h_out.data_ptr()
     h_row_ptrs = [r.data_ptr() for r in h_rows]
+    done = torch.cuda.Event()
     batch = np.asarray(wl.batch, dtype=np.int32)
     kv_per_token = 2 * hkv * d * 2
     bytes_total = 0
@@ -394,26 +400,37 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist):
     t0 = time.perf_counter()
     pairs = prepare(0)
     for i in range(steps):
+        if i == warmup and warmup:
+            # the warm-up steps are done (each was waited for): time from here
+            barrier(dist, device)
+            t0 = time.perf_counter()
+        timed_step = i >= warmup
         if pairs is not None:
             h_pairs_t.numpy()[:len(pairs)] = pairs
             d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
-            h2d += len(pairs) * 16
+            h2d += len(pairs) * 16 if timed_step else 0
             pkv.copy_blocks(t["key_cache"], t["value_cache"], d_pairs[:len(pairs)], status=st["status"])
         # one library call: the region host -> device, the launch, the output device -> host
         plan.step_raw(d_stage_ptr, h_row_ptrs[i], step_bytes, h_out_ptr, sh)
-        bytes_total += int(lens_np[i].sum()) * kv_per_token
-        h2d += step_bytes
-        d2h += h_out.numel() * 2
+        if timed_step:
+            bytes_total += int(lens_np[i].sum()) * kv_per_token
+            h2d += step_bytes
+            d2h += h_out.numel() * 2
         # the next step's block-manager work runs on the host while the GPU
         # runs this step (it does not depend on this step's output values)
+        done.record(stream)
         if i + 1 < steps:
             pairs = prepare(i + 1)
-        stream.synchronize()
+        # wait for the step by polling (a blocking synchronize leaves the
+        # waking of this thread to the OS scheduler, which on a busy host adds
+        # tens of microseconds per step)
+        while not done.query():
+            pass
     elapsed = time.perf_counter() - t0
     elapsed = max_over_ranks(dist, elapsed, device)
     barrier(dist, device)
     plan.close()
-    return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // steps, "d2h": d2h // steps}
+    return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed}
 
 
 def run_pkv(args):
@@ -431,7 +448,8 @@ def run_pkv(args):
     pkv.load()
 
     e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
-    st = build_state(args.config, device, args.identity_tables, e2e_headroom_steps=e2e_steps,
+    st = build_state(args.config, device, args.identity_tables,
+                     e2e_headroom_steps=e2e_steps + E2E_WARMUP if e2e_steps else 0,
                      block_size=args.block_size)
     if not args.two_launch:
         st["fused"] = True
@@ -501,7 +519,7 @@ def run_pkv(args):
 
     e2e = None
     if e2e_steps:
-        e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist)
+        e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist, warmup=E2E_WARMUP)
     clock_info = clocks.finish()
 
     if rank != 0:
@@ -561,11 +579,12 @@ def run_pkv(args):
     if e2e is not None:
         line["e2e"] = {"value": round(world * e2e["bytes"] / e2e["elapsed"] / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                       "steps": e2e_steps,
+                       "steps": e2e_steps, "warmup_steps": E2E_WARMUP,
                        "includes": "host block manager append + table export into the step's pinned staging "
                                    "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
                                    "per step: H2D copy of the region, the launch (append new tokens + attend), "
-                                   "D2H of the output; stream sync per step; the next step's block-manager work "
+                                   "D2H of the output; the host waits for each step (polling an event); the next "
+                                   "step's block-manager work "
                                    "overlaps this step's GPU work"}
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
