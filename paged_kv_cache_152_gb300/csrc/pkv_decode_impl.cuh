@@ -22,7 +22,7 @@
 //    CTA per segment).  Every warp is an independent worker; there is no
 //    CTA-wide synchronisation after the prologue.  A worker walks the cut
 //    pieces at the two ends of its share first, so segments cut between
-//    workers are merged early, under the rest of the stream, not at the tail.
+//    workers complete early, under the rest of the stream, not at the tail.
 //  * Each warp owns a ring of ST stages in shared memory.  Lane 0 issues, ST
 //    chunks ahead, one TMA tensor copy (cp.async.bulk.tensor.3d, 128-byte
 //    swizzle) per cache of the chunk's K and V rows -- the cache is viewed as
@@ -511,7 +511,7 @@ __device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref re
 
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
-// stored partial; the caller counts it in (count_in).  The output is held
+// stored partial; the caller counts it in (count_piece).  The output is held
 // transposed (see consume_chunk): each lane pairs its values with lane ^ 4's
 // so that it stores two neighbouring dims of one head, hh = 2t + (g & 1).
 template <int D, int G, int NW>

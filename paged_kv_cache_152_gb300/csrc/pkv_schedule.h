@@ -250,7 +250,7 @@ PKV_HD int64_t worker_of_cta(const int64_t *bounds, int C, int64_t g, int hint) 
 // starts before gb) -- then everything between them in chunk order.  The
 // other pieces of a cut segment sit at the starts and ends of neighbouring
 // shares, so with every worker doing the same, cut segments complete early
-// and their merges overlap the rest of the work.  Pieces stay contiguous runs
+// and their merges are ready long before the tail.  Pieces stay contiguous runs
 // of the walk, so chunk_flags is unchanged.
 struct ShareOrder {
     int64_t a0, a1;   // range 1: the cut last piece (empty if none)
