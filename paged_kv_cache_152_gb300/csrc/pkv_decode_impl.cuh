@@ -97,7 +97,6 @@ struct DecodeGeometry {
     static constexpr int kRowBytes = D * 2;           // one K (or V) row
     static constexpr int kSlotBytes = kQBytes + 2 * kRowBytes;  // + the new token's K and V rows
     static constexpr int kKSteps = D / 16;            // mma K steps of Q.K^T
-    static constexpr int kDTiles = D / 16;            // mma M tiles of O^T = V^T . P^T
     static constexpr int kBoxBytes = 8 * 128;         // one TMA box: 8 rows x 64 fp16
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert((BS % kRows == 0 || BS == 8) && kRows % 8 == 0,
@@ -291,8 +290,6 @@ struct WorkerCtx {
     const int *cum;          // chunk prefix sums (shared memory)
     const int64_t *bounds;   // CTA ranges, [C + 1] (shared memory)
     int C;                   // CTAs in the grid
-    int64_t W;               // workers in the grid
-    int64_t T;               // chunks in the batch
     int64_t wid;             // this worker
     int64_t gb, ge;          // its share
     uint32_t epoch;          // this call's epoch
@@ -792,7 +789,6 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     const int C = (int)min(min((int64_t)gridDim.x, seg_cap),
                            max((int64_t)1, (T + NW * kMinShare - 1) / (NW * kMinShare)));
     if ((int)blockIdx.x >= C) return;
-    const int64_t W = (int64_t)C * NW;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
     int64_t gb, ge, c_lo, c_len;
     int r0, r1;
@@ -995,7 +991,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     float *part = nullptr;
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
-    const WorkerCtx<NW> wc{cum, bounds, C, W, T, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
+    const WorkerCtx<NW> wc{cum, bounds, C, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
                            c_lo, c_len, r0, r1};
 
     // the CTA's merge queue (count_piece / merge_part)
