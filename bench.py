@@ -397,6 +397,7 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
 
     barrier(dist, device)
     torch.cuda.synchronize()
+    marks = []  # wall clock at the start of each timed step
     t0 = time.perf_counter()
     pairs = prepare(0)
     for i in range(steps):
@@ -405,6 +406,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
             barrier(dist, device)
             t0 = time.perf_counter()
         timed_step = i >= warmup
+        if timed_step:
+            marks.append(time.perf_counter())
         if pairs is not None:
             h_pairs_t.numpy()[:len(pairs)] = pairs
             d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
@@ -426,11 +429,15 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
         # tens of microseconds per step)
         while not done.query():
             pass
-    elapsed = time.perf_counter() - t0
-    elapsed = max_over_ranks(dist, elapsed, device)
+    t_end = time.perf_counter()
+    elapsed = max_over_ranks(dist, t_end - t0, device)
     barrier(dist, device)
     plan.close()
-    return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed}
+    marks.append(t_end)
+    per = sorted(b - a for a, b in zip(marks, marks[1:]))
+    pct = lambda q: round(per[min(len(per) - 1, int(q * len(per)))] * 1e6, 1)
+    return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed,
+            "step_us": {"p50": pct(0.5), "p90": pct(0.9), "max": round(per[-1] * 1e6, 1)}}
 
 
 def run_pkv(args):
@@ -579,7 +586,7 @@ def run_pkv(args):
     if e2e is not None:
         line["e2e"] = {"value": round(world * e2e["bytes"] / e2e["elapsed"] / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                       "steps": e2e_steps, "warmup_steps": E2E_WARMUP,
+                       "steps": e2e_steps, "warmup_steps": E2E_WARMUP, "step_us": e2e["step_us"],
                        "includes": "host block manager append + table export into the step's pinned staging "
                                    "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
                                    "per step: H2D copy of the region, the launch (append new tokens + attend), "
