@@ -261,6 +261,23 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         }
         CHECK(!in_piece, "order ends inside a piece");
     }
+    // the merge queue of a CTA (32 entries in the decode kernel) receives one
+    // entry per cut segment whose part lies in the CTA's range: at most nw + 1
+    // (a cut segment holds a worker or CTA boundary of the range)
+    if (split == 1) {
+        std::vector<int> queued(C, 0);
+        for (int s = 0; s < n; ++s) {
+            const int nch = chunks_for(ctx[s], sr);
+            for (int h = 0; h < hkv && nch > 0; ++h) {
+                const int64_t g0 = cum[s] + (int64_t)h * nch, g1 = g0 + nch;
+                if (wof(g0) == wof(g1 - 1)) continue;  // one piece: not cut
+                for (int c = 0; c < C; ++c)
+                    if (g0 < bounds[c + 1] && g1 > bounds[c]) ++queued[c];
+            }
+        }
+        for (int c = 0; c < C; ++c)
+            CHECK(queued[c] <= nw + 1 && queued[c] <= 32, "cta %d queues %d merges (nw %d)", c, queued[c], nw);
+    }
     // the merge kernel finds exactly the stored partials of every cut segment
     for (int s = 0; s < n; ++s) {
         const int nch = chunks_for(ctx[s], sr);
