@@ -23,10 +23,12 @@ every step (--no-graph: direct binding calls).
   The KV read per step (0.57 GB) is larger than L2 (129 MB), so no L2 flush.
 * e2e: the same metric through the public API with host buffers: every step
   the C++ block manager appends one token per sequence and exports the tables
-  into the step's pinned staging region (with its queries and new K/V rows),
-  one host->device copy moves it, one DecodePlan launch appends the new
-  tokens and attends, the output comes back device->host, stream sync; the
-  next step's block-manager work overlaps the GPU's work on this step.
+  into the step's pinned staging region (with its queries and new K/V rows);
+  one pkv_decode_plan_step call copies the region host->device, appends the
+  new tokens and attends, and copies the output device->host; the host waits
+  for the step (polling an event); the next step's block-manager work
+  overlaps the GPU's work on this step.  20 untimed warm-up steps first; the
+  line also gives the per-step wall-time percentiles.
 * roofline: the decode launch timed alone with CUDA events on its stream
   over the timed region; algorithmic bytes / mean duration vs the
   measured HBM copy bandwidth.
