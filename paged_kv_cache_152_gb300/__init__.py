@@ -68,10 +68,10 @@ SIGNATURES = {
     "pkv_seq_new": (_c_int, [_vp, _intp]),
     "pkv_append_token": (_c_int, [_vp, _c_int, _i64p, _i32p]),
     "pkv_append_tokens": (_c_int, [_vp, _c_int, _c_int, _i64p, _i32p, _intp]),
-    "pkv_append_batch": (_c_int, [_vp, _i32p, _c_int, _i64p, _i32p, _intp]),
+    "pkv_append_batch": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _vp]),  # (void*: raw addresses are cheapest)
     "pkv_fork": (_c_int, [_vp, _c_int, _intp]),
     "pkv_release": (_c_int, [_vp, _c_int, _intp]),
-    "pkv_export_tables": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _i32p]),
+    "pkv_export_tables": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _vp]),
     "pkv_seq_length": (_c_int, [_vp, _c_int, _intp]),
     "pkv_seq_num_blocks": (_c_int, [_vp, _c_int, _intp]),
     "pkv_seq_table": (_c_int, [_vp, _c_int, _i32p, _c_int, _intp]),
@@ -153,6 +153,13 @@ def _check(status, what):
 
 # ---------------------------------------------------------------------------
 # device calls
+
+def _out_array(a, dtype, min_items, name):
+    """Output arrays handed to the library by address: C-contiguous, of the
+    element type the call writes, and large enough."""
+    if a.dtype != dtype or not a.flags["C_CONTIGUOUS"] or a.size < min_items:
+        raise ValueError(f"{name}: need a C-contiguous {np.dtype(dtype).name} array of >= {min_items} items")
+
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
@@ -544,10 +551,11 @@ class BlockAllocator:
         n = s.shape[0]
         slots = slots_out if slots_out is not None else np.empty(max(n, 1), dtype=np.int64)
         pairs = pairs_out if pairs_out is not None else np.empty((max(n, 1), 2), dtype=np.int32)
-        ncow = ctypes.c_int()
-        _check(self._lib.pkv_append_batch(self._h, s.ctypes.data_as(_i32p), n, slots.ctypes.data_as(_i64p),
-                                          pairs.ctypes.data_as(_i32p), ctypes.byref(ncow)), "pkv_append_batch")
-        return slots[:n], pairs[:ncow.value]
+        _out_array(slots, np.int64, n, "slots_out")
+        _out_array(pairs, np.int32, 2 * n, "pairs_out")
+        _check(self._lib.pkv_append_batch(self._h, s.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
+                                          ctypes.byref(self._i)), "pkv_append_batch")
+        return slots[:n], pairs[:self._i.value]
 
     def fork(self, parent):
         _check(self._lib.pkv_fork(self._h, parent, ctypes.byref(self._i)), "pkv_fork")
@@ -564,8 +572,10 @@ class BlockAllocator:
         n = s.shape[0]
         tables = tables_out if tables_out is not None else np.empty((n, max_blocks_per_seq), np.int32)
         lens = lens_out if lens_out is not None else np.empty(n, np.int32)
-        _check(self._lib.pkv_export_tables(self._h, s.ctypes.data_as(_i32p), n, tables.ctypes.data_as(_i32p),
-                                           max_blocks_per_seq, lens.ctypes.data_as(_i32p)), "pkv_export_tables")
+        _out_array(tables, np.int32, n * max_blocks_per_seq, "tables_out")
+        _out_array(lens, np.int32, n, "lens_out")
+        _check(self._lib.pkv_export_tables(self._h, s.ctypes.data, n, tables.ctypes.data, max_blocks_per_seq,
+                                           lens.ctypes.data), "pkv_export_tables")
         return tables, lens
 
     def seq_len(self, seq):
