@@ -62,6 +62,22 @@ def test_schedule_exhaustive(tmp_path):
     assert "schedule ok" in r.stdout
 
 
+def test_alloc_fuzz_sanitized(tmp_path):
+    """Random block-manager calls through the C ABI under ASan/UBSan:
+    conservation, reference counts, table lengths, and failed calls leave the
+    state untouched."""
+    exe = tmp_path / "test_alloc_fuzz"
+    subprocess.run(["g++", "-O1", "-g", "-std=c++17", "-Wall", "-Werror",
+                    "-fsanitize=address,undefined", "-fno-sanitize-recover=undefined",
+                    "-fno-omit-frame-pointer", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "cpp", "test_alloc_fuzz.cpp"),
+                    os.path.join(ROOT, "paged_kv_cache_152_gb300", "csrc", "pkv_alloc.cpp"),
+                    "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "alloc fuzz ok" in r.stdout
+
+
 @pytest.fixture
 def no_gpu():
     """Host-validation tests pass fake device pointers that must be rejected
