@@ -124,7 +124,10 @@ int pkv_version(void);
  *   stream       CUDA stream.
  *
  * Supported: head_dim in {64, 128}; block_size in {8, 16, 32, 64, 128};
- * num_heads / num_kv_heads in {1, 2, 4, 8}; 1 <= num_seqs <= 4096.
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; 1 <= num_seqs <= 4096;
+ * num_blocks * num_kv_heads * block_size < 2^31 (the cache rows the tensor
+ * copies address: up to 512 GB per cache at head_dim 128, 256 GB at 64) and
+ * max_blocks_per_seq * block_size <= 2^30, else PKV_ERR_INVALID_ARG.
  * A context longer than max_blocks_per_seq*block_size, or a table entry
  * outside [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in dev_status; such a
  * context is clamped to its table and such an entry reads block 0.

@@ -92,8 +92,8 @@ def test_decode_rejects_bad_arguments_on_host(lib, no_gpu):
     vp = ctypes.c_void_p(256)    # never dereferenced: validation fails first
     call = lambda **kw: lib.pkv_paged_attention_decode(  # noqa: E731
         kw.get("out", vp), vp, vp, vp, vp, kw.get("mb", 4), vp, kw.get("n", 2), kw.get("h", 8),
-        kw.get("hkv", 8), kw.get("d", 64), kw.get("bs", 16), 10, ctypes.c_float(kw.get("scale", 0.125)),
-        0, kw.get("ws", vp), 1 << 20, None, None)
+        kw.get("hkv", 8), kw.get("d", 64), kw.get("bs", 16), kw.get("nb", 10),
+        ctypes.c_float(kw.get("scale", 0.125)), 0, kw.get("ws", vp), 1 << 20, None, None)
     import paged_kv_cache_152_gb300 as pkv
     assert call(n=0) == pkv.PKV_OK                       # empty batch: nothing to do
     assert call(out=None) == pkv.PKV_ERR_INVALID_ARG
@@ -105,6 +105,9 @@ def test_decode_rejects_bad_arguments_on_host(lib, no_gpu):
     assert call(bs=24) == pkv.PKV_ERR_UNSUPPORTED
     assert call(h=48, hkv=3) == pkv.PKV_ERR_UNSUPPORTED  # group 16
     assert call(out=ctypes.c_void_p(258)) == pkv.PKV_ERR_INVALID_ARG  # misaligned
+    # cache rows (blocks x KV heads x block size) must stay below 2^31
+    assert call(nb=(1 << 31) // (8 * 16)) == pkv.PKV_ERR_INVALID_ARG
+    assert call(mb=(1 << 26) + 1) == pkv.PKV_ERR_INVALID_ARG    # 2^30 tokens per table row
 
 
 def test_cache_ops_reject_bad_arguments_on_host(lib, no_gpu):
