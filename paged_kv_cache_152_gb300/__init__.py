@@ -4,7 +4,9 @@ Argument marshalling only: every step of the hot path runs in the library's
 CUDA kernels or its C++ block manager.  Functions take torch tensors (device
 memory and streams are torch's) and pass raw pointers, sizes and the current
 CUDA stream to the C ABI declared in include/pkv.h.  If the shared library is
-missing or fails to load, every call raises -- there is no fallback.
+missing or fails to load, every call raises -- there is no fallback.  The
+library launches on the current CUDA device, so each call runs with the device
+its tensors live on made current (they must all share one).
 
 Names mirror the C ABI without its ``pkv_`` prefix:
 
@@ -19,6 +21,7 @@ Names mirror the C ABI without its ``pkv_`` prefix:
   pkv_release / pkv_export_tables / pkv_swap_out / pkv_swap_in.
 """
 
+import contextlib
 import ctypes
 import os
 
@@ -184,6 +187,52 @@ def _need(t, dtype, name, ndim=None, device=True):
     return torch
 
 
+def _need_all(*specs):
+    """_need over (tensor, dtype, name, ndim) specs: every element type,
+    layout and rank first, then that every tensor is on a CUDA device."""
+    for t, dtype, name, ndim in specs:
+        _need(t, dtype, name, ndim, device=False)
+    for t, _, name, _ in specs:
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _status_ptr(status):
+    """The caller's device status word: None, or an int32 CUDA tensor."""
+    if status is None:
+        return None
+    _need(status, __import__("torch").int32, "status")
+    if status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
+    return _ptr(status)
+
+
+def _workspace(ws):
+    """A caller-given decode workspace: contiguous device memory (its size
+    and alignment are checked by the library)."""
+    if ws.device.type != "cuda" or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def _device_guard(index):
+    """Make CUDA device `index` current for one library call."""
+    import torch
+    return contextlib.nullcontext() if torch.cuda.current_device() == index else torch.cuda.device(index)
+
+
+def _one_device(tensors, stream=None):
+    """The device guard for a call on `tensors` (host tensors and None are
+    skipped): all CUDA tensors, and the stream if given, on one device."""
+    devs = {t.device.index for t in tensors if t is not None and t.device.type == "cuda"}
+    if len(devs) != 1:
+        raise ValueError("the device tensors of one call must all be on the same CUDA device")
+    index = devs.pop()
+    if stream is not None and stream.device.index != index:
+        raise ValueError(f"stream is on {stream.device}, the tensors on cuda:{index}")
+    return _device_guard(index)
+
+
 def decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0):
     return int(load().pkv_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                                 num_ctas))
@@ -210,23 +259,23 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
     block_tables: int32 [N][MB]; context_lens: int32 [N]; status: int32 [1]
     device tensor or None.  A workspace is allocated (by torch) when None.
     """
-    torch = _need(query, __import__("torch").float16, "query", 3)
-    _need(out, torch.float16, "out", 3)
-    _need(key_cache, torch.float16, "key_cache", 4)
-    _need(value_cache, torch.float16, "value_cache", 4)
-    _need(block_tables, torch.int32, "block_tables", 2)
-    _need(context_lens, torch.int32, "context_lens", 1)
+    import torch
+    _need_all((query, torch.float16, "query", 3), (out, torch.float16, "out", 3),
+              (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+              (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1))
     n, h, d = query.shape
     nb, hkv, bs, d2 = key_cache.shape
     if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
             or block_tables.shape[0] != n or context_lens.shape[0] != n:
         raise ValueError("inconsistent shapes")
-    if workspace is None:
-        workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
-    rc = load().pkv_paged_attention_decode(
-        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale), int(num_ctas),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    with _one_device((out, query, key_cache, value_cache, block_tables, context_lens, workspace, status), stream):
+        if workspace is None:
+            workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+        ws, ws_bytes = _workspace(workspace)
+        rc = load().pkv_paged_attention_decode(
+            _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+            block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale), int(num_ctas),
+            ws, ws_bytes, _status_ptr(status), _stream(stream))
     _check(rc, "pkv_paged_attention_decode")
     return out
 
@@ -236,26 +285,26 @@ def paged_attention_decode_append(out, query, key, value, key_cache, value_cache
     """pkv_paged_attention_decode_append: write each sequence's new token
     (key/value fp16 [N][Hkv][D], position context_len - 1) and attend, in one
     launch."""
-    torch = _need(query, __import__("torch").float16, "query", 3)
-    _need(key, torch.float16, "key", 3)
-    _need(value, torch.float16, "value", 3)
-    _need(out, torch.float16, "out", 3)
-    _need(key_cache, torch.float16, "key_cache", 4)
-    _need(value_cache, torch.float16, "value_cache", 4)
-    _need(block_tables, torch.int32, "block_tables", 2)
-    _need(context_lens, torch.int32, "context_lens", 1)
+    import torch
+    _need_all((query, torch.float16, "query", 3), (key, torch.float16, "key", 3),
+              (value, torch.float16, "value", 3), (out, torch.float16, "out", 3),
+              (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+              (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1))
     n, h, d = query.shape
     nb, hkv, bs, d2 = key_cache.shape
     if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
             or tuple(key.shape) != (n, hkv, d) or tuple(value.shape) != (n, hkv, d) \
             or block_tables.shape[0] != n or context_lens.shape[0] != n:
         raise ValueError("inconsistent shapes")
-    if workspace is None:
-        workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
-    rc = load().pkv_paged_attention_decode_append(
-        _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
-        block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale), int(num_ctas),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    with _one_device((out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
+                      status), stream):
+        if workspace is None:
+            workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+        ws, ws_bytes = _workspace(workspace)
+        rc = load().pkv_paged_attention_decode_append(
+            _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale),
+            int(num_ctas), ws, ws_bytes, _status_ptr(status), _stream(stream))
     _check(rc, "pkv_paged_attention_decode_append")
     return out
 
@@ -265,45 +314,54 @@ class DecodePlan:
     times with the same tensors (their contents may change between launches).
     With key/value given, each launch appends the new tokens and attends
     (paged_attention_decode_append); without, it only attends.  The plan keeps
-    references to every tensor it was built from."""
+    references to every tensor it was built from, and launch() and step() run
+    on their device; launch_raw() and step_raw() expect it to be current."""
 
     def __init__(self, out, query, key_cache, value_cache, block_tables, context_lens, scale, key=None,
                  value=None, num_ctas=0, workspace=None, status=None):
-        torch = _need(query, __import__("torch").float16, "query", 3)
-        _need(out, torch.float16, "out", 3)
-        _need(key_cache, torch.float16, "key_cache", 4)
-        _need(value_cache, torch.float16, "value_cache", 4)
-        _need(block_tables, torch.int32, "block_tables", 2)
-        _need(context_lens, torch.int32, "context_lens", 1)
+        import torch
         if (key is None) != (value is None):
             raise ValueError("key and value go together")
+        specs = [(query, torch.float16, "query", 3), (out, torch.float16, "out", 3),
+                 (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+                 (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1)]
+        if key is not None:
+            specs += [(key, torch.float16, "key", 3), (value, torch.float16, "value", 3)]
+        _need_all(*specs)
         n, h, d = query.shape
         nb, hkv, bs, d2 = key_cache.shape
         if key is not None:
-            _need(key, torch.float16, "key", 3)
-            _need(value, torch.float16, "value", 3)
             if tuple(key.shape) != (n, hkv, d) or tuple(value.shape) != (n, hkv, d):
                 raise ValueError("inconsistent shapes")
         if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
                 or block_tables.shape[0] != n or context_lens.shape[0] != n:
             raise ValueError("inconsistent shapes")
-        if workspace is None:
-            workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
-        self._keep = (out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
-                      status)
         self._lib = load()
         handle = ctypes.c_void_p()
-        rc = self._lib.pkv_decode_plan_create(
-            _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
-            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb, float(scale),
-            int(num_ctas), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
-            ctypes.byref(handle))
+        with _one_device((out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
+                          status)):
+            if workspace is None:
+                workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+            ws, ws_bytes = _workspace(workspace)
+            rc = self._lib.pkv_decode_plan_create(
+                _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb,
+                float(scale), int(num_ctas), ws, ws_bytes, _status_ptr(status), ctypes.byref(handle))
         _check(rc, "pkv_decode_plan_create")
+        self._keep = (out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
+                      status)
+        self._device = query.device.index
         self._h = handle
         self.out = out
 
+    def _guard(self, stream):
+        if stream is not None and stream.device.index != self._device:
+            raise ValueError(f"stream is on {stream.device}, the plan on cuda:{self._device}")
+        return _device_guard(self._device)
+
     def launch(self, stream=None):
-        _check(self._lib.pkv_decode_plan_launch(self._h, _stream(stream)), "pkv_decode_plan_launch")
+        with self._guard(stream):
+            _check(self._lib.pkv_decode_plan_launch(self._h, _stream(stream)), "pkv_decode_plan_launch")
         return self.out
 
     def launch_raw(self, stream_handle):
@@ -327,9 +385,12 @@ class DecodePlan:
             if host_out.is_cuda or not host_out.is_contiguous() or \
                     host_out.numel() * host_out.element_size() != self.out.numel() * self.out.element_size():
                 raise ValueError("host_out must be a contiguous host tensor the size of out")
-        _check(self._lib.pkv_decode_plan_step(self._h, _ptr(dev_in) if nbytes else None,
-                                              _ptr(host_in) if nbytes else None, nbytes,
-                                              _ptr(host_out), _stream(stream)), "pkv_decode_plan_step")
+        if nbytes and dev_in.device.index != self._device:
+            raise ValueError(f"dev_in is on {dev_in.device}, the plan on cuda:{self._device}")
+        with self._guard(stream):
+            _check(self._lib.pkv_decode_plan_step(self._h, _ptr(dev_in) if nbytes else None,
+                                                  _ptr(host_in) if nbytes else None, nbytes,
+                                                  _ptr(host_out), _stream(stream)), "pkv_decode_plan_step")
         return host_out
 
     def step_raw(self, dev_in_ptr, host_in_ptr, nbytes, host_out_ptr, stream_handle):
@@ -352,29 +413,31 @@ class DecodePlan:
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None, stream=None):
     """pkv_reshape_and_cache: key/value fp16 [T][Hkv][D], slot_mapping int64 [T]."""
-    torch = _need(key, __import__("torch").float16, "key", 3)
-    _need(value, torch.float16, "value", 3)
-    _need(key_cache, torch.float16, "key_cache", 4)
-    _need(value_cache, torch.float16, "value_cache", 4)
-    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    import torch
+    _need_all((key, torch.float16, "key", 3), (value, torch.float16, "value", 3),
+              (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+              (slot_mapping, torch.int64, "slot_mapping", 1))
     t, hkv, d = key.shape
     nb, hkv2, bs, d2 = key_cache.shape
     if hkv2 != hkv or d2 != d or tuple(value.shape) != tuple(key.shape) or slot_mapping.shape[0] != t:
         raise ValueError("inconsistent shapes")
-    rc = load().pkv_reshape_and_cache(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
-                                      _ptr(slot_mapping), t, hkv, d, bs, nb, _ptr(status), _stream(stream))
+    with _one_device((key, value, key_cache, value_cache, slot_mapping, status), stream):
+        rc = load().pkv_reshape_and_cache(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                          _ptr(slot_mapping), t, hkv, d, bs, nb, _status_ptr(status),
+                                          _stream(stream))
     _check(rc, "pkv_reshape_and_cache")
 
 
 def copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None):
     """pkv_copy_blocks: block_pairs int64 [n][2] (src, dst) on the device."""
-    torch = _need(key_cache, __import__("torch").float16, "key_cache", 4)
-    _need(value_cache, torch.float16, "value_cache", 4)
-    _need(block_pairs, torch.int64, "block_pairs", 2)
+    import torch
+    _need_all((key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+              (block_pairs, torch.int64, "block_pairs", 2))
     nb = key_cache.shape[0]
     block_bytes = key_cache[0].numel() * key_cache.element_size()
-    rc = load().pkv_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_pairs), block_pairs.shape[0],
-                                block_bytes, nb, _ptr(status), _stream(stream))
+    with _one_device((key_cache, value_cache, block_pairs, status), stream):
+        rc = load().pkv_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(block_pairs),
+                                    block_pairs.shape[0], block_bytes, nb, _status_ptr(status), _stream(stream))
     _check(rc, "pkv_copy_blocks")
 
 
@@ -400,8 +463,10 @@ def reshape_and_cache_layers(keys, values, key_caches, value_caches, slot_mappin
     t_, hkv, d = keys[0].shape
     nb, _, bs, _ = key_caches[0].shape
     ka, va, kca, vca = _ptr_array(keys), _ptr_array(values), _ptr_array(key_caches), _ptr_array(value_caches)
-    rc = load().pkv_reshape_and_cache_layers(ka, va, kca, vca, n, _ptr(slot_mapping), t_, hkv, d, bs, nb,
-                                             _ptr(status), _stream(stream))
+    with _one_device(list(keys) + list(values) + list(key_caches) + list(value_caches) + [slot_mapping, status],
+                     stream):
+        rc = load().pkv_reshape_and_cache_layers(ka, va, kca, vca, n, _ptr(slot_mapping), t_, hkv, d, bs, nb,
+                                                 _status_ptr(status), _stream(stream))
     _check(rc, "pkv_reshape_and_cache_layers")
 
 
@@ -416,8 +481,10 @@ def copy_blocks_layers(key_caches, value_caches, block_pairs, status=None, strea
     _need(block_pairs, torch.int64, "block_pairs", 2)
     nb = key_caches[0].shape[0]
     block_bytes = key_caches[0][0].numel() * key_caches[0].element_size()
-    rc = load().pkv_copy_blocks_layers(_ptr_array(key_caches), _ptr_array(value_caches), n, _ptr(block_pairs),
-                                       block_pairs.shape[0], block_bytes, nb, _ptr(status), _stream(stream))
+    with _one_device(list(key_caches) + list(value_caches) + [block_pairs, status], stream):
+        rc = load().pkv_copy_blocks_layers(_ptr_array(key_caches), _ptr_array(value_caches), n,
+                                           _ptr(block_pairs), block_pairs.shape[0], block_bytes, nb,
+                                           _status_ptr(status), _stream(stream))
     _check(rc, "pkv_copy_blocks_layers")
 
 
@@ -442,9 +509,10 @@ def swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, status=None
         raise ValueError("source and destination pools must have the same block shape")
     _need(block_pairs, torch.int64, "block_pairs", 2)
     block_bytes = src_key[0].numel() * src_key.element_size()
-    rc = load().pkv_swap_blocks(_ptr(src_key), _ptr(src_value), _ptr(dst_key), _ptr(dst_value),
-                                _ptr(block_pairs), block_pairs.shape[0], block_bytes, src_key.shape[0],
-                                dst_key.shape[0], _ptr(status), _stream(stream))
+    with _one_device((src_key, src_value, dst_key, dst_value, block_pairs, status), stream):
+        rc = load().pkv_swap_blocks(_ptr(src_key), _ptr(src_value), _ptr(dst_key), _ptr(dst_value),
+                                    _ptr(block_pairs), block_pairs.shape[0], block_bytes, src_key.shape[0],
+                                    dst_key.shape[0], _status_ptr(status), _stream(stream))
     _check(rc, "pkv_swap_blocks")
 
 
@@ -466,10 +534,12 @@ def swap_blocks_layers(src_keys, src_values, dst_keys, dst_values, block_pairs, 
         raise ValueError("source and destination pools must have the same block shape")
     _need(block_pairs, torch.int64, "block_pairs", 2)
     block_bytes = src_keys[0][0].numel() * src_keys[0].element_size()
-    rc = load().pkv_swap_blocks_layers(_ptr_array(src_keys), _ptr_array(src_values), _ptr_array(dst_keys),
-                                       _ptr_array(dst_values), n, _ptr(block_pairs), block_pairs.shape[0],
-                                       block_bytes, src_keys[0].shape[0], dst_keys[0].shape[0], _ptr(status),
-                                       _stream(stream))
+    with _one_device(list(src_keys) + list(src_values) + list(dst_keys) + list(dst_values) +
+                     [block_pairs, status], stream):
+        rc = load().pkv_swap_blocks_layers(_ptr_array(src_keys), _ptr_array(src_values), _ptr_array(dst_keys),
+                                           _ptr_array(dst_values), n, _ptr(block_pairs), block_pairs.shape[0],
+                                           block_bytes, src_keys[0].shape[0], dst_keys[0].shape[0],
+                                           _status_ptr(status), _stream(stream))
     _check(rc, "pkv_swap_blocks_layers")
 
 
@@ -480,7 +550,12 @@ def validate_block_pairs(pairs, num_blocks):
 
 
 def selftest_wait_timeout(status, limit_ns, stream=None):
-    rc = load().pkv_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream))
+    """pkv_selftest_wait_timeout: a bounded device wait that gives up and
+    reports PKV_ERR_DEVICE_TIMEOUT in status (int32 CUDA tensor)."""
+    if status is None:
+        raise ValueError("status is required")
+    with _one_device((status,), stream):
+        rc = load().pkv_selftest_wait_timeout(_status_ptr(status), int(limit_ns), _stream(stream))
     _check(rc, "pkv_selftest_wait_timeout")
 
 
