@@ -163,6 +163,7 @@ def test_forked_tables_give_identical_outputs():
     np.testing.assert_array_equal(outs[0], outs[2])
     # after b diverges (copy-on-write, then a different token), a and c still agree
     slot, cow = m.append_token(b)
+    assert cow is not None and cow[0] == tables[1][2]   # b's shared partial last block is copied
     C.copy_blocks(kc, vc, [cow])
     C.reshape_and_cache(rng.standard_normal((1, hkv, d)).astype(np.float16),
                         rng.standard_normal((1, hkv, d)).astype(np.float16), kc, vc, [slot])
