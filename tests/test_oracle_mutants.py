@@ -114,6 +114,27 @@ def _cache_op_mutants():
     }
 
 
+# -- memory accounting -----------------------------------------------------------
+
+def _accounting_mutants():
+    from oracle import accounting as M
+
+    def blocks_floor(n_tokens, block_size):
+        return int(n_tokens) // int(block_size)
+
+    def kv_bytes_keys_only(num_layers, num_kv_heads, head_dim, bytes_per_elem):
+        return num_layers * num_kv_heads * head_dim * bytes_per_elem
+
+    def waste_as_use(lengths, block_size):
+        return sum(int(n) for n in lengths) / M.paged_slots(lengths, block_size)
+
+    return {
+        "blocks_floor": (M, "blocks_for_tokens", blocks_floor),
+        "kv_bytes_keys_only": (M, "kv_bytes_per_token", kv_bytes_keys_only),
+        "waste_as_use": (M, "paged_waste_fraction", waste_as_use),
+    }
+
+
 # -- block manager -------------------------------------------------------------
 
 def _block_manager_mutants():
@@ -186,11 +207,11 @@ def _block_manager_mutants():
 MUTANTS = ["ignore_table", "offset_plus_one", "no_scale", "negated_scores", "unnormalised", "drop_last_token",
            "token_major_layout", "gqa_modulo", "block_offset_swapped", "copy_keys_only", "negative_slots_written",
            "free_list_lifo", "fork_without_refs", "release_to_front", "cow_when_full", "cow_loses_fill",
-           "swap_counts_one"]
+           "swap_counts_one", "blocks_floor", "kv_bytes_keys_only", "waste_as_use"]
 
 
 def _install(name):
-    table = {**_attention_mutants(), **_cache_op_mutants(), **_block_manager_mutants()}
+    table = {**_attention_mutants(), **_cache_op_mutants(), **_accounting_mutants(), **_block_manager_mutants()}
     assert sorted(table) == sorted(MUTANTS)
     owner, attr, fn = table[name]
     setattr(owner, attr, fn)
