@@ -565,7 +565,8 @@ def selftest_wait_timeout(status, limit_ns, stream=None):
 class BlockAllocator:
     """The C++ block manager (pkv_alloc_*).  Same method names as the rules
     describe: new_seq, append_token, append_tokens, append_batch, fork,
-    release, export."""
+    release, export.  Not thread-safe (like the C object): one thread, or the
+    caller's lock, per allocator."""
 
     def __init__(self, num_blocks, block_size, initial_free_order=None):
         lib = load()
