@@ -221,14 +221,16 @@ def _install(name):
 def pin_runs():
     """Exit code and output of the pin run for every mutant and for none;
     the children run side by side (each is independent)."""
-    procs = {m: subprocess.Popen([sys.executable, os.path.abspath(__file__), m], cwd=ROOT, text=True,
-                                 stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
-             for m in ["none"] + MUTANTS}
-    out = {}
-    for m, p in procs.items():
-        text, _ = p.communicate(timeout=600)
-        out[m] = (p.returncode, text[-3000:])
-    return out
+    from concurrent.futures import ThreadPoolExecutor
+    env = dict(os.environ, OMP_NUM_THREADS="1", MKL_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1")
+
+    def run(m):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), m], cwd=ROOT, env=env, text=True,
+                           stdout=subprocess.PIPE, stderr=subprocess.STDOUT, timeout=600)
+        return m, (r.returncode, r.stdout[-3000:])
+
+    with ThreadPoolExecutor(max_workers=max(2, os.cpu_count() or 2)) as pool:
+        return dict(pool.map(run, ["none"] + MUTANTS))
 
 
 def test_unmutated_oracle_passes_its_pins(pin_runs):
