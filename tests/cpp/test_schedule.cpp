@@ -321,6 +321,15 @@ int main() {
     run_case({1}, 1, 16, 16, 1, 1000);
     run_case({0, 5, 0, 0, 17, 0}, 3, 16, 16, 2, 3);
     run_case({4096, 256, 1000}, 8, 32, 16, 128, 1216);
+    // the largest batch (4096 sequences): short contexts, some empty, one long
+    for (int bs : {16, 128}) {
+        std::vector<int> ctx(4096);
+        for (auto &c : ctx) c = (rng() % 20 == 0) ? 0 : (int)(rng() % 25);
+        ctx[1234] = 3000;
+        const int mb = (3000 + bs - 1) / bs;
+        run_case(ctx, 1, bs, 16, mb, 1216);
+        run_case(ctx, 1, bs, 16, mb, 8);
+    }
     CHECK(relieved > 1000, "relief exercised only %ld times", relieved);
     if (fails) { std::printf("%d failures\n", fails); return 1; }
     std::printf("schedule ok: %d random cases (%ld relieved CTA ends)\n", cases, relieved);

@@ -150,6 +150,28 @@ def test_brute_force_shapes(pkv, d, bs, group):
         assert (out[lens == 0] == 0).all()
 
 
+@pytest.mark.parametrize("d,bs,group,hkv,max_len", [(128, 16, 8, 1, 24), (64, 128, 2, 1, 24)])
+def test_maximum_batch(pkv, d, bs, group, hkv, max_len):
+    """num_seqs at its limit (4096): the per-sequence arrays take the most
+    shared memory there; short contexts (some empty) plus one long one that is
+    cut across workers; every row against the oracle, on the default grid and
+    on a single CTA."""
+    rng = np.random.default_rng(4096 + d + bs)
+    n = 4096
+    lens = rng.integers(0, max_len + 1, n)
+    lens[rng.random(n) < 0.05] = 0
+    lens[1234] = 3000
+    q, kc, vc, tables, lens = _random_case(rng, n, hkv * group, hkv, d, bs, lens)
+    scale = 1.0 / math.sqrt(d)
+    ref = OA.paged_decode_attention(q, kc, vc, tables, lens, scale)
+    for num_ctas in (0, 1):
+        out, st = _run_gpu(pkv, q, kc, vc, tables, lens, scale, num_ctas)
+        assert st == 0
+        assert np.isfinite(out).all()
+        assert np.max(np.abs(out - ref)) <= TOL, (num_ctas, np.max(np.abs(out - ref)))
+        assert (out[lens == 0] == 0).all()
+
+
 def test_long_context_and_many_pieces(pkv):
     """One 32k-token sequence among short ones: cut across many workers."""
     rng = np.random.default_rng(5)
