@@ -543,6 +543,42 @@ int pkv_host_block_fill(const pkv_alloc_t *a, int block, int *fill);
 int pkv_num_free_host(const pkv_alloc_t *a, int *num_free);
 int pkv_host_free_list(const pkv_alloc_t *a, int32_t *out, int cap, int *n);
 
+/*
+ * Checkpoint of the block manager: its whole state as a byte blob, and an
+ * object rebuilt from one.  The KV contents are the caller's device (or
+ * pinned host) memory and are not part of it; a blob restores the tables
+ * that index them.
+ *
+ * pkv_alloc_save: *bytes (required) receives the blob's size.  buf == NULL
+ *   asks for the size only (PKV_OK).  Otherwise cap must be >= that size
+ *   (else PKV_ERR_INVALID_ARG, nothing written) and the blob is written to
+ *   buf (host memory, caller-owned).
+ * pkv_alloc_load: builds a new object from `bytes` bytes at buf and stores
+ *   it in *out (destroy it with pkv_alloc_destroy).  The restored object is
+ *   indistinguishable from the saved one: same free-list orders, counts,
+ *   fills, sequence ids (the next new id included), swap states and tables,
+ *   so every later call gives the same results on both.
+ *
+ * Blob format (version 1), every field a little-endian int32 unless noted:
+ *   magic 0x41564B50 ("PKVA" in memory), version, num_blocks, block_size,
+ *   num_host_blocks, number of sequence ids handed out (M);
+ *   device free list: its length F, then F block ids in FIFO order;
+ *   device fills: num_blocks entries;
+ *   host free list: length, then ids in FIFO order; host fills:
+ *   num_host_blocks entries;
+ *   M sequence records: flags (bit 0 alive, bit 1 swapped out), table
+ *   length L, then L block ids (host block ids when swapped out).
+ * Reference counts are not stored: they are the number of table entries
+ * naming each block.  A blob is accepted only if it is a state the rules
+ * above can reach: fields in range, every block either free (count 0, fill
+ * 0, listed once) or held, every block but a table's last one full, a last
+ * block holding 1..block_size tokens, no table or swap flag on a released
+ * id, and no bytes left over.  Anything else returns PKV_ERR_INVALID_ARG
+ * and leaves *out untouched.
+ */
+int pkv_alloc_save(const pkv_alloc_t *a, void *buf, size_t cap, size_t *bytes);
+int pkv_alloc_load(const void *buf, size_t bytes, pkv_alloc_t **out);
+
 /* ------------------------------------------------------------------------ */
 /* Self-test                                                                 */
 /* ------------------------------------------------------------------------ */

@@ -68,6 +68,8 @@ SIGNATURES = {
     "pkv_copy_blocks_layers": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _c_size, _c_int, _vp, _vp]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, _i32p, ctypes.POINTER(_vp)]),
     "pkv_alloc_destroy": (None, [_vp]),
+    "pkv_alloc_save": (_c_int, [_vp, _vp, _c_size, ctypes.POINTER(_c_size)]),
+    "pkv_alloc_load": (_c_int, [_vp, _c_size, ctypes.POINTER(_vp)]),
     "pkv_seq_new": (_c_int, [_vp, _intp]),
     "pkv_append_token": (_c_int, [_vp, _c_int, _i64p, _i32p]),
     "pkv_append_tokens": (_c_int, [_vp, _c_int, _c_int, _i64p, _i32p, _intp]),
@@ -139,6 +141,9 @@ def load(path=None):
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+_load_library = load
 
 
 def status_string(status):
@@ -682,6 +687,30 @@ class BlockAllocator:
         _check(self._lib.pkv_free_list(self._h, out.ctypes.data_as(_i32p), self.num_blocks,
                                        ctypes.byref(self._i)), "pkv_free_list")
         return out[:self._i.value].tolist()
+
+    # -- checkpoint ------------------------------------------------------------
+    def save(self):
+        """The whole block-manager state as bytes (pkv_alloc_save)."""
+        n = ctypes.c_size_t()
+        _check(self._lib.pkv_alloc_save(self._h, None, 0, ctypes.byref(n)), "pkv_alloc_save")
+        buf = ctypes.create_string_buffer(max(n.value, 1))
+        _check(self._lib.pkv_alloc_save(self._h, buf, n.value, ctypes.byref(n)), "pkv_alloc_save")
+        return buf.raw[:n.value]
+
+    @classmethod
+    def load(cls, blob):
+        """A block manager restored from save()'s bytes (pkv_alloc_load);
+        refuses (PkvError) any blob that is not a reachable state."""
+        blob = bytes(blob)
+        self = cls.__new__(cls)
+        self._lib = _load_library()
+        handle = ctypes.c_void_p()
+        _check(self._lib.pkv_alloc_load(blob, len(blob), ctypes.byref(handle)), "pkv_alloc_load")
+        self._h = handle
+        self._i = ctypes.c_int()
+        self.num_blocks, self.block_size, self.num_host_blocks = (
+            int(v) for v in np.frombuffer(blob, dtype="<i4", count=3, offset=8))
+        return self
 
     # -- swapping ------------------------------------------------------------
     def host_pool(self, num_host_blocks, host_free_order=None):

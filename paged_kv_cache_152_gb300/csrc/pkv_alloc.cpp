@@ -468,3 +468,180 @@ extern "C" int pkv_host_free_list(const pkv_alloc_t *a, int32_t *out, int cap, i
     if (n) *n = i;
     return PKV_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Checkpoint (format and acceptance rules in the header)
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr uint32_t kBlobMagic = 0x41564B50u;  // "PKVA" as little-endian bytes
+constexpr int32_t kBlobVersion = 1;
+
+// Little-endian int32 writer; counts bytes when out is null.
+struct BlobWriter {
+    unsigned char *out;
+    size_t n = 0;
+    void i32(int32_t v) {
+        const uint32_t u = (uint32_t)v;
+        if (out)
+            for (int k = 0; k < 4; ++k) out[n + k] = (unsigned char)(u >> (8 * k));
+        n += 4;
+    }
+    template <class C>
+    void ids(const C &c) {
+        i32((int32_t)c.size());
+        for (int32_t b : c) i32(b);
+    }
+};
+
+// Little-endian int32 reader that fails (instead of reading past the end).
+struct BlobReader {
+    const unsigned char *in;
+    size_t size, n = 0;
+    bool ok = true;
+    int32_t i32() {
+        if (!ok || size - n < 4) {
+            ok = false;
+            return 0;
+        }
+        uint32_t u = 0;
+        for (int k = 0; k < 4; ++k) u |= (uint32_t)in[n + k] << (8 * k);
+        n += 4;
+        return (int32_t)u;
+    }
+    // a count of int32 items that must still fit in the blob
+    int32_t count(int64_t max_items) {
+        const int32_t c = i32();
+        if (!ok || c < 0 || c > max_items || (size_t)c > (size - n) / 4) ok = false;
+        return ok ? c : 0;
+    }
+};
+
+void write_state(const pkv_alloc &a, BlobWriter &w) {
+    w.i32((int32_t)kBlobMagic);
+    w.i32(kBlobVersion);
+    w.i32(a.num_blocks);
+    w.i32(a.block_size);
+    w.i32(a.num_host_blocks);
+    w.i32((int32_t)a.seqs.size());
+    w.ids(a.free_list);
+    for (int32_t f : a.fill) w.i32(f);
+    w.ids(a.host_free_list);
+    for (int32_t f : a.host_fill) w.i32(f);
+    for (const pkv_alloc::Seq &s : a.seqs) {
+        w.i32((s.alive ? 1 : 0) | (s.swapped ? 2 : 0));
+        w.ids(s.table);
+    }
+}
+
+// One pool's part of the acceptance check: the free list and the holders
+// (counts rebuilt from the tables) partition the pool, free blocks have fill
+// 0, and held blocks obey the fill rules recorded in full / last.
+bool pool_consistent(int nb, int bs, const std::deque<int32_t> &free_list, const std::vector<int32_t> &refs,
+                     const std::vector<int32_t> &fill, const std::vector<char> &non_last,
+                     const std::vector<char> &last) {
+    std::vector<char> listed(nb, 0);
+    for (int32_t b : free_list) {
+        if (b < 0 || b >= nb || listed[b]) return false;
+        listed[b] = 1;
+    }
+    for (int b = 0; b < nb; ++b) {
+        if (fill[b] < 0 || fill[b] > bs) return false;
+        if (refs[b] == 0) {
+            if (!listed[b] || fill[b] != 0) return false;
+        } else {
+            if (listed[b]) return false;
+            if (non_last[b] && fill[b] != bs) return false;
+            if (last[b] && fill[b] < 1) return false;
+        }
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" int pkv_alloc_save(const pkv_alloc_t *a, void *buf, size_t cap, size_t *bytes) {
+    if (!a || !bytes) return PKV_ERR_INVALID_ARG;
+    BlobWriter count{nullptr};
+    write_state(*a, count);
+    *bytes = count.n;
+    if (!buf) return PKV_OK;
+    if (cap < count.n) return PKV_ERR_INVALID_ARG;
+    BlobWriter w{static_cast<unsigned char *>(buf)};
+    write_state(*a, w);
+    return PKV_OK;
+}
+
+extern "C" int pkv_alloc_load(const void *buf, size_t bytes, pkv_alloc_t **out) {
+    if (!buf || !out) return PKV_ERR_INVALID_ARG;
+    BlobReader r{static_cast<const unsigned char *>(buf), bytes};
+    if ((uint32_t)r.i32() != kBlobMagic || r.i32() != kBlobVersion) return PKV_ERR_INVALID_ARG;
+    const int32_t nb = r.i32(), bs = r.i32(), nh = r.i32(), m = r.i32();
+    if (!r.ok || nb <= 0 || bs <= 0 || nh < 0 || m < 0 || (int64_t)nb * bs > INT64_C(1) << 40)
+        return PKV_ERR_INVALID_ARG;
+    // every array must fit in what is left before anything is allocated
+    const size_t left = bytes - r.n;
+    if ((size_t)nb + (size_t)nh + 2 * (size_t)m + 2 > left / 4) return PKV_ERR_INVALID_ARG;
+
+    std::deque<int32_t> free_list, host_free_list;
+    std::vector<int32_t> fill(nb), host_fill(nh);
+    for (int32_t i = 0, f = r.count(nb); i < f; ++i) free_list.push_back(r.i32());
+    for (int32_t &v : fill) v = r.i32();
+    for (int32_t i = 0, f = r.count(nh); i < f; ++i) host_free_list.push_back(r.i32());
+    for (int32_t &v : host_fill) v = r.i32();
+    std::vector<pkv_alloc::Seq> seqs(m);
+    for (pkv_alloc::Seq &s : seqs) {
+        const int32_t flags = r.i32();
+        if (flags != 0 && flags != 1 && flags != 3) r.ok = false;
+        s.alive = flags & 1;
+        s.swapped = (flags & 2) != 0;
+        const int32_t len = r.count(s.swapped ? nh : nb);
+        if (!s.alive && len != 0) r.ok = false;
+        s.table.resize(len);
+        for (int32_t &b : s.table) b = r.i32();
+        if (!r.ok) break;
+    }
+    if (!r.ok || r.n != bytes) return PKV_ERR_INVALID_ARG;
+
+    // counts from the tables, and the rules a reachable state obeys
+    std::vector<int32_t> refs(nb, 0), host_refs(nh, 0);
+    std::vector<char> non_last(nb, 0), last(nb, 0), host_non_last(nh, 0), host_last(nh, 0);
+    std::vector<int32_t> seen(nb, -1), host_seen(nh, -1), pos(nb, -1), host_pos(nh, -1);
+    for (int32_t id = 0; id < m; ++id) {
+        const pkv_alloc::Seq &s = seqs[id];
+        const int32_t pool = s.swapped ? nh : nb;
+        std::vector<int32_t> &cnt = s.swapped ? host_refs : refs;
+        std::vector<char> &nl = s.swapped ? host_non_last : non_last;
+        std::vector<char> &ls = s.swapped ? host_last : last;
+        std::vector<int32_t> &sn = s.swapped ? host_seen : seen;
+        std::vector<int32_t> &ps = s.swapped ? host_pos : pos;
+        for (size_t i = 0; i < s.table.size(); ++i) {
+            const int32_t b = s.table[i];
+            if (b < 0 || b >= pool || sn[b] == id) return PKV_ERR_INVALID_ARG;  // outside, or twice in one table
+            if (ps[b] >= 0 && ps[b] != (int32_t)i) return PKV_ERR_INVALID_ARG;  // a shared block moved
+            sn[b] = id;
+            ps[b] = (int32_t)i;
+            cnt[b] += 1;
+            (i + 1 < s.table.size() ? nl : ls)[b] = 1;
+        }
+    }
+    if (!pool_consistent(nb, bs, free_list, refs, fill, non_last, last) ||
+        !pool_consistent(nh, bs, host_free_list, host_refs, host_fill, host_non_last, host_last))
+        return PKV_ERR_INVALID_ARG;
+
+    pkv_alloc *a = new (std::nothrow) pkv_alloc;
+    if (!a) return PKV_ERR_INVALID_ARG;
+    a->num_blocks = nb;
+    a->block_size = bs;
+    a->free_list = std::move(free_list);
+    a->refs = std::move(refs);
+    a->fill = std::move(fill);
+    a->num_host_blocks = nh;
+    a->host_free_list = std::move(host_free_list);
+    a->host_refs = std::move(host_refs);
+    a->host_fill = std::move(host_fill);
+    a->seqs = std::move(seqs);
+    *out = a;
+    return PKV_OK;
+}

@@ -2,7 +2,10 @@
 // AddressSanitizer and UndefinedBehaviorSanitizer (tests/test_native_host.py).
 // After every call: blocks and references are conserved in both pools, every
 // table matches its context length, and a call that fails leaves the whole
-// state exactly as it was.  Exits non-zero on the first violation.
+// state exactly as it was.  Every 50 calls the state is checkpointed: the
+// restored object must equal the saved one (and the fuzzing goes on with it
+// half of the time), and corrupted blobs must be refused or load as a state
+// that keeps the invariants.  Exits non-zero on the first violation.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -168,6 +171,82 @@ struct Fuzz {
     }
 };
 
+// The object a blob describes, seen through the Fuzz checks: its live ids
+// are probed (the blob header says how many ids were handed out).
+static Fuzz view_of(pkv_alloc_t *b, const std::vector<unsigned char> &blob) {
+    Fuzz g;
+    g.a = b;
+    auto field = [&](int k) {
+        uint32_t u = 0;
+        for (int i = 0; i < 4; ++i) u |= (uint32_t)blob[4 * k + i] << (8 * i);
+        return (int)u;
+    };
+    g.nb = field(2);
+    g.bs = field(3);
+    g.nh = field(4);
+    for (int id = 0, m = field(5); id < m; ++id) {
+        int len = 0;
+        if (pkv_seq_length(b, id, &len) == PKV_OK) g.live.insert(id);
+    }
+    return g;
+}
+
+static std::vector<unsigned char> save(pkv_alloc_t *a) {
+    size_t n = 0;
+    CHECK(pkv_alloc_save(a, nullptr, 0, &n) == PKV_OK && n >= 24, "blob size");
+    std::vector<unsigned char> blob(n);
+    size_t n2 = 0;
+    CHECK(pkv_alloc_save(a, blob.data(), n, &n2) == PKV_OK && n2 == n, "save");
+    if (n > 0) {
+        std::vector<unsigned char> small(n - 1);
+        CHECK(pkv_alloc_save(a, small.data(), n - 1, &n2) == PKV_ERR_INVALID_ARG, "short buffer accepted");
+    }
+    return blob;
+}
+
+static long loads_accepted = 0, loads_refused = 0;
+
+// Save, restore, compare; then corrupt the blob in several ways.
+static void checkpoint(Fuzz &f) {
+    const std::vector<unsigned char> blob = save(f.a);
+    pkv_alloc_t *b = nullptr;
+    CHECK(pkv_alloc_load(blob.data(), blob.size(), &b) == PKV_OK, "load of a saved state");
+    if (!b) return;
+    Fuzz g = view_of(b, blob);
+    CHECK(g.live == f.live, "live ids differ after restore");
+    CHECK(g.snap() == f.snap(), "restored state differs");
+    CHECK(save(b) == blob, "re-saved blob differs");
+    if (f.rng() % 2) {  // go on with the restored object
+        pkv_alloc_destroy(f.a);
+        f.a = b;
+    } else {
+        pkv_alloc_destroy(b);
+    }
+    for (int k = 0; k < 20; ++k) {
+        std::vector<unsigned char> bad = blob;
+        switch (f.rng() % 4) {
+            case 0: bad[f.rng() % bad.size()] ^= (unsigned char)(1u << (f.rng() % 8)); break;
+            case 1: bad.resize(f.rng() % bad.size()); break;
+            case 2: bad.push_back((unsigned char)f.rng()); break;
+            default: {  // a plausible small change to one int32 field
+                const size_t at = 4 * (f.rng() % (bad.size() / 4));
+                bad[at] = (unsigned char)(bad[at] + (f.rng() % 2 ? 1 : 255));
+            }
+        }
+        pkv_alloc_t *c = nullptr;
+        if (pkv_alloc_load(bad.data(), bad.size(), &c) != PKV_OK) {
+            CHECK(c == nullptr, "refused load wrote *out");
+            ++loads_refused;
+            continue;
+        }
+        ++loads_accepted;
+        Fuzz h = view_of(c, bad);
+        h.invariants(h.snap());
+        CHECK(save(c) == bad, "an accepted blob does not re-save to itself");
+        pkv_alloc_destroy(c);
+    }
+}
+
 int main() {
     long ops = 0, failed_calls = 0;
     for (int trial = 0; trial < 12; ++trial) {
@@ -185,13 +264,18 @@ int main() {
         for (int i = 0; i < 1000; ++i) {
             failed_calls += f.step();
             ++ops;
+            if (i % 50 == 49) checkpoint(f);
         }
         pkv_alloc_destroy(f.a);
     }
+    CHECK(loads_refused > 1000 && loads_accepted > 10, "corruptions: %ld refused, %ld accepted", loads_refused,
+          loads_accepted);
     if (fails) {
         std::printf("%d failures\n", fails);
         return 1;
     }
-    std::printf("alloc fuzz ok: %ld operations (%ld refused, state unchanged)\n", ops, failed_calls);
+    std::printf("alloc fuzz ok: %ld operations (%ld refused, state unchanged); checkpoints: %ld corrupt blobs "
+                "refused, %ld loaded as valid states\n",
+                ops, failed_calls, loads_refused, loads_accepted);
     return 0;
 }

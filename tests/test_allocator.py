@@ -244,7 +244,40 @@ def test_random_operations_with_swaps_bit_exact(pkv, seed):
                 assert [tuple(p) for p in fn(group).tolist()] == expect
         if step % 20 == 0:
             assert_same_state(model, alloc)
+        if step % 37 == 36:   # the rest of the trace runs on a checkpointed copy
+            blob = alloc.save()
+            alloc = pkv.BlockAllocator.load(blob)
+            assert alloc.save() == blob
     assert_same_state(model, alloc)
+
+
+def test_checkpoint_restores_everything_and_refuses_bad_blobs(pkv):
+    a = pkv.BlockAllocator(12, 4, list(range(11, -1, -1)))
+    a.host_pool(6)
+    s0, s1 = a.new_seq(), a.new_seq()
+    a.append_tokens(s0, 9)
+    s2 = a.fork(s0)
+    a.append_tokens(s1, 3)
+    a.swap_out([s1])
+    a.release(s2)
+    blob = a.save()
+    b = pkv.BlockAllocator.load(blob)
+    assert (b.num_blocks, b.block_size, b.num_host_blocks) == (12, 4, 6)
+    assert b.free_list() == a.free_list() and b.host_free_list() == a.host_free_list()
+    assert b.table(s0) == a.table(s0) and b.is_swapped(s1) and b.seq_len(s1) == 3
+    assert b.new_seq() == a.new_seq() == 3            # ids are not reused after a restore either
+    with pytest.raises(pkv.PkvError):
+        b.table(s2)                                   # released before the checkpoint
+    for bad in (blob[:-4], blob + b"\0\0\0\0", b"", b"XKVA" + blob[4:], blob[:8] + b"\xff" * 4 + blob[12:]):
+        with pytest.raises(pkv.PkvError):
+            pkv.BlockAllocator.load(bad)
+    # a fill below a full block in the middle of a table is not a reachable state
+    m = bytearray(blob)
+    fills_at = 4 * (6 + 1 + len(a.free_list()))       # header, free-list length, the free ids
+    full = a.table(s0)[0]
+    m[fills_at + 4 * full] = 3
+    with pytest.raises(pkv.PkvError):
+        pkv.BlockAllocator.load(bytes(m))
 
 
 def test_swap_errors(pkv):
