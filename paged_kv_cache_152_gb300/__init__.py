@@ -23,6 +23,7 @@ Names mirror the C ABI without its ``pkv_`` prefix:
 
 import contextlib
 import ctypes
+import functools
 import os
 
 import numpy as np
@@ -145,6 +146,27 @@ def load(path=None):
 
 _load_library = load
 
+# PKV_NVTX=1 (read at import): every device call is an NVTX range named after
+# it, for profilers that filter or group by range (ncu --nvtx).  Off by
+# default; the functions are then the plain ones.
+NVTX = os.environ.get("PKV_NVTX") == "1"
+
+
+def _traced(fn):
+    if not NVTX:
+        return fn
+    import torch
+    name = "pkv." + fn.__qualname__
+
+    @functools.wraps(fn)
+    def ranged(*args, **kwargs):
+        torch.cuda.nvtx.range_push(name)
+        try:
+            return fn(*args, **kwargs)
+        finally:
+            torch.cuda.nvtx.range_pop()
+    return ranged
+
 
 def status_string(status):
     return load().pkv_status_string(int(status)).decode()
@@ -256,6 +278,7 @@ def new_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_c
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+@_traced
 def paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens, scale,
                            num_ctas=0, workspace=None, status=None, stream=None):
     """pkv_paged_attention_decode on torch tensors (see include/pkv.h).
@@ -285,6 +308,7 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
     return out
 
 
+@_traced
 def paged_attention_decode_append(out, query, key, value, key_cache, value_cache, block_tables, context_lens,
                                   scale, num_ctas=0, workspace=None, status=None, stream=None):
     """pkv_paged_attention_decode_append: write each sequence's new token
@@ -364,6 +388,7 @@ class DecodePlan:
             raise ValueError(f"stream is on {stream.device}, the plan on cuda:{self._device}")
         return _device_guard(self._device)
 
+    @_traced
     def launch(self, stream=None):
         with self._guard(stream):
             _check(self._lib.pkv_decode_plan_launch(self._h, _stream(stream)), "pkv_decode_plan_launch")
@@ -374,6 +399,7 @@ class DecodePlan:
         that look the stream up once."""
         _check(self._lib.pkv_decode_plan_launch(self._h, stream_handle), "pkv_decode_plan_launch")
 
+    @_traced
     def step(self, dev_in=None, host_in=None, host_out=None, stream=None):
         """One serving step (pkv_decode_plan_step): host_in -> dev_in (same
         byte size; the region the plan's inputs live in), the launch, then
@@ -416,6 +442,7 @@ class DecodePlan:
             pass
 
 
+@_traced
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=None, stream=None):
     """pkv_reshape_and_cache: key/value fp16 [T][Hkv][D], slot_mapping int64 [T]."""
     import torch
@@ -433,6 +460,7 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, status=N
     _check(rc, "pkv_reshape_and_cache")
 
 
+@_traced
 def copy_blocks(key_cache, value_cache, block_pairs, status=None, stream=None):
     """pkv_copy_blocks: block_pairs int64 [n][2] (src, dst) on the device."""
     import torch
@@ -451,6 +479,7 @@ def _ptr_array(tensors):
     return arr
 
 
+@_traced
 def reshape_and_cache_layers(keys, values, key_caches, value_caches, slot_mapping, status=None, stream=None):
     """pkv_reshape_and_cache_layers: lists (one entry per layer) of key/value
     fp16 [T][Hkv][D] and pools fp16 [NB][Hkv][bs][D]; one slot mapping."""
@@ -475,6 +504,7 @@ def reshape_and_cache_layers(keys, values, key_caches, value_caches, slot_mappin
     _check(rc, "pkv_reshape_and_cache_layers")
 
 
+@_traced
 def copy_blocks_layers(key_caches, value_caches, block_pairs, status=None, stream=None):
     """pkv_copy_blocks_layers: the same (src, dst) pairs in every layer's pool."""
     torch = __import__("torch")
@@ -502,6 +532,7 @@ def _pool(t, name):
     return torch
 
 
+@_traced
 def swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, status=None, stream=None):
     """pkv_swap_blocks: copy block src of the source pools over block dst of
     the destination pools for each (src, dst) in block_pairs (int64 [n][2],
@@ -521,6 +552,7 @@ def swap_blocks(src_key, src_value, dst_key, dst_value, block_pairs, status=None
     _check(rc, "pkv_swap_blocks")
 
 
+@_traced
 def swap_blocks_layers(src_keys, src_values, dst_keys, dst_values, block_pairs, status=None, stream=None):
     """pkv_swap_blocks_layers: swap_blocks for every layer in one launch."""
     torch = __import__("torch")
@@ -554,6 +586,7 @@ def validate_block_pairs(pairs, num_blocks):
     return load().pkv_validate_block_pairs(a.ctypes.data_as(_i64p), a.shape[0], num_blocks) == PKV_OK
 
 
+@_traced
 def selftest_wait_timeout(status, limit_ns, stream=None):
     """pkv_selftest_wait_timeout: a bounded device wait that gives up and
     reports PKV_ERR_DEVICE_TIMEOUT in status (int32 CUDA tensor)."""

@@ -135,3 +135,26 @@ def test_status_word_and_workspace_are_checked():
         pkv.reshape_and_cache(k, k, a["key_cache"], a["value_cache"],
                               torch.zeros(2, dtype=torch.int64, device="cuda"),
                               status=torch.zeros(0, dtype=torch.int32, device="cuda"))
+
+
+def test_nvtx_ranges_are_opt_in():
+    """PKV_NVTX=1 wraps every device call in an NVTX range (a refused call
+    still raises through it); without it the calls are the plain functions."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    probe = ("import torch, paged_kv_cache_152_gb300 as pkv\n"
+             "fns = [pkv.paged_attention_decode, pkv.reshape_and_cache, pkv.copy_blocks, pkv.swap_blocks,\n"
+             "       pkv.DecodePlan.launch, pkv.DecodePlan.step]\n"
+             "print(pkv.NVTX, all(hasattr(f, '__wrapped__') for f in fns))\n"
+             "try:\n"
+             "    pkv.copy_blocks(torch.zeros(2, 1, 16, 64, dtype=torch.float16),\n"
+             "                    torch.zeros(2, 1, 16, 64, dtype=torch.float16), torch.zeros(1, 2, dtype=torch.int64))\n"
+             "except ValueError:\n"
+             "    print('refused')\n")
+    for flag, expect in (("1", "True True\nrefused"), ("0", "False False\nrefused")):
+        r = subprocess.run([sys.executable, "-c", probe], cwd=root, capture_output=True, text=True,
+                           env=dict(os.environ, PKV_NVTX=flag))
+        assert r.returncode == 0, r.stderr
+        assert r.stdout.strip() == expect
