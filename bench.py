@@ -40,7 +40,6 @@ every step (--no-graph: direct binding calls).
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
