@@ -49,6 +49,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+from workloads import BASE_SEED as W_BASE_SEED  # noqa: E402  (numpy only; torch loads lazily)
 
 METRIC = "paged decode attention: KV-read HBM GB/s (% of GB300 peak), seqs/s per layer"
 UNIT = "GB/s"
@@ -77,6 +78,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     p.add_argument("--config", choices=list(WORKLOAD_TEXT), default="7b")
+    p.add_argument("--seed", type=int, default=None,
+                   help="base seed of the workload's draws (lengths, free orders, values); default 152")
     p.add_argument("--num-ctas", type=int, default=0)
     p.add_argument("--block-size", type=int, default=0,
                    help="override the workload's block size (8, 16, 32, 64, 128): the block-size sweep")
@@ -250,14 +253,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the product arm
 
-def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0, block_size=0):
+def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0, block_size=0, seed=None):
     """Allocator + device tensors of a workload at its decode step."""
     import numpy as np
     import torch
     import paged_kv_cache_152_gb300 as pkv
     import workloads as W
 
-    wl = W.make(cfg, block_size=block_size) if block_size else W.make(cfg)
+    kw = {"block_size": block_size} if block_size else {}
+    if seed is not None:
+        kw["base"] = seed
+    wl = W.make(cfg, **kw)
     n = wl.num_seqs
     extra = n * (-(-e2e_headroom_steps // wl.block_size) + 1) if e2e_headroom_steps else 0
     nb = wl.num_blocks + extra
@@ -458,7 +464,7 @@ def run_pkv(args):
     e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
     st = build_state(args.config, device, args.identity_tables,
                      e2e_headroom_steps=e2e_steps + E2E_WARMUP if e2e_steps else 0,
-                     block_size=args.block_size)
+                     block_size=args.block_size, seed=args.seed)
     if not args.two_launch:
         st["fused"] = True
         st["launches_per_step"] -= 1
@@ -538,7 +544,10 @@ def run_pkv(args):
     peak, peak_kind = measured_hbm_peak()
     value = world * kv_bytes * args.steps / (ms_total / 1e3) / 1e9
     achieved = kv_bytes / (dec_mean / 1e3) / 1e9
-    traffic = recorded_traffic(args.config)
+    # the ncu record was taken on the default launch of the default inputs
+    default_launch = not (args.block_size or args.two_launch or args.identity_tables or args.num_ctas
+                          or args.seed not in (None, W_BASE_SEED))
+    traffic = recorded_traffic(args.config) if default_launch else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -554,6 +563,7 @@ def run_pkv(args):
         "storage_dtype": "f16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "seed": args.seed if args.seed is not None else W_BASE_SEED,
                    "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": st["nb"],
                    "sum_context": int(sum(wl.context_lens)), "kv_bytes_per_step": kv_bytes,
@@ -595,7 +605,7 @@ def run_pkv(args):
                                    "step's block-manager work "
                                    "overlaps this step's GPU work"}
     if not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds, args.seed)
     if dist is not None:
         dist.destroy_process_group()
     return line
@@ -617,7 +627,7 @@ def run_layers(args):
     from paged_kv_cache_152_gb300 import build as b
     b.build()
     pkv.load()
-    st = build_state(args.config, device, block_size=args.block_size)
+    st = build_state(args.config, device, block_size=args.block_size, seed=args.seed)
     wl, t = st["wl"], st["t"]
     L = args.layers
     shape = tuple(t["key_cache"].shape)
@@ -696,7 +706,7 @@ def run_swap(args):
     from paged_kv_cache_152_gb300 import build as b
     b.build()
     pkv.load()
-    st = build_state(args.config, device, block_size=args.block_size)
+    st = build_state(args.config, device, block_size=args.block_size, seed=args.seed)
     wl, alloc, t = st["wl"], st["alloc"], st["t"]
     kc, vc = t["key_cache"], t["value_cache"]
     nh = st["nb"]
@@ -768,14 +778,14 @@ def run_swap(args):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 
-def _oracle_worker(cfg, seqs, barrier_, results):
+def _oracle_worker(cfg, seed, seqs, barrier_, results):
     """Spawned process: build the workload (untimed), wait for the others at
     the barrier, run the oracle on `seqs`, report the elapsed seconds."""
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     import torch
     torch.set_num_threads(1)
-    st = _oracle_state(cfg)
+    st = _oracle_state(cfg, seed)
     barrier_.wait()
     t0 = time.perf_counter()
     _oracle_decode(st, seqs)
@@ -785,14 +795,14 @@ def _oracle_worker(cfg, seqs, barrier_, results):
 _ORACLE_CACHE = {}
 
 
-def _oracle_state(cfg):
+def _oracle_state(cfg, seed=None):
     """The workload at its decode step, with the oracle's own tables (CPU)."""
-    if cfg in _ORACLE_CACHE:
-        return _ORACLE_CACHE[cfg]
+    if (cfg, seed) in _ORACLE_CACHE:
+        return _ORACLE_CACHE[(cfg, seed)]
     import numpy as np
     import workloads as W
     from oracle.block_manager import BlockManagerModel
-    wl = W.make(cfg)
+    wl = W.make(cfg) if seed is None else W.make(cfg, base=seed)
     model = BlockManagerModel(wl.num_blocks, wl.block_size, wl.free_order)
     W.replay(model, wl.ops)
     slots = [model.append_token(s)[0] for s in wl.batch]
@@ -801,7 +811,7 @@ def _oracle_state(cfg):
     st = {"wl": wl, "tables": np.array(tables), "lens": np.array(lens), "slots": np.array(slots),
           "q": t["query"].numpy(), "k": t["key"].numpy(), "v": t["value"].numpy(),
           "kc": t["key_cache"].numpy(), "vc": t["value_cache"].numpy()}
-    _ORACLE_CACHE[cfg] = st
+    _ORACLE_CACHE[(cfg, seed)] = st
     return st
 
 
@@ -819,7 +829,7 @@ def _seq_bytes(wl, seqs):
     return sum(2 * wl.context_lens[s] * wl.num_kv_heads * wl.head_dim * 2 for s in seqs)
 
 
-def cpu_baseline(cfg, seconds):
+def cpu_baseline(cfg, seconds, seed=None):
     """Oracle throughput on the host cores, on a bounded sample of the workload.
 
     Single core: the first sequences of the batch, as many as fit in about
@@ -827,7 +837,7 @@ def cpu_baseline(cfg, seconds):
     os.cpu_count() processes (single-threaded BLAS each), timed once.
     """
     import multiprocessing as mp
-    st = _oracle_state(cfg)
+    st = _oracle_state(cfg, seed)
     wl = st["wl"]
     t0 = time.perf_counter()
     _oracle_decode(st, [0])
@@ -846,7 +856,7 @@ def cpu_baseline(cfg, seconds):
         ctx = mp.get_context("spawn")
         bar = ctx.Barrier(len(chunks) + 1)
         results = ctx.Queue()
-        procs = [ctx.Process(target=_oracle_worker, args=(cfg, c, bar, results)) for c in chunks]
+        procs = [ctx.Process(target=_oracle_worker, args=(cfg, seed, c, bar, results)) for c in chunks]
         for p in procs:
             p.start()
         bar.wait()
@@ -872,7 +882,7 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return None
-    st = _oracle_state(args.config)
+    st = _oracle_state(args.config, args.seed)
     wl = st["wl"]
     t0 = time.perf_counter()
     _oracle_decode(st, [0])
@@ -892,7 +902,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config, "sample": sample},
+            "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                       "seed": args.seed if args.seed is not None else W_BASE_SEED, "sample": sample},
             "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -6,6 +6,7 @@ import os
 import subprocess
 import sys
 
+import pytest
 import torch.multiprocessing as mp
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -39,9 +40,11 @@ def test_two_gloo_ranks_take_max_and_sum():
     assert got == [(0, 11.0, 3.0), (1, 11.0, 3.0)]
 
 
-def test_reference_arm_json_line():
+@pytest.mark.parametrize("seed", [None, 7])
+def test_reference_arm_json_line(seed):
+    extra = [] if seed is None else ["--seed", str(seed)]
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--config", "tiny", "--steps", "3", "--warmup", "1"],
+                        "--config", "tiny", "--steps", "3", "--warmup", "1", *extra],
                        capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -52,6 +55,7 @@ def test_reference_arm_json_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"]["seed"] == (152 if seed is None else seed)
 
 
 def test_reference_arm_nonzero_rank_exits_quietly():

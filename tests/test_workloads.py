@@ -61,3 +61,13 @@ def test_tensors_are_seeded():
     for k in a:
         assert a[k].dtype.itemsize == 2 and (a[k] == b[k]).all()
     assert tuple(a["key_cache"].shape) == (64, 8, 16, 64)
+
+
+def test_base_seed_default_and_override():
+    """`base` defaults to BASE_SEED (the inputs every test and record use) and
+    a different base draws different lengths and free orders."""
+    for name in ("7b", "chat", "gqa", "prefix"):
+        a, b, c = W.make(name), W.make(name, base=W.BASE_SEED), W.make(name, base=W.BASE_SEED + 1000)
+        assert a.context_lens == b.context_lens and a.seed == b.seed
+        assert np.array_equal(a.free_order, b.free_order)
+        assert a.context_lens != c.context_lens and c.seed == a.seed + 1000

@@ -91,9 +91,9 @@ def _ceil_div(a, b):
     return -(-int(a) // int(b))
 
 
-def _simple(name, index, lens, heads, kv_heads, head_dim, block_size, pool=None):
+def _simple(name, index, lens, heads, kv_heads, head_dim, block_size, pool=None, base=BASE_SEED):
     """Independent sequences appended one after another, in index order."""
-    rng = np.random.default_rng(BASE_SEED + index)
+    rng = np.random.default_rng(base + index)
     lens = [int(x) for x in lens]
     if pool is None:
         pool = math.ceil(1.25 * sum(_ceil_div(n, block_size) for n in lens))
@@ -105,28 +105,28 @@ def _simple(name, index, lens, heads, kv_heads, head_dim, block_size, pool=None)
             ops.append(("append", s, n - 1))
     return Workload(name, index, heads, kv_heads, head_dim, block_size, pool,
                     free_order, ops, list(range(len(lens))), lens,
-                    1.0 / math.sqrt(head_dim), BASE_SEED + index)
+                    1.0 / math.sqrt(head_dim), base + index)
 
 
-def tiny(block_size=16):
+def tiny(block_size=16, base=BASE_SEED):
     pool = 64 if block_size == 16 else None
-    return _simple("tiny", 0, [40, 17, 100, 5], 8, 8, 64, block_size, pool=pool)
+    return _simple("tiny", 0, [40, 17, 100, 5], 8, 8, 64, block_size, pool=pool, base=base)
 
 
-def decode_7b(num_seqs=64, block_size=16):
-    rng = np.random.default_rng(BASE_SEED + 1)
+def decode_7b(num_seqs=64, block_size=16, base=BASE_SEED):
+    rng = np.random.default_rng(base + 1)
     lens = rng.integers(50, 901, size=max(64, num_seqs))[:num_seqs]
-    return _simple("7b", 1, lens, 32, 32, 128, block_size)
+    return _simple("7b", 1, lens, 32, 32, 128, block_size, base=base)
 
 
-def gqa(num_seqs=256, block_size=32):
-    rng = np.random.default_rng(BASE_SEED + 3)
+def gqa(num_seqs=256, block_size=32, base=BASE_SEED):
+    rng = np.random.default_rng(base + 3)
     u = rng.uniform(math.log(256), math.log(4097), size=256)[:num_seqs]
     lens = np.clip(np.floor(np.exp(u)).astype(np.int64), 256, 4096)
-    return _simple("gqa", 3, lens, 32, 8, 128, block_size)
+    return _simple("gqa", 3, lens, 32, 8, 128, block_size, base=base)
 
 
-def chat(num_main=128, num_transient=64, block_size=16):
+def chat(num_main=128, num_transient=64, block_size=16, base=BASE_SEED):
     """Arrival-order allocation with interleaved frees (see module docstring).
 
     Step k: (1) main request k (k < num_main) arrives and appends its prompt;
@@ -136,7 +136,7 @@ def chat(num_main=128, num_transient=64, block_size=16):
     released.  Main requests stop after gen - 1 generated tokens; the decode
     step appends the last one.
     """
-    rng = np.random.default_rng(BASE_SEED + 2)
+    rng = np.random.default_rng(base + 2)
     prompt = rng.integers(100, 2001, size=128)[:num_main]
     gen = rng.integers(50, 501, size=128)[:num_main]
     t_prompt = rng.integers(100, 2001, size=64)[:num_transient]
@@ -194,12 +194,12 @@ def chat(num_main=128, num_transient=64, block_size=16):
     pool = math.ceil(1.25 * max(peak_blocks, final_blocks))
     free_order = rng.permutation(pool).astype(np.int32)
     return Workload("chat", 2, 32, 32, 128, block_size, pool, free_order, ops,
-                    batch, lens, 1.0 / math.sqrt(128), BASE_SEED + 2)
+                    batch, lens, 1.0 / math.sqrt(128), base + 2)
 
 
-def prefix(num_seqs=128, prefix_len=500, block_size=16):
+def prefix(num_seqs=128, prefix_len=500, block_size=16, base=BASE_SEED):
     """One prefix forked num_seqs - 1 times, then private suffixes."""
-    rng = np.random.default_rng(BASE_SEED + 4)
+    rng = np.random.default_rng(base + 4)
     suffix = rng.integers(50, 501, size=128)[:num_seqs]
     ops = [("new",), ("append", 0, prefix_len)]
     for _ in range(num_seqs - 1):
@@ -218,10 +218,13 @@ def prefix(num_seqs=128, prefix_len=500, block_size=16):
     free_order = rng.permutation(pool).astype(np.int32)
     return Workload("prefix", 4, 32, 32, 128, block_size, pool, free_order, ops,
                     list(range(num_seqs)), lens, 1.0 / math.sqrt(128),
-                    BASE_SEED + 4, marks)
+                    base + 4, marks)
 
 
 def make(name, **kw):
+    """The named workload; keyword arguments go to its generator (sizes,
+    block_size, and base: the seed its draws derive from, BASE_SEED unless
+    given)."""
     return {"tiny": tiny, "7b": decode_7b, "chat": chat, "gqa": gqa,
             "prefix": prefix}[name](**kw)
 
