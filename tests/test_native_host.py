@@ -3,7 +3,9 @@
 * libpkv.so builds, loads and exports every function include/pkv.h declares;
 * the decode kernel's work split (pkv_schedule.h) passes its exhaustive CPU
   check;
-* host argument validation rejects bad calls before any launch.
+* host argument validation rejects bad calls before any launch;
+* the block manager survives a sanitized fuzz (tests/cpp/test_alloc_fuzz.cpp);
+* the header is plain C99 and usable from C (tests/c/test_header_c99.c).
 """
 
 import os
@@ -76,6 +78,20 @@ def test_alloc_fuzz_sanitized(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "alloc fuzz ok" in r.stdout
+
+
+def test_header_is_c99_and_usable_from_c(lib, tmp_path):
+    """pkv.h compiles as pedantic C99 and a C program drives the block manager
+    (and its checkpoint) through libpkv.so."""
+    from paged_kv_cache_152_gb300 import LIB_PATH
+    libdir = os.path.dirname(LIB_PATH)
+    exe = tmp_path / "test_header_c99"
+    subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c", "test_header_c99.c"),
+                    "-L", libdir, "-lpkv", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c99 header ok" in r.stdout
 
 
 @pytest.fixture
