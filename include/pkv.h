@@ -6,11 +6,21 @@
  *
  *   pkv_paged_attention_decode  single-query decode attention that reads the
  *                               KV cache through per-sequence block tables;
+ *   pkv_paged_attention_decode_append
+ *                               the same, writing each sequence's new token
+ *                               in the same launch;
+ *   pkv_decode_plan_*           a decode call validated once and launched (or
+ *                               run as a whole serving step) many times;
  *   pkv_reshape_and_cache       the slot-mapped write of new tokens' K/V;
  *   pkv_copy_blocks             the whole-block copy behind copy-on-write;
+ *   pkv_swap_blocks             block copies between device and page-locked
+ *                               host pools (swap out / in);
+ *   *_layers                    the cache ops over every layer's pool in one
+ *                               launch;
  *   pkv_alloc_* / pkv_seq_* ... the host block manager that hands out blocks,
  *                               counts references, forks and copies on write,
- *                               and exports the block tables.
+ *                               swaps sequences out and in, exports the block
+ *                               tables, and checkpoints its state.
  *
  * Sources (cited by page title and section):
  *   [P1] "Paged Attention: OS-Inspired Memory Management for KV Caches",
