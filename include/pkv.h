@@ -271,13 +271,22 @@ int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim,
  * Limit: the scratch a call needs is pkv_decode_workspace_size(num_seqs,
  * num_heads, num_kv_heads, head_dim, block_size, num_ctas); a call that needs
  * more than PKV_DECODE_NOALLOC_SCRATCH_BYTES returns PKV_ERR_INVALID_ARG and
- * launches nothing.  (At the default grid of one wave on 152 SMs this allows
- * every supported shape; it bounds how large num_ctas may be.)
+ * launches nothing.  The need grows with num_seqs * num_kv_heads (16 bytes
+ * each) and with the grid.  At the default grid of one CTA per SM on a
+ * 152-SM GB300 the call fits while num_seqs * num_kv_heads is at most:
+ *
+ *                 group 1    group 2    group 4    group 8
+ *   head_dim 64   1,003,408    958,272    867,984    687,408
+ *   head_dim 128    959,632    870,720    692,880    337,200
+ *
+ * (so at num_seqs = 4096, group 8, head_dim 128, num_kv_heads may be at most
+ * 82).  A larger num_ctas leaves less room.
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it; make that
  * first call before any stream capture.  A failed look-up returns
- * PKV_ERR_CUDA.
+ * PKV_ERR_CUDA.  Devices with ordinals 0 to 63 are served; a call with a
+ * higher ordinal current returns PKV_ERR_UNSUPPORTED.
  *
  * Sharing: all calls in the process share the one array, and it keeps what
  * the last call left in it.  Nothing needs clearing between calls: partial

@@ -24,10 +24,11 @@ void *g_scratch_addr[kMaxDevices];
 // Device address of g_decode_scratch on the current device (looked up once).
 int scratch_address(void **out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
+    if (dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;  // a limit of this table, not a CUDA failure
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (g_scratch_addr[dev] == nullptr) {
         void *p = nullptr;
