@@ -97,12 +97,3 @@ def max_abs_err(gpu_out, ref, seqs=None):
     g = gpu_out.float().cpu().numpy().astype(np.float64)
     rows = range(g.shape[0]) if seqs is None else seqs
     return max(float(np.max(np.abs(g[s] - ref[s]))) for s in rows)
-
-
-def sample_seqs(wl, k, seed=0):
-    """k sequences: the shortest, the longest and random others."""
-    lens = np.array(wl.context_lens)
-    rng = np.random.default_rng(seed)
-    pick = {int(lens.argmin()), int(lens.argmax())}
-    pick.update(int(x) for x in rng.choice(len(lens), size=min(k, len(lens)), replace=False))
-    return sorted(pick)[:max(k, 2)]
