@@ -32,6 +32,17 @@ every step (--no-graph: direct binding calls).
 * roofline: the decode launch timed alone with CUDA events on its stream
   over the timed region; algorithmic bytes / mean duration vs the
   measured HBM copy bandwidth.
+* e2e.breakdown: 50 more serving steps with the step's parts issued as
+  separate operations, CUDA events between them and host clocks around them
+  (medians): where the e2e step's time outside the kernel goes.
+* secondary (the default run on one GPU): the headline launch again, 50
+  back-to-back repetitions and 50 with a 256 MB buffer read between
+  repetitions (outside the event pair, so each starts with a cold L2); the
+  chat, gqa and prefix workloads the same way (prefix also against the bytes
+  of the distinct blocks it reaches); identity against shuffled tables (the
+  paging overhead); copy_blocks on the prefix workload's first divergent
+  step (127 copy-on-write pairs) and reshape_and_cache of the 7B-class
+  step's new rows (L2-flushed medians).
 * cpu_baseline: the fp64 oracle on the host cores, on a bounded sample of the
   same workload.
 * --impl reference: the oracle as the reference arm (rank 0 only).
@@ -54,7 +65,7 @@ from workloads import BASE_SEED as W_BASE_SEED  # noqa: E402  (numpy only; torch
 METRIC = "paged decode attention: KV-read HBM GB/s (% of GB300 peak), seqs/s per layer"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_7b_traffic.txt")
+FLUSH_BYTES = 256 << 20  # read between flushed repetitions: twice the 129 MB L2
 KERNEL_SOURCES = ["pkv_decode_impl.cuh", "pkv_decode_inst.cuh", "pkv_decode.cu", "pkv_device.cuh",
                   "pkv_schedule.h", "pkv_decode_params.h"]
 
@@ -86,6 +97,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the secondary measurements (other workloads, identity tables, cache ops, "
+                        "L2-flushed repetitions) that the default run adds to its line")
     p.add_argument("--two-launch", action="store_true",
                    help="reshape_and_cache, then a decode that only reads (instead of the decode launch "
                         "that writes the new tokens itself)")
@@ -174,12 +188,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def traffic_file(workload):
+    return os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+
+
 def recorded_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current kernel source and this workload (else None)."""
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(traffic_file(workload)) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
@@ -330,9 +348,10 @@ def device_step(pkv, st, ws, num_ctas, ev=None):
 
 
 E2E_WARMUP = 20  # untimed serving steps before the timed ones (first-use costs on the host)
+E2E_BREAKDOWN = 50  # untimed steps after them, each part timed on its own
 
 
-def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
+def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_steps=0):
     """Serving-loop steps through the public API with host buffers.
 
     Every step: the C++ block manager appends one token per sequence and
@@ -439,12 +458,217 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0):
     t_end = time.perf_counter()
     elapsed = max_over_ranks(dist, t_end - t0, device)
     barrier(dist, device)
-    plan.close()
     marks.append(t_end)
     per = sorted(b - a for a, b in zip(marks, marks[1:]))
     pct = lambda q: round(per[min(len(per) - 1, int(q * len(per)))] * 1e6, 1)
+    breakdown = e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, st["out"], stream, breakdown_steps)
+    plan.close()
     return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed,
-            "step_us": {"p50": pct(0.5), "p90": pct(0.9), "max": round(per[-1] * 1e6, 1)}}
+            "step_us": {"p50": pct(0.5), "p90": pct(0.9), "max": round(per[-1] * 1e6, 1)},
+            "breakdown": breakdown}
+
+
+def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, steps):
+    """Where an e2e step's time goes: the same serving step with its parts
+    issued as separate operations (the H2D copy of the staging region, the
+    plan's launch, the D2H copy of the output), CUDA events between them,
+    host clocks around the submission, the block manager's work for the next
+    step and the wait.  Untimed for the e2e value; medians in microseconds."""
+    import torch
+    if steps <= 0:
+        return None
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    host = {"submit": [], "block_manager": [], "wait_after_block_manager": [], "step_wall": []}
+    sh = stream.cuda_stream
+    n_rows = len(h_rows)
+    prepare(0)
+    done = torch.cuda.Event()
+    for j in range(steps):
+        i = j % n_rows
+        ta = time.perf_counter()
+        ev[j][0].record(stream)
+        d_stage.copy_(h_rows[i], non_blocking=True)
+        ev[j][1].record(stream)
+        plan.launch_raw(sh)
+        ev[j][2].record(stream)
+        h_out.copy_(d_out, non_blocking=True)
+        ev[j][3].record(stream)
+        done.record(stream)
+        tb = time.perf_counter()
+        if j + 1 < steps:
+            prepare((j + 1) % n_rows)
+        tc = time.perf_counter()
+        while not done.query():
+            pass
+        td = time.perf_counter()
+        host["submit"].append(tb - ta)
+        host["block_manager"].append(tc - tb)
+        host["wait_after_block_manager"].append(td - tc)
+        host["step_wall"].append(td - ta)
+    torch.cuda.synchronize()
+    med = lambda xs: round(statistics.median(xs) * 1e6, 2)  # noqa: E731
+    dev = {"h2d": [e[0].elapsed_time(e[1]) / 1e3 for e in ev], "kernel": [e[1].elapsed_time(e[2]) / 1e3 for e in ev],
+           "d2h": [e[2].elapsed_time(e[3]) / 1e3 for e in ev]}
+    out = {f"device_{k}_us": med(v) for k, v in dev.items()}
+    out.update({f"host_{k}_us": med(v) for k, v in host.items()})
+    gpu = [a + b + c for a, b, c in zip(dev["h2d"], dev["kernel"], dev["d2h"])]
+    out["outside_device_work_us"] = med([w - g for w, g in zip(host["step_wall"], gpu)])
+    out["steps"] = steps
+    out["how"] = ("the parts of the step as separate calls (torch H2D copy of the staging region, the plan's "
+                  "launch, torch D2H copy of the output) with CUDA events between them; host clocks around the "
+                  "submission, the next step's block-manager work and the wait; outside_device_work_us = wall "
+                  "time of the step minus its three device intervals")
+    return out
+
+
+def time_launches(fn, reps, stream, flush=None):
+    """Device time (ms) of each of `reps` calls of fn(), from CUDA events on
+    `stream`.  With `flush` (a buffer larger than L2) the buffer is read
+    between calls, outside the event pair: each call starts with nothing of
+    its inputs in L2 (clean lines only, so no write-back lands in the timed
+    call), and the read also keeps the GPU busy while the host enqueues the
+    call, so no host gap falls between the events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, z in ev:
+        if flush is not None:
+            flush.amax()
+        a.record(stream)
+        fn()
+        z.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(z) for a, z in ev]
+
+
+def unique_kv_bytes(tables, lens, block_size, num_kv_heads, head_dim):
+    """K+V bytes of the distinct physical blocks the tables reach (rows in
+    use only): what a launch must bring from DRAM when blocks shared between
+    sequences are read once."""
+    rows = {}
+    for s, n in enumerate(lens):
+        n = int(n)
+        for i in range(-(-n // block_size)):
+            b = int(tables[s][i])
+            rows[b] = max(rows.get(b, 0), min(block_size, n - i * block_size))
+    return 2 * sum(rows.values()) * num_kv_heads * head_dim * 2
+
+
+def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False):
+    """One workload's decode launch (the fused append + attend of the bench
+    step, through a DecodePlan): back-to-back mean and L2-flushed median."""
+    import torch
+    stream = torch.cuda.current_stream()
+    st = build_state(name, device, identity_tables=identity_tables)
+    wl, t = st["wl"], st["t"]
+    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, 0, device)
+    plan = pkv.DecodePlan(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"], st["lens"],
+                          wl.scale, key=t["key"], value=t["value"], workspace=ws, status=st["status"])
+    for _ in range(5):
+        plan.launch()
+    b2b = time_launches(plan.launch, reps, stream)
+    fl = time_launches(plan.launch, reps, stream, flush)
+    assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
+    kv = wl.kv_read_bytes()
+    mean_us, med_us = statistics.fmean(b2b) * 1e3, statistics.median(fl) * 1e3
+    r = {"decode_us_mean": round(mean_us, 2), "decode_us_median_l2_flushed": round(med_us, 2), "reps": reps,
+         "kv_bytes": kv, "GB_s": round(kv / mean_us / 1e3, 1), "frac": round(kv / mean_us / 1e3 / peak, 4),
+         "GB_s_l2_flushed": round(kv / med_us / 1e3, 1), "frac_l2_flushed": round(kv / med_us / 1e3 / peak, 4),
+         "seqs_per_s": round(wl.num_seqs / mean_us * 1e6, 1),
+         "traffic": None if identity_tables else recorded_traffic(name)}
+    if name == "prefix":
+        u = unique_kv_bytes(st["tables"].cpu().numpy(), wl.context_lens, wl.block_size, wl.num_kv_heads,
+                            wl.head_dim)
+        r["logical"] = "kv_bytes counts every sequence's read of the shared prefix"
+        r["unique_kv_bytes"] = u
+        r["unique_GB_s"] = round(u / mean_us / 1e3, 1)
+        r["unique_frac"] = round(u / mean_us / 1e3 / peak, 4)
+    plan.close()
+    del plan, ws, st, t
+    torch.cuda.empty_cache()
+    return r
+
+
+def measure_cache_ops(pkv, device, peak, reps, flush):
+    """copy_blocks on the prefix workload's first divergent step (the 127
+    copy-on-write copies of the shared tail block) and reshape_and_cache of
+    the 7B-class decode step's 64 new tokens: L2-flushed medians."""
+    import numpy as np
+    import torch
+    import workloads as W
+    stream = torch.cuda.current_stream()
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    wl = W.make("prefix")
+    alloc = pkv.BlockAllocator(wl.num_blocks, wl.block_size, wl.free_order)
+    stop = wl.marks["divergence"]
+    W.replay(alloc, wl.ops, 0, stop)
+    step = [op[1] for op in wl.ops[stop:wl.marks["after_divergence"]]]
+    _, pairs = alloc.append_batch(step)
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    kc = W.normal_fp16_large(shape, wl.seed * 1000 + 4, device)
+    vc = W.normal_fp16_large(shape, wl.seed * 1000 + 5, device)
+    dpairs = torch.from_numpy(pairs.astype(np.int64)).to(device)
+    block_bytes = kc[0].numel() * kc.element_size()
+    moved = 2 * len(pairs) * block_bytes          # per direction (read and written), K and V
+    ms = time_launches(lambda: pkv.copy_blocks(kc, vc, dpairs, status=status), reps, stream, flush)
+    cb_us = statistics.median(ms) * 1e3
+    alloc.close()
+    del kc, vc
+    st = build_state("7b", device)
+    t = st["t"]
+    ms = time_launches(lambda: pkv.reshape_and_cache(t["key"], t["value"], t["key_cache"], t["value_cache"],
+                                                     st["slots"], status=status), reps, stream, flush)
+    rc_us = statistics.median(ms) * 1e3
+    rc_bytes = 2 * 2 * t["key"].numel() * 2      # K and V rows, read once and written once
+    rc_tokens = int(t["key"].shape[0])
+    assert int(status.item()) == 0, pkv.status_string(int(status.item()))
+    del st, t
+    torch.cuda.empty_cache()
+    return {
+        "copy_blocks_prefix_divergence": {
+            "pairs": int(len(pairs)), "block_bytes_per_cache": block_bytes, "bytes_read": moved,
+            "bytes_written": moved, "us_median_l2_flushed": round(cb_us, 2), "reps": reps,
+            "GB_s": round(2 * moved / cb_us / 1e3, 1), "frac": round(2 * moved / cb_us / 1e3 / peak, 4),
+            "note": "read + written bytes over time, like the copy bandwidth it is compared with"},
+        "reshape_and_cache_7b": {
+            "tokens": rc_tokens, "bytes_read_plus_written": rc_bytes, "us_median_l2_flushed": round(rc_us, 2),
+            "reps": reps, "note": "one decode step's new rows: launch-latency bound"},
+    }
+
+
+def run_secondary(pkv, device, peak, st_main, ws_main, reps=50):
+    """The secondary measurements of the default run: the headline launch
+    with L2 flushed between repetitions; chat, gqa and prefix; identity
+    against shuffled tables (the paging overhead); copy_blocks and
+    reshape_and_cache."""
+    import torch
+    stream = torch.cuda.current_stream()
+    flush = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    wl, t = st_main["wl"], st_main["t"]
+    plan = pkv.DecodePlan(st_main["out"], t["query"], t["key_cache"], t["value_cache"], st_main["tables"],
+                          st_main["lens"], wl.scale, key=t["key"], value=t["value"], workspace=ws_main,
+                          status=st_main["status"])
+    b2b = time_launches(plan.launch, reps, stream)
+    fl = time_launches(plan.launch, reps, stream, flush)
+    plan.close()
+    kv = wl.kv_read_bytes()
+    res = {"7b": {"decode_us_mean": round(statistics.fmean(b2b) * 1e3, 2),
+                  "decode_us_median_l2_flushed": round(statistics.median(fl) * 1e3, 2), "reps": reps,
+                  "GB_s_l2_flushed": round(kv / statistics.median(fl) / 1e6, 1),
+                  "frac_l2_flushed": round(kv / statistics.median(fl) / 1e6 / peak, 4)}}
+    for name in ("chat", "gqa", "prefix"):
+        res[name] = measure_decode(pkv, name, device, peak, reps, flush)
+    ident = measure_decode(pkv, "7b", device, peak, reps, flush, identity_tables=True)
+    shuf = res["7b"]["decode_us_mean"]
+    res["paging_overhead_7b"] = {
+        "identity_tables_us_mean": ident["decode_us_mean"], "shuffled_tables_us_mean": shuf,
+        "identity_tables_us_median_l2_flushed": ident["decode_us_median_l2_flushed"],
+        "shuffled_tables_us_median_l2_flushed": res["7b"]["decode_us_median_l2_flushed"],
+        "pct": round(100 * (shuf - ident["decode_us_mean"]) / ident["decode_us_mean"], 2),
+        "note": "shuffled pool vs each sequence's blocks contiguous and in order, same kernel"}
+    res.update(measure_cache_ops(pkv, device, peak, reps, flush))
+    del flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_pkv(args):
@@ -463,7 +687,7 @@ def run_pkv(args):
 
     e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
     st = build_state(args.config, device, args.identity_tables,
-                     e2e_headroom_steps=e2e_steps + E2E_WARMUP if e2e_steps else 0,
+                     e2e_headroom_steps=e2e_steps + E2E_WARMUP + E2E_BREAKDOWN if e2e_steps else 0,
                      block_size=args.block_size, seed=args.seed)
     if not args.two_launch:
         st["fused"] = True
@@ -533,20 +757,26 @@ def run_pkv(args):
 
     e2e = None
     if e2e_steps:
-        e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist, warmup=E2E_WARMUP)
+        e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist, warmup=E2E_WARMUP,
+                      breakdown_steps=E2E_BREAKDOWN)
     clock_info = clocks.finish()
+
+    # the secondary measurements: on the default run of one process only
+    default_launch = not (args.block_size or args.two_launch or args.identity_tables or args.num_ctas
+                          or args.seed not in (None, W_BASE_SEED))
+    secondary = None
+    peak, peak_kind = measured_hbm_peak()
+    if world == 1 and args.config == "7b" and default_launch and not args.no_secondary and not args.no_graph:
+        secondary = run_secondary(pkv, device, peak, st, ws)
 
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return None
 
-    peak, peak_kind = measured_hbm_peak()
     value = world * kv_bytes * args.steps / (ms_total / 1e3) / 1e9
     achieved = kv_bytes / (dec_mean / 1e3) / 1e9
     # the ncu record was taken on the default launch of the default inputs
-    default_launch = not (args.block_size or args.two_launch or args.identity_tables or args.num_ctas
-                          or args.seed not in (None, W_BASE_SEED))
     traffic = recorded_traffic(args.config) if default_launch else None
     line = {
         "metric": METRIC,
@@ -598,12 +828,15 @@ def run_pkv(args):
         line["e2e"] = {"value": round(world * e2e["bytes"] / e2e["elapsed"] / 1e9, 2), "unit": UNIT,
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "steps": e2e_steps, "warmup_steps": E2E_WARMUP, "step_us": e2e["step_us"],
+                       "breakdown": e2e["breakdown"],
                        "includes": "host block manager append + table export into the step's pinned staging "
                                    "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
                                    "per step: H2D copy of the region, the launch (append new tokens + attend), "
                                    "D2H of the output; the host waits for each step (polling an event); the next "
                                    "step's block-manager work "
                                    "overlaps this step's GPU work"}
+    if secondary is not None:
+        line["secondary"] = secondary
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config, args.cpu_seconds, args.seed)
     if dist is not None:

@@ -64,3 +64,17 @@ def test_reference_arm_nonzero_rank_exits_quietly():
                         "--config", "tiny", "--steps", "2", "--warmup", "1"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_unique_kv_bytes_counts_shared_blocks_once():
+    """The prefix workload's DRAM-side byte count: a block two tables share is
+    counted once, with the most rows any sequence reads from it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    # block 5 is shared (full, 16 rows); blocks 7 and 9 are private tails
+    tables = [[5, 7, -1], [5, 9, -1]]
+    lens = [20, 30]                      # 16 + 4 rows, 16 + 14 rows
+    per_row = 2 * 2 * 128 * 2            # K and V, 2 KV heads, head_dim 128, fp16
+    assert bench.unique_kv_bytes(tables, lens, 16, 2, 128) == (16 + 4 + 14) * per_row
+    # without sharing it is the logical count
+    assert bench.unique_kv_bytes([[1, 2], [3, 4]], lens, 16, 2, 128) == (20 + 30) * per_row
