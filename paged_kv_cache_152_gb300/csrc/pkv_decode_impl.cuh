@@ -686,7 +686,6 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     using Smem = DecodeSmem<NW, ST, D, BS, G>;
     extern __shared__ unsigned char smem_raw[];
     __shared__ int warp_sums[32];
-    __shared__ int grand_total;
     // 1024-byte aligned base: the 128-byte swizzle pattern is tied to address bits
     unsigned char *smem =
         smem_raw + ((Smem::kAlign - (smem_addr(smem_raw) & (Smem::kAlign - 1))) & (Smem::kAlign - 1));
@@ -752,7 +751,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         mq.tail = mq.head = 0;
     }
     __syncthreads();
-    if (warp == 0) {
+    {
+        // every warp scans the warps' sums itself (no second barrier)
         const int v = lane < NW ? warp_sums[lane] : 0;
         int vi = v;
 #pragma unroll
@@ -760,17 +760,13 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             const int y = __shfl_up_sync(kFullMask, vi, o);
             if (lane >= o) vi += y;
         }
-        warp_sums[lane] = vi - v;
-        if (lane == 31) grand_total = vi;
-    }
-    __syncthreads();
-    {
-        int run = warp_sums[warp] + incl - local;
+        int run = __shfl_sync(kFullMask, vi - v, warp) + incl - local;
+        const int total = __shfl_sync(kFullMask, vi, 31);
         for (int s = s_lo; s < s_hi; ++s) {
             cum[s] = run;
             run += Hkv * chunks_for(ctx[s], Geo::kRows);
         }
-        if (tid == 0) cum[N] = grand_total;
+        if (tid == 0) cum[N] = total;
     }
     __syncthreads();
 
@@ -867,17 +863,23 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         return chunk_desc_at(g, locate_chunk(cum, N, Hkv, g), tab);
     };
     // windows 0 and 1: each lane locates its two positions in one search and
-    // starts their table loads (window 0's position is kept for its descriptor)
+    // starts their table loads; window 0's descriptors follow as soon as the
+    // entries arrive (the CTA-wide ranges, which only the merges need, come
+    // after the first copies are out)
     int win = 0;
-    ChunkPos q0, q1;
-    int2 tab0 = make_int2(0, 0), tab_nxt = make_int2(0, 0);
-    if (n > 0) {
-        locate_chunk2(cum, N, Hkv, lane < n ? order.at(lane) : gb, 32 + lane < n ? order.at(32 + lane) : gb, q0,
-                      q1);
-        if (lane < n) tab0 = table_entry_at(q0);
-        if (32 + lane < n) tab_nxt = table_entry_at(q1);
+    int4 desc = make_int4(0, 0, 0, 0);  // descriptors of window win
+    int2 tab_nxt = make_int2(0, 0);     // table entries of window win + 1
+    {
+        ChunkPos q0, q1;
+        int2 tab0 = make_int2(0, 0);
+        if (n > 0) {
+            locate_chunk2(cum, N, Hkv, lane < n ? order.at(lane) : gb, 32 + lane < n ? order.at(32 + lane) : gb,
+                          q0, q1);
+            if (lane < n) tab0 = table_entry_at(q0);
+            if (32 + lane < n) tab_nxt = table_entry_at(q1);
+        }
+        if (lane < n) desc = chunk_desc_at(order.at(lane), q0, tab0);
     }
-    int4 desc;  // descriptors of window win (window 0's are built below)
 
     unsigned char *wst = smem + (size_t)warp * ST * Geo::kStageBytes;
     const uint32_t wst_a = smem_addr(wst);
@@ -946,23 +948,22 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     };
 
     int issued = 0;
-    // the CTA-wide ranges (needed only by the merges)
-    for (int c = tid; c <= C; c += NW * 32)
-        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
-    // window 0's descriptors (the table entries have arrived meanwhile)
-    desc = lane < n ? chunk_desc_at(order.at(lane), q0, tab0) : make_int4(0, 0, 0, 0);
-    __syncthreads();
 
     // ---- from here on the kernel reads and writes what the preceding kernel
     // may write: the caches, the workspace, the output ----
     grid_dependency_wait();
     launch_dependents();
-    for (; issued < min(ST, n); ++issued) issue(issued);
     // this call counts on the counters of its epoch's parity, and prepares the
     // other parity's counters for the next call (the epoch only changes when
-    // every CTA of a call is out, so every warp of this call reads the same)
+    // every CTA of a call is out, so every warp of this call reads the same);
+    // the load goes out before the first copies, its value is used after them
     uint32_t epoch = 0;
     if (lane == 0) epoch = (uint32_t)__ldcg(p.ws_sync);
+    for (; issued < min(ST, n); ++issued) issue(issued);
+    // the CTA-wide ranges (needed only by the merges)
+    for (int c = tid; c <= C; c += NW * 32)
+        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+    __syncthreads();  // the ranges are visible to every warp's merges
     epoch = __shfl_sync(kFullMask, epoch, 0);
     const int parity = epoch & 1;
     unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;

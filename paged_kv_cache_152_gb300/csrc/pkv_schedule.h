@@ -41,6 +41,13 @@ enum ChunkFlags {
     kAppendRow = 16  // (set by the kernel) the chunk's last row is the decode step's new token
 };
 
+// a / b for 0 <= a, 0 < b: a 32-bit unsigned division when both fit (the
+// usual case; a 64-bit division is a long instruction sequence on the GPU).
+PKV_HD int64_t div_nonneg(int64_t a, int64_t b) {
+    if (((uint64_t)a | (uint64_t)b) >> 32 == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 PKV_HD int chunks_for(int ctx, int rows_per_chunk) {
     return ctx <= 0 ? 0 : (ctx + rows_per_chunk - 1) / rows_per_chunk;
 }
@@ -76,9 +83,9 @@ struct ChunkPos {
 PKV_HD ChunkPos locate_chunk(const int *cum, int n, int num_kv_heads, int64_t g) {
     ChunkPos p;
     p.s = find_seq(cum, n, g);
-    p.nch = (cum[p.s + 1] - cum[p.s]) / num_kv_heads;
+    p.nch = (int)((unsigned)(cum[p.s + 1] - cum[p.s]) / (unsigned)num_kv_heads);
     const int off = (int)(g - cum[p.s]);
-    p.kvh = off / p.nch;
+    p.kvh = (int)((unsigned)off / (unsigned)p.nch);
     p.c = off - p.kvh * p.nch;
     return p;
 }
@@ -97,11 +104,11 @@ PKV_HD void locate_chunk2(const int *cum, int n, int num_kv_heads, int64_t g0, i
     }
     p0.s = lo0;
     p1.s = lo1;
-    p0.nch = (cum[lo0 + 1] - cum[lo0]) / num_kv_heads;
-    p1.nch = (cum[lo1 + 1] - cum[lo1]) / num_kv_heads;
+    p0.nch = (int)((unsigned)(cum[lo0 + 1] - cum[lo0]) / (unsigned)num_kv_heads);
+    p1.nch = (int)((unsigned)(cum[lo1 + 1] - cum[lo1]) / (unsigned)num_kv_heads);
     const int off0 = (int)(g0 - cum[lo0]), off1 = (int)(g1 - cum[lo1]);
-    p0.kvh = off0 / p0.nch;
-    p1.kvh = off1 / p1.nch;
+    p0.kvh = (int)((unsigned)off0 / (unsigned)p0.nch);
+    p1.kvh = (int)((unsigned)off1 / (unsigned)p1.nch);
     p0.c = off0 - p0.kvh * p0.nch;
     p1.c = off1 - p1.kvh * p1.nch;
 }
@@ -113,7 +120,7 @@ PKV_HD void next_chunk(ChunkPos &p, const int *cum, int n, int num_kv_heads) {
     if (++p.kvh < num_kv_heads) return;
     p.kvh = 0;
     do { ++p.s; } while (p.s < n - 1 && cum[p.s + 1] == cum[p.s]);
-    p.nch = (cum[p.s + 1] - cum[p.s]) / num_kv_heads;
+    p.nch = (int)((unsigned)(cum[p.s + 1] - cum[p.s]) / (unsigned)num_kv_heads);
 }
 
 // Flags of chunk g (at position p) for the worker owning [gb, ge).
@@ -146,12 +153,13 @@ PKV_HD int partial_slot(int64_t st, int64_t g0) {
 PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_t c, int64_t C, int64_t T,
                                  int64_t snap_cap, bool *cuts = nullptr) {
     if (cuts) *cuts = false;
-    const int64_t nominal = (c * T) / C;
+    const int64_t nominal = div_nonneg(c * T, C);
     if (c == 0 || nominal >= T) return nominal >= T ? T : 0;
     const ChunkPos p = locate_chunk(cum, n, num_kv_heads, nominal);
     const int64_t g0 = nominal - p.c;          // segment's first chunk
     const int64_t g1 = g0 + p.nch;             // one past its last
-    const int64_t snap = T / (4 * C) < snap_cap ? T / (4 * C) : snap_cap;
+    const int64_t quarter = div_nonneg(T, 4 * C);
+    const int64_t snap = quarter < snap_cap ? quarter : snap_cap;
     const int64_t left = nominal - g0, right = g1 - nominal;
     if (left == 0) return nominal;
     if (left <= right && left <= snap) return g0;
