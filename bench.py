@@ -25,7 +25,9 @@ every step (--no-graph: direct binding calls).
   the C++ block manager appends one token per sequence and exports the tables
   into the step's pinned staging region (with its queries and new K/V rows);
   one pkv_decode_plan_step call copies the region host->device, appends the
-  new tokens and attends, and copies the output device->host; the host waits
+  new tokens and attends, the kernel writing the output straight into a
+  pinned host buffer over the CPU-GPU link (--e2e-copy-out: a device->host
+  copy after the launch instead); the host waits
   for the step (polling an event); the next step's block-manager work
   overlaps the GPU's work on this step.  20 untimed warm-up steps first; the
   line also gives the per-step wall-time percentiles.
@@ -96,6 +98,9 @@ def parse_args(argv=None):
                    help="override the workload's block size (8, 16, 32, 64, 128): the block-size sweep")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-copy-out", action="store_true",
+                   help="e2e: the kernel writes device memory and a D2H copy brings the output back (default: "
+                        "the kernel writes the pinned host buffer directly)")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the secondary measurements (other workloads, identity tables, cache ops, "
@@ -351,7 +356,7 @@ E2E_WARMUP = 20  # untimed serving steps before the timed ones (first-use costs 
 E2E_BREAKDOWN = 50  # untimed steps after them, each part timed on its own
 
 
-def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_steps=0):
+def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_steps=0, copy_out=False):
     """Serving-loop steps through the public API with host buffers.
 
     Every step: the C++ block manager appends one token per sequence and
@@ -359,8 +364,9 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     staging region, which also holds the step's queries and new K/V rows;
     copy-on-write pairs (if any) go through copy_blocks; then ONE library call
     (pkv_decode_plan_step of a DecodePlan built once: append the new tokens +
-    attend) copies the region host->device, launches the step and copies the
-    output device->host; the stream is synchronised.  The
+    attend) copies the region host->device and launches the step, whose
+    kernel writes the output into pinned host memory (copy_out: a D2H copy
+    follows); the stream is synchronised.  The
     block-manager work of step i+1 runs on the host while the GPU runs step
     i (as a serving loop schedules ahead)."""
     import numpy as np
@@ -398,16 +404,20 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     d_tables = dview("tables", torch.int32, (n, mb))
     d_lens = dview("lens", torch.int32, (n,))
     t = st["t"]
-    plan = pkv.DecodePlan(st["out"], d_q, t["key_cache"], t["value_cache"], d_tables, d_lens, wl.scale,
+    h_out = torch.empty((n, h, d), dtype=torch.float16).pin_memory()
+    # by default the kernel writes the output straight into the pinned host
+    # buffer (over the CPU-GPU link, as rows become final); copy_out: it writes
+    # device memory and a D2H copy follows the launch
+    plan = pkv.DecodePlan(st["out"] if copy_out else h_out, d_q, t["key_cache"], t["value_cache"], d_tables,
+                          d_lens, wl.scale,
                           key=d_k, value=d_v, num_ctas=num_ctas, workspace=ws, status=st["status"])
     h_slots = np.empty(n, dtype=np.int64)
     h_pairs_t = torch.empty((n, 2), dtype=torch.int64).pin_memory()
     h_pairs32 = np.empty((n, 2), dtype=np.int32)
     d_pairs = torch.empty((n, 2), dtype=torch.int64, device=device)
-    h_out = torch.empty((n, h, d), dtype=torch.float16).pin_memory()
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    d_stage_ptr, h_out_ptr = d_stage.data_ptr(), h_out.data_ptr()
+    d_stage_ptr, h_out_ptr = d_stage.data_ptr(), (h_out.data_ptr() if copy_out else None)
     h_row_ptrs = [r.data_ptr() for r in h_rows]
     done = torch.cuda.Event()
     batch = np.asarray(wl.batch, dtype=np.int32)
@@ -461,7 +471,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     marks.append(t_end)
     per = sorted(b - a for a, b in zip(marks, marks[1:]))
     pct = lambda q: round(per[min(len(per) - 1, int(q * len(per)))] * 1e6, 1)
-    breakdown = e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, st["out"], stream, breakdown_steps)
+    breakdown = e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out if copy_out else None, st["out"],
+                              stream, breakdown_steps)
     plan.close()
     return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed,
             "step_us": {"p50": pct(0.5), "p90": pct(0.9), "max": round(per[-1] * 1e6, 1)},
@@ -491,7 +502,8 @@ def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, s
         ev[j][1].record(stream)
         plan.launch_raw(sh)
         ev[j][2].record(stream)
-        h_out.copy_(d_out, non_blocking=True)
+        if h_out is not None:  # (else the kernel has written the host buffer itself)
+            h_out.copy_(d_out, non_blocking=True)
         ev[j][3].record(stream)
         done.record(stream)
         tb = time.perf_counter()
@@ -515,7 +527,8 @@ def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, s
     out["outside_device_work_us"] = med([w - g for w, g in zip(host["step_wall"], gpu)])
     out["steps"] = steps
     out["how"] = ("the parts of the step as separate calls (torch H2D copy of the staging region, the plan's "
-                  "launch, torch D2H copy of the output) with CUDA events between them; host clocks around the "
+                  "launch, and a torch D2H copy of the output only when the kernel does not write the host "
+                  "buffer itself) with CUDA events between them; host clocks around the "
                   "submission, the next step's block-manager work and the wait; outside_device_work_us = wall "
                   "time of the step minus its three device intervals")
     return out
@@ -685,7 +698,9 @@ def run_pkv(args):
     barrier(dist, device)
     pkv.load()
 
-    e2e_steps = 0 if args.no_e2e else max(1, min(args.e2e_steps, args.steps))
+    # the e2e loop runs its own step count (a step is ~0.1 ms; a short run is at
+    # the mercy of one slow host wake-up)
+    e2e_steps = 0 if args.no_e2e else max(1, args.e2e_steps)
     st = build_state(args.config, device, args.identity_tables,
                      e2e_headroom_steps=e2e_steps + E2E_WARMUP + E2E_BREAKDOWN if e2e_steps else 0,
                      block_size=args.block_size, seed=args.seed)
@@ -758,7 +773,7 @@ def run_pkv(args):
     e2e = None
     if e2e_steps:
         e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist, warmup=E2E_WARMUP,
-                      breakdown_steps=E2E_BREAKDOWN)
+                      breakdown_steps=E2E_BREAKDOWN, copy_out=args.e2e_copy_out)
     clock_info = clocks.finish()
 
     # the secondary measurements: on the default run of one process only
@@ -829,12 +844,14 @@ def run_pkv(args):
                        "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                        "steps": e2e_steps, "warmup_steps": E2E_WARMUP, "step_us": e2e["step_us"],
                        "breakdown": e2e["breakdown"],
+                       "output": ("D2H copy after the launch" if args.e2e_copy_out else
+                                  "written by the kernel straight into the pinned host buffer over the CPU-GPU "
+                                  "link (the plan's out is mapped host memory); no copy after the launch"),
                        "includes": "host block manager append + table export into the step's pinned staging "
                                    "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
                                    "per step: H2D copy of the region, the launch (append new tokens + attend), "
-                                   "D2H of the output; the host waits for each step (polling an event); the next "
-                                   "step's block-manager work "
-                                   "overlaps this step's GPU work"}
+                                   "the output into host memory; the host waits for each step (polling an event); "
+                                   "the next step's block-manager work overlaps this step's GPU work"}
     if secondary is not None:
         line["secondary"] = secondary
     if not args.no_cpu:

@@ -210,6 +210,18 @@ int pkv_paged_attention_decode_append(void *out, const void *query,
  * must not be moved or freed while it is in use.  A plan is read-only after
  * creation (launches from several host threads are fine; on one workspace
  * they must be stream-ordered, as for the direct calls).
+ *
+ * A plan's out may also be page-locked host memory mapped into the device's
+ * address space (cudaHostAlloc / cudaMallocHost memory on a system with
+ * unified addressing, or memory registered with cudaHostRegisterMapped).
+ * The kernel then writes each output row over the CPU-GPU link as soon as it
+ * is final, so a serving step needs no copy of the output back
+ * (pkv_decode_plan_step with host_out == NULL); the host reads out once the
+ * stream has passed the launch.  pkv_decode_plan_create checks where out
+ * lives (cudaPointerGetAttributes): device memory of the current device,
+ * managed memory or mapped host memory; anything else (pageable host memory,
+ * another device's memory) is PKV_ERR_INVALID_ARG, a failed query
+ * PKV_ERR_CUDA.  The direct calls take device or managed memory only.
  */
 typedef struct pkv_decode_plan pkv_decode_plan_t;
 int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,

@@ -344,18 +344,26 @@ class DecodePlan:
     With key/value given, each launch appends the new tokens and attends
     (paged_attention_decode_append); without, it only attends.  The plan keeps
     references to every tensor it was built from, and launch() and step() run
-    on their device; launch_raw() and step_raw() expect it to be current."""
+    on their device; launch_raw() and step_raw() expect it to be current.
+
+    out may also be a pinned (page-locked) host tensor: the kernel then writes
+    the output over the CPU-GPU link as rows become final, and a serving step
+    needs no copy back (step() without host_out); read it once the stream has
+    passed the launch."""
 
     def __init__(self, out, query, key_cache, value_cache, block_tables, context_lens, scale, key=None,
                  value=None, num_ctas=0, workspace=None, status=None):
         import torch
         if (key is None) != (value is None):
             raise ValueError("key and value go together")
-        specs = [(query, torch.float16, "query", 3), (out, torch.float16, "out", 3),
+        specs = [(query, torch.float16, "query", 3),
                  (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
                  (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1)]
         if key is not None:
             specs += [(key, torch.float16, "key", 3), (value, torch.float16, "value", 3)]
+        _need(out, torch.float16, "out", 3, device=False)
+        if out.device.type != "cuda" and not out.is_pinned():
+            raise ValueError("out must be a CUDA tensor or a pinned host tensor")
         _need_all(*specs)
         n, h, d = query.shape
         nb, hkv, bs, d2 = key_cache.shape

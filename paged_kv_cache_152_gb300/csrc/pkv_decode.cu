@@ -336,6 +336,37 @@ extern "C" int pkv_paged_attention_decode_append(void *out, const void *query, c
                        num_ctas, workspace, workspace_bytes, dev_status, stream);
 }
 
+namespace {
+
+// Where a plan's kernel writes its output: device memory of the current
+// device, managed memory, or page-locked host memory mapped into the
+// device's address space (then through its device address: the output goes
+// straight over the CPU-GPU link as segments finish, and a serving step
+// needs no copy back).  Pageable host memory and other devices' memory are
+// refused.
+int plan_output(void *out, pkv_decode_plan *plan) {
+    cudaPointerAttributes attr;
+    int dev = -1;
+    if (cudaPointerGetAttributes(&attr, out) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+            return attr.device == dev ? PKV_OK : PKV_ERR_INVALID_ARG;
+        case cudaMemoryTypeManaged:
+            return PKV_OK;
+        case cudaMemoryTypeHost:
+            if (attr.devicePointer == nullptr || !aligned16(attr.devicePointer)) return PKV_ERR_INVALID_ARG;
+            plan->params.out = static_cast<__half *>(attr.devicePointer);
+            return PKV_OK;
+        default:
+            return PKV_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
 extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,
                                       void *key_cache, void *value_cache, const int32_t *block_tables,
                                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
@@ -347,9 +378,10 @@ extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *
     if ((key == nullptr) != (value == nullptr)) return PKV_ERR_INVALID_ARG;
     pkv_decode_plan *plan = new (std::nothrow) pkv_decode_plan;
     if (!plan) return PKV_ERR_INVALID_ARG;
-    const int rc = build_plan(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                              context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                              scale, num_ctas, workspace, workspace_bytes, dev_status, plan);
+    int rc = build_plan(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        num_ctas, workspace, workspace_bytes, dev_status, plan);
+    if (rc == PKV_OK && !plan->empty) rc = plan_output(out, plan);
     if (rc != PKV_OK) {
         delete plan;
         return rc;

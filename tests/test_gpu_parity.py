@@ -533,6 +533,47 @@ def test_decode_plan_step_stages_inputs_and_output(pkv):
     plan.close()
 
 
+def test_decode_plan_writes_mapped_host_output(pkv):
+    """A plan whose out is pinned host memory: the kernel writes the output
+    over the CPU-GPU link, with the bits of the device-output plan; host
+    memory the device cannot reach (pageable) is refused before any launch."""
+    import ctypes
+    wl = W.make("7b", num_seqs=11)
+    dev_case, host_case = Case(wl), Case(wl)
+    host_out = torch.full(tuple(dev_case.out.shape), float("nan"), dtype=torch.float16).pin_memory()
+    plans = []
+    for case, out in ((dev_case, dev_case.out), (host_case, host_out)):
+        plans.append(pkv.DecodePlan(out, case.t["query"], case.t["key_cache"], case.t["value_cache"], case.tables,
+                                    case.lens, wl.scale, key=case.t["key"], value=case.t["value"],
+                                    status=case.status))
+    for step in range(3):
+        for pl in plans:
+            pl.launch()
+        torch.cuda.synchronize()
+        assert int(dev_case.status.item()) == 0 and int(host_case.status.item()) == 0
+        assert torch.equal(host_out.view(torch.int16), dev_case.out.cpu().view(torch.int16))
+        assert torch.equal(host_case.t["key_cache"].view(torch.int16), dev_case.t["key_cache"].view(torch.int16))
+    for pl in plans:
+        pl.close()
+    host_case.oracle_write_new_tokens()
+    assert max_abs_err(host_out, host_case.oracle_decode()) <= TOL
+    # pageable host memory: refused by the library's pointer check
+    pageable = np.zeros(host_out.numel(), dtype=np.float16)
+    t = host_case.t
+    h = ctypes.c_void_p()
+    p = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, 0)
+    rc = pkv.load().pkv_decode_plan_create(
+        ctypes.c_void_p(pageable.ctypes.data), p(t["query"]), None, None, p(t["key_cache"]), p(t["value_cache"]),
+        p(host_case.tables), host_case.tables.shape[1], p(host_case.lens), wl.num_seqs, wl.num_heads,
+        wl.num_kv_heads, wl.head_dim, wl.block_size, t["key_cache"].shape[0], ctypes.c_float(wl.scale), 0, p(ws),
+        ws.numel(), None, ctypes.byref(h))
+    assert rc == pkv.PKV_ERR_INVALID_ARG and h.value is None
+    with pytest.raises(ValueError):
+        pkv.DecodePlan(torch.empty_like(host_out), t["query"], t["key_cache"], t["value_cache"], host_case.tables,
+                       host_case.lens, wl.scale)
+
+
 @pytest.mark.parametrize("d,h,hkv,bs,lens", [
     (128, 4, 4, 16, [16384]),           # group 1: 1,024-chunk segments over many CTAs, partials in shared memory
     (128, 16, 4, 32, [9000, 40, 5000]),  # group 4
