@@ -40,10 +40,10 @@ def _sources():
     return cu, cpp, deps
 
 
-def _stale(deps):
-    if not os.path.exists(LIB):
+def _stale(deps, lib=LIB):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in deps)
 
 
@@ -57,16 +57,19 @@ def _run(cmd):
 def build(force=False, verbose=False, ptxas_verbose=False, defines=(), lib_path=None):
     """Compile and link libpkv.so if any source changed; returns its path.
 
-    defines (e.g. ["PKV_DECODE_WARPS=8"]) and lib_path build a variant into
-    another file (with its own object directory) for tuning experiments.
+    defines (e.g. ["PKV_DECODE_G1_CUDACORE=1"]) and lib_path build a variant
+    into another file (with its own object directory); a variant is rebuilt
+    when a source is newer than it (its defines are the caller's to keep
+    apart, one path per variant).
     """
     lib, obj_dir = LIB, OBJ
     if lib_path is not None:
         lib, obj_dir = os.path.abspath(lib_path), os.path.abspath(lib_path) + ".obj"
     cu, cpp, deps = _sources()
-    if not force and lib_path is None and not _stale(deps):
+    if not force and not _stale(deps, lib):
         return lib
     os.makedirs(obj_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC] + [f"-D{d}" for d in defines]
     jobs = []

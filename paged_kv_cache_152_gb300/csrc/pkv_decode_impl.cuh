@@ -252,6 +252,105 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     }
 }
 
+// ---- the CUDA-core form of one chunk, group 1 only (built with
+// PKV_DECODE_G1_CUDACORE=1; the tensor-core form above is the default) ----
+// Lane (h, r) = (lane >> 4, lane & 15) owns row r of the chunk and the dims
+// [h * D/2, (h + 1) * D/2) of the one query head: q . K_r over its dims is
+// D/2 fp32 FMAs, one shuffle adds the two halves, the online softmax takes
+// 8 more, and o keeps that lane's row's share of P.V for its dims (summed
+// over the 16 rows only when the piece ends, in finish_piece_cc).
+template <int D>
+struct CudaCoreLayout {
+    static constexpr int kDH = D / 2;     // dims per lane
+    static constexpr int kNV = kDH / 8;   // 16-byte vectors per lane and row
+    // byte offset, in a swizzled [half][row][64 dims] tile, of vector v of
+    // the lane's row and dims
+    __device__ __forceinline__ static int off(int lane, int v) {
+        const int r = lane & 15, h = lane >> 4;
+        if (D == 128) return h * DecodeGeometry<128, 16, 1>::kHalfBytes + r * 128 + ((v ^ (r & 7)) << 4);
+        return r * 128 + (((h * 4 + v) ^ (r & 7)) << 4);
+    }
+};
+
+template <int D>
+__device__ __forceinline__ void consume_chunk_cc(const unsigned char *kt, const unsigned char *vt, int R,
+                                                 const float (&q)[D / 2], float scale_log2, float &m, float &l,
+                                                 float (&o)[D / 2], int lane) {
+    using L = CudaCoreLayout<D>;
+    const int r = lane & 15;
+    float s0 = 0.f, s1 = 0.f;  // two chains
+#pragma unroll
+    for (int v = 0; v < L::kNV; ++v) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(kt + L::off(lane, v)), f);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            s0 = fmaf(q[8 * v + e], f[e], s0);
+            s1 = fmaf(q[8 * v + e + 1], f[e + 1], s1);
+        }
+    }
+    float sc = s0 + s1;
+    sc += __shfl_xor_sync(kFullMask, sc, 16);
+    const float x = r < R ? sc * scale_log2 : -CUDART_INF_F;  // rows past R: masked (their K may be anything)
+    float mx = x;
+#pragma unroll
+    for (int k = 1; k < 16; k <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, k));
+    const float mn = fmaxf(m, mx);  // row 0 is valid: finite
+    const float corr = exp2f(m - mn);
+    m = mn;
+    const float pr = exp2f(x - mn);
+    float ps = pr;
+#pragma unroll
+    for (int k = 1; k < 16; k <<= 1) ps += __shfl_xor_sync(kFullMask, ps, k);
+    l = l * corr + ps;
+    if (corr != 1.f) {  // the same on every lane
+#pragma unroll
+        for (int j = 0; j < D / 2; ++j) o[j] *= corr;
+    }
+#pragma unroll
+    for (int v = 0; v < L::kNV; ++v) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(vt + L::off(lane, v)), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[8 * v + e] = fmaf(pr, f[e], o[8 * v + e]);
+    }
+}
+
+// The query dims of lane (h, r) as fp32, from the group's query row in the
+// stage's slot (plain [D] fp16).
+template <int D>
+__device__ __forceinline__ void load_query_cc(const unsigned char *sq, float (&q)[D / 2], int lane) {
+    const int h = lane >> 4;
+#pragma unroll
+    for (int v = 0; v < D / 16; ++v) {
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sq + (h * (D / 2) + 8 * v) * 2), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q[8 * v + e] = f[e];
+    }
+}
+
+// Sums o over the 16 lanes that share h (rows 0..15): afterwards lane L holds
+// the piece's output dims [L * D/32, (L + 1) * D/32) (halving exchanges: at
+// each step a lane keeps the half of its values that its bit selects and
+// adds its partner's copy of that half).
+template <int D>
+__device__ __forceinline__ void reduce_rows_cc(float (&o)[D / 2], int lane) {
+    constexpr int N0 = D / 2;
+#pragma unroll
+    for (int step = 0; step < 4; ++step) {
+        const int bit = 8 >> step;           // lane mask of this step
+        const int n = N0 >> (step + 1);      // values kept after it
+        const bool upper = (lane & bit) != 0;
+#pragma unroll
+        for (int j = 0; j < n; ++j) {
+            const float keep = upper ? o[n + j] : o[j];
+            const float send = upper ? o[j] : o[n + j];
+            o[j] = keep + __shfl_xor_sync(kFullMask, send, bit);
+        }
+    }
+}
+
 // Completion counters hold (epoch << 32 | count).  Every call prepares the
 // counters of the NEXT call (the other parity) as (epoch + 1, 0), so counting
 // in is normally a single atomic add.  A counter in any other state (a fresh
@@ -557,6 +656,36 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
     return true;
 }
 
+// finish_piece for the CUDA-core form (group 1): the rows are summed first
+// (reduce_rows_cc), then lane L writes its D/32 dims of the output row or of
+// the partial; l and m are the same on every lane.
+template <int D, int NW>
+__device__ __forceinline__ bool finish_piece_cc(const DecodeParams &p, const WorkerCtx<NW> &wc, const int4 md,
+                                                float m, float l, float (&o)[D / 2], SegInfo &si, int lane) {
+    constexpr int PER = D / 32;
+    reduce_rows_cc<D>(o, lane);
+    const int s = md.x, kvh = md.y, flags = md.w;
+    if (flags & kWhole) {
+        const float inv = 1.f / l;
+        __half *dst = p.out + ((int64_t)s * p.num_heads + kvh) * D + lane * PER;
+        if (PER == 4) {
+            uint2 w;
+            w.x = pack_half2(o[0] * inv, o[1] * inv);
+            w.y = pack_half2(o[2] * inv, o[3] * inv);
+            *reinterpret_cast<uint2 *>(dst) = w;
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_half2(o[0] * inv, o[1] * inv);
+        }
+        return false;
+    }
+    si = segment_info(p, wc, s, kvh);
+    const PieceRef at = worker_piece<D, 1, NW>(p, wc, wc.wid, (flags & kSlot1) ? 1 : 0);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) at.acc[lane * PER + k] = o[k];
+    if (lane == 0) reinterpret_cast<float2 *>(at.ml)[0] = make_float2(m, l);
+    return true;
+}
+
 // Counts a stored partial of segment (s, kvh) in, in two levels.
 //  1. The pieces in this CTA's range (the whole segment, if it stays in the
 //     CTA) count their chunks in on a shared-memory counter (count_piece);
@@ -681,6 +810,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     constexpr int kReliefDiv = PKV_DECODE_RELIEF_DIV;
 #else
     constexpr int kReliefDiv = 16;  // ... at most 1/16 of a nominal share
+#endif
+#ifdef PKV_DECODE_G1_CUDACORE
+    constexpr bool kCudaCore = PKV_DECODE_G1_CUDACORE != 0 && G == 1;
+#else
+    constexpr bool kCudaCore = false;  // group 1 on the tensor cores too (see consume_chunk_cc)
 #endif
     using Geo = DecodeGeometry<D, BS, G>;
     using Smem = DecodeSmem<NW, ST, D, BS, G>;
@@ -1060,6 +1194,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     for (int kk = 0; kk < D / 16; ++kk) qa[kk][0] = qa[kk][1] = 0u;
 #pragma unroll
     for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    // the CUDA-core form (group 1, opt-in build): the lane's query dims and
+    // its row's share of the output (consume_chunk_cc)
+    float qc[kCudaCore ? D / 2 : 1], oc[kCudaCore ? D / 2 : 1];
+#pragma unroll
+    for (int j = 0; j < (kCudaCore ? D / 2 : 1); ++j) qc[j] = oc[j] = 0.f;
 
     for (int i = 0; i < n; ++i) {
         const int stage = i % ST;
@@ -1076,18 +1215,25 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         }
         const int4 md = wmeta[2 * stage];
         if (md.w & kFirst) {
-            // query rows of the group as mma A fragments (rows g >= G stay 0)
             const unsigned char *sq = wq + stage * Geo::kSlotBytes;
+            if constexpr (kCudaCore) {
+                load_query_cc<D>(sq, qc, lane);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                qa[kk][0] = gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
-                qa[kk][1] =
-                    gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 8 + 2 * tq) * 2) : 0u;
+                for (int j = 0; j < D / 2; ++j) oc[j] = 0.f;
+            } else {
+                // query rows of the group as mma A fragments (rows g >= G stay 0)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    qa[kk][0] =
+                        gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
+                    qa[kk][1] =
+                        gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 8 + 2 * tq) * 2) : 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             }
             m = -CUDART_INF_F;
             l = 0.f;
-#pragma unroll
-            for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
         }
         if (md.z < Geo::kRows) zero_tail_rows<D, BS, G>(wst + stage * Geo::kStageBytes + Geo::kTileBytes, md.z, lane);
         if (md.w & kAppendRow) {
@@ -1116,13 +1262,24 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         // no fence: every ldmatrix has delivered before the mma that uses it.
         if (md.z < Geo::kRows || (md.w & kAppendRow)) fence_proxy_async_smem();
         const uint32_t kt = wst_a + stage * Geo::kStageBytes;
-        consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
+        if constexpr (kCudaCore)
+            consume_chunk_cc<D>(wst + stage * Geo::kStageBytes, wst + stage * Geo::kStageBytes + Geo::kTileBytes,
+                                md.z, qc, p.scale_log2, m, l, oc, lane);
+        else
+            consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
         // refill the stage first: a piece's finish (and a cut piece's count and
         // merge) then overlaps the copies in flight instead of draining the ring
         __syncwarp();
         if (issued < n) issue(issued++);
         SegInfo si;
-        if ((md.w & kLast) && finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane) &&
+        bool stored = false;
+        if (md.w & kLast) {
+            if constexpr (kCudaCore)
+                stored = finish_piece_cc<D, NW>(p, wc, md, m, l, oc, si, lane);
+            else
+                stored = finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane);
+        }
+        if (stored &&
             count_piece<D, G, NW>(wc, si, lane)) {
             // with long shares the merge goes to a warp that is done with its
             // own (the merging warp would otherwise end late); with short ones
