@@ -251,6 +251,58 @@ int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void
                          void *host_out, pkv_stream_t stream);
 void pkv_decode_plan_destroy(pkv_decode_plan_t *plan);
 
+/*
+ * Decode attention with prefix sharing.
+ *
+ * [P1] "Memory sharing across requests" and [P2] "How PagedAttention works"
+ * (prefix sharing): sequences forked from one prompt read the same physical
+ * blocks for it.  These calls compute exactly what
+ * pkv_paged_attention_decode_append (key/value non-NULL) or
+ * pkv_paged_attention_decode (both NULL) compute, and take one more input:
+ *
+ *   shared_blocks  int32 [num_seqs] (device): for s >= 1, how many leading
+ *                  logical blocks sequence s has in common with sequence
+ *                  s - 1 (same physical block at the same logical index);
+ *                  entry 0 is ignored.  pkv_export_shared_prefix computes it.
+ *                  It must not claim more than the tables hold in common
+ *                  (the shared blocks are read through the first sequence's
+ *                  table); smaller values are always correct, and all zeros
+ *                  is the plain decode.
+ *
+ * Up to 8 consecutive sequences that share blocks form a group; the group's
+ * shared full blocks (never the block of a member's last token) are read
+ * once for all of them, with the members' queries as the rows of one
+ * tensor-core tile, and each member's remaining blocks on its own.  The two
+ * parts of a member's row are merged in a fixed order, so results are
+ * run-to-run deterministic for a fixed grid; they agree with the plain decode
+ * within rounding (not bit for bit).  The grouped kernel serves group 1
+ * (num_heads == num_kv_heads), block sizes 16 to 128 and up to 1024
+ * sequences; other calls run the plain kernel (shared_blocks is then not
+ * read).  The workspace is pkv_decode_workspace_size_shared(...) bytes, and
+ * otherwise follows the rules of pkv_paged_attention_decode.  A NULL
+ * shared_blocks with num_seqs > 0 is PKV_ERR_INVALID_ARG.
+ */
+int pkv_paged_attention_decode_shared(void *out, const void *query, const void *key,
+                                      const void *value, void *key_cache, void *value_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, const int32_t *shared_blocks,
+                                      int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks,
+                                      float scale, int num_ctas,
+                                      void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, pkv_stream_t stream);
+int pkv_decode_plan_create_shared(void *out, const void *query, const void *key, const void *value,
+                                  void *key_cache, void *value_cache,
+                                  const int32_t *block_tables, int max_blocks_per_seq,
+                                  const int32_t *context_lens, const int32_t *shared_blocks,
+                                  int num_seqs, int num_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int num_blocks,
+                                  float scale, int num_ctas,
+                                  void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, pkv_decode_plan_t **plan);
+size_t pkv_decode_workspace_size_shared(int num_seqs, int num_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int num_ctas);
+
 /* Bytes of workspace pkv_paged_attention_decode needs (host call; queries the
  * current device's SM count when num_ctas == 0).  Returns 0 for unsupported
  * shapes. */
@@ -544,6 +596,14 @@ int pkv_release(pkv_alloc_t *a, int seq, int *n_freed);
 int pkv_export_tables(const pkv_alloc_t *a, const int32_t *seqs, int n,
                       int32_t *tables, int max_blocks_per_seq,
                       int32_t *ctx_lens);
+
+/* Prefix sharing of a batch, for pkv_paged_attention_decode_shared: for i in
+ * [1, n), shared_out[i] = the number of leading logical blocks of sequence
+ * seqs[i] whose physical block is the one of seqs[i-1] at the same logical
+ * index (the blocks a fork shares with its parent until copy-on-write);
+ * shared_out[0] = 0.  Same errors as pkv_export_tables (nothing written). */
+int pkv_export_shared_prefix(const pkv_alloc_t *a, const int32_t *seqs, int n,
+                             int32_t *shared_out);
 
 int pkv_seq_length(const pkv_alloc_t *a, int seq, int *num_tokens);
 int pkv_seq_num_blocks(const pkv_alloc_t *a, int seq, int *num_blocks);

@@ -56,6 +56,10 @@ SIGNATURES = {
                                                    _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_float,
                                                    _c_int, _vp, _c_size, _vp, _vp]),
     "pkv_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pkv_paged_attention_decode_shared": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int,
+                                                   _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_float,
+                                                   _c_int, _vp, _c_size, _vp, _vp]),
+    "pkv_decode_workspace_size_shared": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "pkv_paged_attention_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int,
                                                     _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _c_int,
                                                     _vp, _vp]),
@@ -78,6 +82,7 @@ SIGNATURES = {
     "pkv_fork": (_c_int, [_vp, _c_int, _intp]),
     "pkv_release": (_c_int, [_vp, _c_int, _intp]),
     "pkv_export_tables": (_c_int, [_vp, _vp, _c_int, _vp, _c_int, _vp]),
+    "pkv_export_shared_prefix": (_c_int, [_vp, _vp, _c_int, _vp]),
     "pkv_seq_length": (_c_int, [_vp, _c_int, _intp]),
     "pkv_seq_num_blocks": (_c_int, [_vp, _c_int, _intp]),
     "pkv_seq_table": (_c_int, [_vp, _c_int, _i32p, _c_int, _intp]),
@@ -92,6 +97,9 @@ SIGNATURES = {
     "pkv_decode_plan_create": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
                                         _c_int, _c_int, _c_int, ctypes.c_float, _c_int, _vp, _c_size, _vp,
                                         ctypes.POINTER(_vp)]),
+    "pkv_decode_plan_create_shared": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int,
+                                               _c_int, _c_int, _c_int, _c_int, _c_int, ctypes.c_float, _c_int,
+                                               _vp, _c_size, _vp, ctypes.POINTER(_vp)]),
     "pkv_decode_plan_launch": (_c_int, [_vp, _vp]),
     "pkv_decode_plan_step": (_c_int, [_vp, _vp, _vp, _c_size, _vp, _vp]),
     "pkv_decode_plan_destroy": (None, [_vp]),
@@ -269,10 +277,18 @@ def decode_default_ctas(num_heads, num_kv_heads, head_dim, block_size):
     return int(load().pkv_decode_default_ctas(num_heads, num_kv_heads, head_dim, block_size))
 
 
-def new_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0, device="cuda"):
-    """A device workspace of the size pkv_decode_workspace_size asks for."""
+def decode_workspace_size_shared(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0):
+    return int(load().pkv_decode_workspace_size_shared(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                       num_ctas))
+
+
+def new_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas=0, device="cuda",
+                  shared=False):
+    """A device workspace of the size pkv_decode_workspace_size (shared:
+    pkv_decode_workspace_size_shared) asks for."""
     import torch
-    n = decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas)
+    size = decode_workspace_size_shared if shared else decode_workspace_size
+    n = size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas)
     if n == 0:
         raise PkvError(PKV_ERR_UNSUPPORTED, "decode_workspace_size")
     return torch.empty(n, dtype=torch.uint8, device=device)
@@ -338,6 +354,45 @@ def paged_attention_decode_append(out, query, key, value, key_cache, value_cache
     return out
 
 
+@_traced
+def paged_attention_decode_shared(out, query, key_cache, value_cache, block_tables, context_lens, shared_blocks,
+                                  scale, key=None, value=None, num_ctas=0, workspace=None, status=None,
+                                  stream=None):
+    """pkv_paged_attention_decode_shared: decode (with key/value: append the
+    new tokens and attend) reading blocks that consecutive sequences share
+    once for all of them.  shared_blocks: int32 [N] CUDA tensor, entry s the
+    leading blocks sequence s shares with s - 1 (BlockAllocator.shared_prefix).
+    A workspace (shared layout) is allocated when None."""
+    import torch
+    if (key is None) != (value is None):
+        raise ValueError("key and value go together")
+    specs = [(query, torch.float16, "query", 3), (out, torch.float16, "out", 3),
+             (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
+             (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1),
+             (shared_blocks, torch.int32, "shared_blocks", 1)]
+    if key is not None:
+        specs += [(key, torch.float16, "key", 3), (value, torch.float16, "value", 3)]
+    _need_all(*specs)
+    n, h, d = query.shape
+    nb, hkv, bs, d2 = key_cache.shape
+    if key is not None and (tuple(key.shape) != (n, hkv, d) or tuple(value.shape) != (n, hkv, d)):
+        raise ValueError("inconsistent shapes")
+    if tuple(out.shape) != (n, h, d) or d2 != d or tuple(value_cache.shape) != tuple(key_cache.shape) \
+            or block_tables.shape[0] != n or context_lens.shape[0] != n or shared_blocks.shape[0] != n:
+        raise ValueError("inconsistent shapes")
+    with _one_device((out, query, key, value, key_cache, value_cache, block_tables, context_lens, shared_blocks,
+                      workspace, status), stream):
+        if workspace is None:
+            workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device, shared=True)
+        ws, ws_bytes = _workspace(workspace)
+        rc = load().pkv_paged_attention_decode_shared(
+            _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), _ptr(shared_blocks), n, h, hkv, d, bs,
+            nb, float(scale), int(num_ctas), ws, ws_bytes, _status_ptr(status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_shared")
+    return out
+
+
 class DecodePlan:
     """pkv_decode_plan_*: a decode call validated once and launched many
     times with the same tensors (their contents may change between launches).
@@ -352,10 +407,14 @@ class DecodePlan:
     passed the launch."""
 
     def __init__(self, out, query, key_cache, value_cache, block_tables, context_lens, scale, key=None,
-                 value=None, num_ctas=0, workspace=None, status=None):
+                 value=None, num_ctas=0, workspace=None, status=None, shared_blocks=None):
         import torch
         if (key is None) != (value is None):
             raise ValueError("key and value go together")
+        if shared_blocks is not None:
+            _need(shared_blocks, torch.int32, "shared_blocks", 1)
+            if shared_blocks.shape[0] != query.shape[0]:
+                raise ValueError("inconsistent shapes")
         specs = [(query, torch.float16, "query", 3),
                  (key_cache, torch.float16, "key_cache", 4), (value_cache, torch.float16, "value_cache", 4),
                  (block_tables, torch.int32, "block_tables", 2), (context_lens, torch.int32, "context_lens", 1)]
@@ -376,17 +435,24 @@ class DecodePlan:
         self._lib = load()
         handle = ctypes.c_void_p()
         with _one_device((out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
-                          status)):
+                          status, shared_blocks)):
             if workspace is None:
-                workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device)
+                workspace = new_workspace(n, h, hkv, d, bs, num_ctas, query.device, shared=shared_blocks is not None)
             ws, ws_bytes = _workspace(workspace)
-            rc = self._lib.pkv_decode_plan_create(
-                _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
-                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb,
-                float(scale), int(num_ctas), ws, ws_bytes, _status_ptr(status), ctypes.byref(handle))
+            if shared_blocks is None:
+                rc = self._lib.pkv_decode_plan_create(
+                    _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), n, h, hkv, d, bs, nb,
+                    float(scale), int(num_ctas), ws, ws_bytes, _status_ptr(status), ctypes.byref(handle))
+            else:
+                rc = self._lib.pkv_decode_plan_create_shared(
+                    _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), _ptr(shared_blocks), n, h, hkv,
+                    d, bs, nb, float(scale), int(num_ctas), ws, ws_bytes, _status_ptr(status),
+                    ctypes.byref(handle))
         _check(rc, "pkv_decode_plan_create")
         self._keep = (out, query, key, value, key_cache, value_cache, block_tables, context_lens, workspace,
-                      status)
+                      status, shared_blocks)
         self._device = query.device.index
         self._h = handle
         self.out = out
@@ -699,6 +765,17 @@ class BlockAllocator:
         _check(self._lib.pkv_export_tables(self._h, s.ctypes.data, n, tables.ctypes.data, max_blocks_per_seq,
                                            lens.ctypes.data), "pkv_export_tables")
         return tables, lens
+
+    def shared_prefix(self, seqs, out=None):
+        """-> int32 [n]: entry i the leading blocks seqs[i] shares with
+        seqs[i - 1] (0 for i = 0): the hint of paged_attention_decode_shared."""
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = s.shape[0]
+        res = out if out is not None else np.empty(n, np.int32)
+        _out_array(res, np.int32, n, "out")
+        _check(self._lib.pkv_export_shared_prefix(self._h, s.ctypes.data, n, res.ctypes.data),
+               "pkv_export_shared_prefix")
+        return res
 
     def seq_len(self, seq):
         _check(self._lib.pkv_seq_length(self._h, seq, ctypes.byref(self._i)), "pkv_seq_length")

@@ -281,6 +281,25 @@ extern "C" int pkv_export_tables(const pkv_alloc_t *a, const int32_t *seqs, int 
     return PKV_OK;
 }
 
+extern "C" int pkv_export_shared_prefix(const pkv_alloc_t *a, const int32_t *seqs, int n, int32_t *shared_out) {
+    if (!a || n < 0 || (n > 0 && (!seqs || !shared_out))) return PKV_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const pkv_alloc::Seq *s = a->find(seqs[i]);
+        if (!s) return PKV_ERR_NOT_FOUND;
+        if (s->swapped) return PKV_ERR_SWAPPED;
+    }
+    for (int i = 0; i < n; ++i) {
+        int32_t common = 0;
+        if (i > 0) {
+            const std::vector<int32_t> &x = a->find(seqs[i])->table, &y = a->find(seqs[i - 1])->table;
+            const size_t m = x.size() < y.size() ? x.size() : y.size();
+            while ((size_t)common < m && x[common] == y[common]) ++common;
+        }
+        shared_out[i] = common;
+    }
+    return PKV_OK;
+}
+
 extern "C" int pkv_seq_length(const pkv_alloc_t *a, int seq, int *num_tokens) {
     if (!a || !num_tokens) return PKV_ERR_INVALID_ARG;
     const pkv_alloc::Seq *s = a->find(seq);

@@ -39,6 +39,14 @@ PKV_DECLARE_INFO(128, 2)
 PKV_DECLARE_INFO(128, 4)
 PKV_DECLARE_INFO(128, 8)
 #undef PKV_DECLARE_INFO
+bool decode_kernel_info_d64_grp(int, DecodeKernelInfo *);
+bool decode_kernel_info_d128_grp(int, DecodeKernelInfo *);
+
+bool decode_kernel_info_grouped(int head_dim, int block_size, DecodeKernelInfo *info) {
+    if (head_dim == 64) return decode_kernel_info_d64_grp(block_size, info);
+    if (head_dim == 128) return decode_kernel_info_d128_grp(block_size, info);
+    return false;
+}
 
 bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInfo *info) {
 #define PKV_CASE(d, g) \
@@ -58,6 +66,8 @@ bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInf
 namespace {
 
 constexpr int kMaxSeqs = 4096;
+constexpr int kMaxSeqsGrouped = 1024;  // the grouped kernel's per-sequence shared memory (32 bytes each)
+constexpr int kGroupRows = 8;          // query rows of a grouped item: up to 8 sequences of group 1
 constexpr int kMaxCtas = 4096;
 
 struct Resolved {
@@ -93,9 +103,19 @@ int ensure_smem_attr(const void *fn, size_t smem) {
     return PKV_OK;
 }
 
+// Whether a call with prefix-sharing hints runs the grouped kernel: group 1,
+// whole-block chunks (block size 16 or more), a batch whose per-sequence
+// arrays fit; other calls run the plain kernel and the hints are not needed.
+bool use_grouped(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size) {
+    DecodeKernelInfo info;
+    return num_heads == num_kv_heads && block_size >= 16 && num_seqs <= kMaxSeqsGrouped &&
+           decode_kernel_info_grouped(head_dim, block_size, &info);
+}
+
 int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_ctas,
-            Resolved *r) {
-    if (!decode_kernel_info(head_dim, num_heads / num_kv_heads, block_size, &r->info))
+            Resolved *r, bool grouped = false) {
+    if (grouped ? !decode_kernel_info_grouped(head_dim, block_size, &r->info)
+                : !decode_kernel_info(head_dim, num_heads / num_kv_heads, block_size, &r->info))
         return PKV_ERR_UNSUPPORTED;
     // [cum (N+1)][ctx (N)] padded to 8 bytes, then [bounds (C+1)]
     const size_t seq_bytes = ((r->info.smem_per_seq * (size_t)num_seqs + 4) + 7) & ~(size_t)7;
@@ -185,14 +205,31 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int nu
 
 using namespace pkv;
 
-extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                                            int block_size, int num_ctas) {
+namespace {
+
+size_t workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int num_ctas,
+                      bool shared) {
     if (num_seqs < 1 || num_seqs > kMaxSeqs) return 0;
     if (!shape_supported(num_heads, num_kv_heads, head_dim, block_size)) return 0;
+    const bool grouped = shared && use_grouped(num_seqs, num_heads, num_kv_heads, head_dim, block_size);
     Resolved r;
-    if (resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r) != PKV_OK) return 0;
-    return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas, num_heads / num_kv_heads, head_dim)
+    if (resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r, grouped) != PKV_OK)
+        return 0;
+    return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas,
+                                 grouped ? kGroupRows : num_heads / num_kv_heads, head_dim, grouped)
         .total;
+}
+
+}  // namespace
+
+extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                            int block_size, int num_ctas) {
+    return workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, false);
+}
+
+extern "C" size_t pkv_decode_workspace_size_shared(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                   int block_size, int num_ctas) {
+    return workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, true);
 }
 
 extern "C" int pkv_decode_default_ctas(int num_heads, int num_kv_heads, int head_dim, int block_size) {
@@ -209,9 +246,9 @@ namespace {
 // call with no sequences (nothing to launch).
 int build_plan(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
                const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
-               const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-               int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
-               int32_t *dev_status, pkv_decode_plan *plan) {
+               const int32_t *context_lens, const int32_t *shared_blocks, int num_seqs, int num_heads,
+               int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, int num_ctas,
+               void *workspace, size_t workspace_bytes, int32_t *dev_status, pkv_decode_plan *plan) {
     plan->empty = num_seqs == 0;
     if (num_seqs == 0) return PKV_OK;
     if ((new_key == nullptr) != (new_value == nullptr)) return PKV_ERR_INVALID_ARG;
@@ -229,11 +266,14 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     if ((int64_t)num_blocks * num_kv_heads * block_size >= (INT64_C(1) << 31)) return PKV_ERR_INVALID_ARG;
     if (!shape_supported(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
 
+    const bool grouped = shared_blocks != nullptr &&
+                         use_grouped(num_seqs, num_heads, num_kv_heads, head_dim, block_size);
     Resolved r;
-    int rc = resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r);
+    int rc = resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r, grouped);
     if (rc != PKV_OK) return rc;
     const int group = num_heads / num_kv_heads;
-    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas, group, head_dim);
+    const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas,
+                                                     grouped ? kGroupRows : group, head_dim, grouped);
     if (workspace_bytes < ws.total) return PKV_ERR_INVALID_ARG;
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
@@ -269,6 +309,10 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.ws_sync = reinterpret_cast<unsigned long long *>(wsb + ws.sync);
     p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count);
     p.status = dev_status;
+    p.shared_blocks = grouped ? shared_blocks : nullptr;
+    p.ws_sh = grouped ? reinterpret_cast<float *>(wsb + ws.sh) : nullptr;
+    p.ws_pv = grouped ? reinterpret_cast<float *>(wsb + ws.pv) : nullptr;
+    p.ws_fc = grouped ? reinterpret_cast<unsigned long long *>(wsb + ws.fc) : nullptr;
     p.num_seqs = num_seqs;
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;
@@ -298,13 +342,14 @@ int launch_plan(const pkv_decode_plan &plan, pkv_stream_t stream) {
 
 int decode_impl(void *out, const void *query, const void *new_key, const void *new_value, const void *key_cache,
                 const void *value_cache, const int32_t *block_tables, int max_blocks_per_seq,
-                const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-                int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
-                int32_t *dev_status, pkv_stream_t stream) {
+                const int32_t *context_lens, const int32_t *shared_blocks, int num_seqs, int num_heads,
+                int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale, int num_ctas,
+                void *workspace, size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream) {
     pkv_decode_plan plan;
     const int rc = build_plan(out, query, new_key, new_value, key_cache, value_cache, block_tables,
-                              max_blocks_per_seq, context_lens, num_seqs, num_heads, num_kv_heads, head_dim,
-                              block_size, num_blocks, scale, num_ctas, workspace, workspace_bytes, dev_status, &plan);
+                              max_blocks_per_seq, context_lens, shared_blocks, num_seqs, num_heads, num_kv_heads,
+                              head_dim, block_size, num_blocks, scale, num_ctas, workspace, workspace_bytes,
+                              dev_status, &plan);
     if (rc != PKV_OK) return rc;
     return launch_plan(plan, stream);
 }
@@ -318,8 +363,8 @@ extern "C" int pkv_paged_attention_decode(void *out, const void *query, const vo
                                           int num_blocks, float scale, int num_ctas, void *workspace,
                                           size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream) {
     return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                       num_ctas, workspace, workspace_bytes, dev_status, stream);
+                       context_lens, nullptr, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, num_ctas, workspace, workspace_bytes, dev_status, stream);
 }
 
 extern "C" int pkv_paged_attention_decode_append(void *out, const void *query, const void *key,
@@ -332,8 +377,23 @@ extern "C" int pkv_paged_attention_decode_append(void *out, const void *query, c
                                                  pkv_stream_t stream) {
     if (num_seqs > 0 && (!key || !value)) return PKV_ERR_INVALID_ARG;
     return decode_impl(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                       num_ctas, workspace, workspace_bytes, dev_status, stream);
+                       context_lens, nullptr, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, num_ctas, workspace, workspace_bytes, dev_status, stream);
+}
+
+extern "C" int pkv_paged_attention_decode_shared(void *out, const void *query, const void *key, const void *value,
+                                                 void *key_cache, void *value_cache, const int32_t *block_tables,
+                                                 int max_blocks_per_seq, const int32_t *context_lens,
+                                                 const int32_t *shared_blocks, int num_seqs, int num_heads,
+                                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                                 float scale, int num_ctas, void *workspace,
+                                                 size_t workspace_bytes, int32_t *dev_status,
+                                                 pkv_stream_t stream) {
+    if ((key == nullptr) != (value == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && !shared_blocks) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       context_lens, shared_blocks, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, scale, num_ctas, workspace, workspace_bytes, dev_status, stream);
 }
 
 namespace {
@@ -367,20 +427,21 @@ int plan_output(void *out, pkv_decode_plan *plan) {
 
 }  // namespace
 
-extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,
-                                      void *key_cache, void *value_cache, const int32_t *block_tables,
-                                      int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                                      int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                      float scale, int num_ctas, void *workspace, size_t workspace_bytes,
-                                      int32_t *dev_status, pkv_decode_plan_t **plan_out) {
+namespace {
+
+int plan_create(void *out, const void *query, const void *key, const void *value, void *key_cache,
+                void *value_cache, const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                const int32_t *shared_blocks, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                int block_size, int num_blocks, float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                int32_t *dev_status, pkv_decode_plan_t **plan_out) {
     if (!plan_out) return PKV_ERR_INVALID_ARG;
     *plan_out = nullptr;
     if ((key == nullptr) != (value == nullptr)) return PKV_ERR_INVALID_ARG;
     pkv_decode_plan *plan = new (std::nothrow) pkv_decode_plan;
     if (!plan) return PKV_ERR_INVALID_ARG;
     int rc = build_plan(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                        num_ctas, workspace, workspace_bytes, dev_status, plan);
+                        context_lens, shared_blocks, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, scale, num_ctas, workspace, workspace_bytes, dev_status, plan);
     if (rc == PKV_OK && !plan->empty) rc = plan_output(out, plan);
     if (rc != PKV_OK) {
         delete plan;
@@ -388,6 +449,33 @@ extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *
     }
     *plan_out = plan;
     return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_plan_create(void *out, const void *query, const void *key, const void *value,
+                                      void *key_cache, void *value_cache, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                      int num_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                      float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                                      int32_t *dev_status, pkv_decode_plan_t **plan_out) {
+    return plan_create(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       context_lens, nullptr, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       scale, num_ctas, workspace, workspace_bytes, dev_status, plan_out);
+}
+
+extern "C" int pkv_decode_plan_create_shared(void *out, const void *query, const void *key, const void *value,
+                                             void *key_cache, void *value_cache, const int32_t *block_tables,
+                                             int max_blocks_per_seq, const int32_t *context_lens,
+                                             const int32_t *shared_blocks, int num_seqs, int num_heads,
+                                             int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                             float scale, int num_ctas, void *workspace, size_t workspace_bytes,
+                                             int32_t *dev_status, pkv_decode_plan_t **plan_out) {
+    if (plan_out) *plan_out = nullptr;
+    if (num_seqs > 0 && !shared_blocks) return PKV_ERR_INVALID_ARG;
+    return plan_create(out, query, key, value, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                       context_lens, shared_blocks, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, scale, num_ctas, workspace, workspace_bytes, dev_status, plan_out);
 }
 
 extern "C" int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream) {

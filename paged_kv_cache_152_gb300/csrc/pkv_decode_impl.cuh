@@ -108,7 +108,9 @@ struct DecodeGeometry {
 // Dynamic shared memory (from a 1024-byte aligned base):
 // [stages][query + new-row slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)]
 // [partial slots (optional): NW workers x 2 (first / last piece) x G x (2 + D) fp32].
-template <int NW, int ST, int D, int BS, int G>
+// (grouped kernel: [ctx (N)][shared (N)][cum (2N+1)] padded to 8 bytes, then
+// [item (2N) int2][bounds (C+1)] -- 32 bytes per sequence)
+template <int NW, int ST, int D, int BS, int G, bool GRP = false>
 struct DecodeSmem {
     using Geo = DecodeGeometry<D, BS, G>;
     static constexpr size_t kQ = (size_t)NW * ST * Geo::kStageBytes;
@@ -117,7 +119,7 @@ struct DecodeSmem {
     static constexpr size_t kCum = kMeta + (size_t)NW * ST * 32;  // two int4 per stage
     static constexpr size_t kAlign = 1024;              // slack for aligning the base
     static constexpr size_t kFixed = kCum + kAlign;
-    static constexpr size_t kPerSeq = 8;
+    static constexpr size_t kPerSeq = GRP ? 32 : 8;
     static constexpr size_t kSlotFloats = (size_t)G * (2 + D);  // (m, l) per head, then the outputs
     static constexpr size_t kPartials = (size_t)NW * 2 * kSlotFloats * 4 + 16;  // + alignment slack
 };
@@ -398,6 +400,11 @@ struct WorkerCtx {
     float *part;             // partial slots of this CTA's workers (shared), or NULL
     int64_t lo, len;         // this CTA's range [lo, lo + len)
     int r0, r1;              // chunks its first / last worker give up (cta_share_start)
+    // grouped kernel only (else NULL): sequences' contexts, the items, and
+    // this call's per-(sequence, KV head) counters of the two parts
+    const int *ctx;
+    const int2 *info;
+    unsigned long long *fc;
 
     // first chunk of worker w, one of this CTA's workers or the next CTA's first
     __device__ __forceinline__ int64_t start(int64_t w) const {
@@ -605,12 +612,99 @@ __device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref re
     }
 }
 
+// ---- the grouped (prefix-sharing) kernel ----------------------------------
+// The caller tells, per sequence, how many leading blocks its table shares
+// with the previous sequence's.  Up to 8 consecutive sequences that share
+// blocks form a group; the work is cut into ITEMS instead of sequences: a
+// group's shared full blocks, read once with the members' queries as the rows
+// of one segment (group 1: one query row per member, like the heads of a
+// group-8 segment), then every member's own remaining chunks.  A member's
+// output is the merge of its two parts: each part is stored in its slot and
+// counted in on the member's counter, and whichever completes the count
+// folds them (shared part first, then its own) and writes the row.
+// Sequences outside groups are items of their own, written as usual.
+struct ItemInfo {
+    int s0;  // first (or only) sequence
+    int ns;  // sequences: >= 2 for a group's shared part
+    int c0;  // the item's first chunk within the sequence
+};
+__device__ __forceinline__ ItemInfo item_info(const int2 *info, int it) {
+    const int2 v = info[it];
+    return {v.x & 0xffff, v.x >> 16, v.y};
+}
+
+// The slot of sequence s's part over its group's shared blocks (shared) or
+// over its own chunks: (max, sum) then the D unnormalised outputs.
+template <int D>
+__device__ __forceinline__ float *part_slot(const DecodeParams &p, bool shared, int s, int kvh) {
+    return (shared ? p.ws_sh : p.ws_pv) + ((int64_t)s * p.num_kv_heads + kvh) * (2 + D);
+}
+
+// After item `it`'s rows were stored in their part slots: count each row's
+// chunks in on its sequence's counter; every sequence whose count is then
+// complete gets its two parts merged, in a fixed order, and its row written.
+template <int D, int NW>
+__device__ __forceinline__ void settle_parts(const DecodeParams &p, const WorkerCtx<NW> &wc, int it, int kvh,
+                                             int lane) {
+    const ItemInfo ii = item_info(wc.info, it);
+    const int amount = (wc.cum[it + 1] - wc.cum[it]) / p.num_kv_heads;
+    fence_acq_rel_gpu();  // the parts are visible device-wide before they are counted
+    __syncwarp();
+    bool last = false;
+    if (lane < ii.ns) {
+        const int sq = ii.s0 + lane;
+        const int total = chunks_for(wc.ctx[sq], 16);
+        last = count_in_tagged(wc.fc + (int64_t)sq * p.num_kv_heads + kvh, wc.epoch, total, amount) == total;
+    }
+    unsigned mask = __ballot_sync(kFullMask, last);
+    if (mask == 0) return;
+    fence_acq_rel_gpu();
+    while (mask) {
+        const int g = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int sq = ii.s0 + g;
+        float *a = part_slot<D>(p, true, sq, kvh);
+        float *b = part_slot<D>(p, false, sq, kvh);
+        MergeState<D, 1> ms;
+        ms.init();
+        ms.add(PieceRef{a, a + 2, false, true}, lane);
+        ms.add(PieceRef{b, b + 2, false, true}, lane);
+        ms.write_out(p, sq, kvh, lane);
+    }
+}
+
+// The result of item `it` after a merge (lane j holds dims j*D/32 ... of each
+// row): a sequence's whole output row, or the parts of the item's sequences.
+template <int D, int G, int NW>
+__device__ __forceinline__ void emit_merged_grp(const DecodeParams &p, const WorkerCtx<NW> &wc,
+                                                const MergeState<D, G> &ms, int it, int kvh, int lane) {
+    constexpr int PER = D / 32;
+    const ItemInfo ii = item_info(wc.info, it);
+    if (ii.ns == 1 && ii.c0 == 0) {
+        __half *dst = p.out + ((int64_t)ii.s0 * p.num_heads + kvh) * D + lane * PER;
+        const float inv = 1.f / ms.L[0];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(ms.O[0][k] * inv);
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (g < ii.ns) {
+            float *slot = part_slot<D>(p, ii.ns > 1, ii.s0 + g, kvh);
+            if (lane == 0) *reinterpret_cast<float2 *>(slot) = make_float2(ms.M[g], ms.L[g]);
+#pragma unroll
+            for (int k = 0; k < PER; ++k) slot[2 + lane * PER + k] = ms.O[g][k];
+        }
+    }
+    settle_parts<D, NW>(p, wc, it, kvh, lane);
+}
+
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
 // row (whole segment) or store the partial (cut segment).  Returns true for a
 // stored partial; the caller counts it in (count_piece).  The output is held
 // transposed (see consume_chunk): each lane pairs its values with lane ^ 4's
 // so that it stores two neighbouring dims of one head, hh = 2t + (g & 1).
-template <int D, int G, int NW>
+template <int D, int G, int NW, bool GRP = false>
 __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const WorkerCtx<NW> &wc, const int4 md, float m,
                                              float l, const float (&o)[D / 16][4], SegInfo &si, int lane) {
     const int g = lane >> 2;
@@ -626,7 +720,41 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
         const float y = __shfl_xor_sync(kFullMask, (g & 1) ? own_e : own_o, 4);
         return (g & 1) ? make_float2(y, own_o) : make_float2(own_e, y);
     };
-    if (flags & kWhole) {
+    if constexpr (GRP) {
+        // a whole item: a sequence's output row (row 0), or its rows' parts
+        const ItemInfo ii = item_info(wc.info, s);
+        if ((flags & kWhole) && !(ii.ns == 1 && ii.c0 == 0)) {
+            float *dst = part_slot<D>(p, ii.ns > 1, ii.s0 + (hh < ii.ns ? hh : 0), kvh) + 2 + d0;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                const float2 a = pair(o[i][0], o[i][1]);
+                const float2 b = pair(o[i][2], o[i][3]);
+                if (hh < ii.ns) {
+                    *reinterpret_cast<float2 *>(dst + 16 * i) = a;
+                    *reinterpret_cast<float2 *>(dst + 16 * i + 8) = b;
+                }
+            }
+            if (t == 0 && g < ii.ns)
+                *reinterpret_cast<float2 *>(part_slot<D>(p, ii.ns > 1, ii.s0 + g, kvh)) = make_float2(m, l);
+            settle_parts<D, NW>(p, wc, s, kvh, lane);
+            return false;
+        }
+        if (flags & kWhole) {
+            const float inv = 1.f / __shfl_sync(kFullMask, l, 0);  // l of row 0
+            __half *dst = p.out + ((int64_t)ii.s0 * p.num_heads + kvh) * D + d0;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+                const float2 a = pair(o[i][0], o[i][1]);
+                const float2 b = pair(o[i][2], o[i][3]);
+                if (hh == 0) {
+                    *reinterpret_cast<uint32_t *>(dst + 16 * i) = pack_half2(a.x * inv, a.y * inv);
+                    *reinterpret_cast<uint32_t *>(dst + 16 * i + 8) = pack_half2(b.x * inv, b.y * inv);
+                }
+            }
+            return false;
+        }
+    }
+    if (!GRP && (flags & kWhole)) {
         const float inv = 1.f / __shfl_sync(kFullMask, l, 4 * hh);  // l of head hh
         __half *dst = p.out + ((int64_t)s * p.num_heads + kvh * G + hh) * D + d0;
 #pragma unroll
@@ -723,7 +851,7 @@ __device__ __forceinline__ bool count_piece(const WorkerCtx<NW> &wc, const SegIn
 
 // Merges this CTA's part of cut segment (s, kvh) (see count_piece); si is
 // its segment_info (only the CTA-level fields are used).
-template <int D, int G, int NW>
+template <int D, int G, int NW, bool GRP = false>
 __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCtx<NW> &wc, int s, int kvh,
                                            const SegInfo &si, int lane) {
     const int64_t g1 = si.g0 + si.nch;
@@ -745,7 +873,10 @@ __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCt
     else
         merge_wide<D, G>(ms, cnt, wref, lane);
     if (si.local) {
-        ms.write_out(p, s, kvh, lane);
+        if constexpr (GRP)
+            emit_merged_grp<D, G, NW>(p, wc, ms, s, kvh, lane);
+        else
+            ms.write_out(p, s, kvh, lane);
         return;
     }
     ms.store(cta_piece<D, G>(p, blockIdx.x, si.xw), lane);
@@ -770,7 +901,10 @@ __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCt
         merge_seq<D, G>(ms2, cb - ca + 1, cref, lane);
     else
         merge_wide<D, G>(ms2, cb - ca + 1, cref, lane);
-    ms2.write_out(p, s, kvh, lane);
+    if constexpr (GRP)
+        emit_merged_grp<D, G, NW>(p, wc, ms2, s, kvh, lane);
+    else
+        ms2.write_out(p, s, kvh, lane);
 }
 
 // The CTA's merge queue (shared memory): segments whose CTA part is complete
@@ -784,7 +918,7 @@ struct MergeQueue {
     int head;                // entries taken by consumers
 };
 
-template <int D, int BS, int G, int NW, int ST>
+template <int D, int BS, int G, int NW, int ST, bool GRP = false>
 __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #ifdef PKV_DECODE_SNAP_CAP
     constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
@@ -817,18 +951,33 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     constexpr bool kCudaCore = false;  // group 1 on the tensor cores too (see consume_chunk_cc)
 #endif
     using Geo = DecodeGeometry<D, BS, G>;
-    using Smem = DecodeSmem<NW, ST, D, BS, G>;
+    using Smem = DecodeSmem<NW, ST, D, BS, G, GRP>;
+    static_assert(!GRP || (G == 8 && BS >= 16), "the grouped kernel: 8 query rows per item, whole-block chunks");
     extern __shared__ unsigned char smem_raw[];
     __shared__ int warp_sums[32];
+    __shared__ int warp_sums2[32];
     // 1024-byte aligned base: the 128-byte swizzle pattern is tied to address bits
     unsigned char *smem =
         smem_raw + ((Smem::kAlign - (smem_addr(smem_raw) & (Smem::kAlign - 1))) & (Smem::kAlign - 1));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Smem::kBars);
     int4 *meta = reinterpret_cast<int4 *>(smem + Smem::kMeta);
-    int *cum = reinterpret_cast<int *>(smem + Smem::kCum);
     const int N = p.num_seqs;
-    int *ctx = cum + N + 1;
-    int64_t *bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
+    // per-sequence arrays: [cum (N+1)][ctx (N)] | grouped: [ctx (N)][shared (N)]
+    // [cum over items (2N+1)] [items (2N)]; then the CTA bounds
+    int *cum, *ctx, *shv = nullptr;
+    int2 *info = nullptr;
+    int64_t *bounds;
+    if constexpr (GRP) {
+        ctx = reinterpret_cast<int *>(smem + Smem::kCum);
+        shv = ctx + N;
+        cum = shv + N;
+        info = reinterpret_cast<int2 *>(smem + Smem::kCum + (((size_t)(4 * N + 1) * 4 + 7) & ~(size_t)7));
+        bounds = reinterpret_cast<int64_t *>(info + 2 * N);
+    } else {
+        cum = reinterpret_cast<int *>(smem + Smem::kCum);
+        ctx = cum + N + 1;
+        bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
+    }
     __shared__ int cta_count[NW];
     __shared__ int exit_count;
     __shared__ int cta_cross;
@@ -857,6 +1006,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     const int s_lo = min(N, tid * per);
     const int s_hi = min(N, s_lo + per);
     int local = 0;
+    int last_start = -1;  // grouped: the last sequence of this thread's range that starts a chain
     for (int s = s_lo; s < s_hi; ++s) {
         int c = p.context_lens[s];
         if (c < 0 || c > max_ctx) {
@@ -865,12 +1015,18 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         }
         ctx[s] = c;
         local += Hkv * chunks_for(c, Geo::kRows);
+        if constexpr (GRP) {
+            const int h = s == 0 ? 0 : max(0, (int)p.shared_blocks[s]);
+            shv[s] = h;
+            if (h == 0) last_start = s;
+        }
     }
+    if constexpr (GRP) local = last_start;  // the first scan is a max over chain starts
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFullMask, incl, o);
-        if (lane >= o) incl += y;
+        if (lane >= o) incl = GRP ? max(incl, y) : incl + y;
     }
     if (lane == 31) warp_sums[warp] = incl;
     if (tid == 0) {
@@ -885,7 +1041,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         mq.tail = mq.head = 0;
     }
     __syncthreads();
-    {
+    int NI = N;  // segments' owners: sequences, or the grouped kernel's items
+    if constexpr (!GRP) {
         // every warp scans the warps' sums itself (no second barrier)
         const int v = lane < NW ? warp_sums[lane] : 0;
         int vi = v;
@@ -901,6 +1058,100 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             run += Hkv * chunks_for(ctx[s], Geo::kRows);
         }
         if (tid == 0) cum[N] = total;
+    } else {
+        // The chain start before this thread's range: the max over the
+        // threads before it (each warp scans the warps' maxima itself).
+        int chain;
+        {
+            const int v = lane < NW ? warp_sums[lane] : -1;
+            int vi = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, vi, o);
+                if (lane >= o) vi = max(vi, y);
+            }
+            const int before_warp = warp > 0 ? __shfl_sync(kFullMask, vi, warp - 1) : -1;
+            const int before_lane = __shfl_up_sync(kFullMask, incl, 1);
+            chain = max(before_warp, lane > 0 ? before_lane : -1);
+        }
+        // Each sequence's group (the leader and its members, up to 8
+        // consecutive sequences of one chain) and the shared full blocks P:
+        // at most the blocks every member shares with its predecessor, and
+        // never the block of a member's last token.  Items per sequence: a
+        // group's leader opens the shared item, then every member has its own.
+        auto group_of = [&](int s, int cs, int &lead, int &ns, int &shared_chunks) {
+            lead = cs + ((s - cs) & ~7);
+            ns = 1;
+            int pb = ctx[lead] >= 1 ? (ctx[lead] - 1) / BS : -1;
+            for (int j = 1; j < 8; ++j) {
+                const int m = lead + j;
+                if (m >= N || shv[m] == 0) break;
+                ++ns;
+                pb = min(pb, min(shv[m], ctx[m] >= 1 ? (ctx[m] - 1) / BS : -1));
+            }
+            shared_chunks = (ns >= 2 && pb >= 1) ? pb * (BS / Geo::kRows) : 0;
+        };
+        int nitems = 0, nchunks = 0;
+        {
+            int cs = chain;
+            for (int s = s_lo; s < s_hi; ++s) {
+                if (shv[s] == 0) cs = s;
+                int lead, ns, sc;
+                group_of(s, cs, lead, ns, sc);
+                nitems += (sc > 0 && s == lead) ? 2 : 1;
+                nchunks += Hkv * (chunks_for(ctx[s], Geo::kRows) - (sc > 0 && s != lead ? sc : 0));
+            }
+        }
+        // exclusive scans of (items, chunks) over the threads
+        int ii = nitems, ic = nchunks;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yi = __shfl_up_sync(kFullMask, ii, o);
+            const int yc = __shfl_up_sync(kFullMask, ic, o);
+            if (lane >= o) {
+                ii += yi;
+                ic += yc;
+            }
+        }
+        __syncthreads();  // every warp has read warp_sums
+        if (lane == 31) {
+            warp_sums[warp] = ii;
+            warp_sums2[warp] = ic;
+        }
+        __syncthreads();
+        int vi = lane < NW ? warp_sums[lane] : 0, vc = lane < NW ? warp_sums2[lane] : 0;
+        const int v0 = vi, c0 = vc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yi = __shfl_up_sync(kFullMask, vi, o);
+            const int yc = __shfl_up_sync(kFullMask, vc, o);
+            if (lane >= o) {
+                vi += yi;
+                vc += yc;
+            }
+        }
+        int item = __shfl_sync(kFullMask, vi - v0, warp) + ii - nitems;
+        int run = __shfl_sync(kFullMask, vc - c0, warp) + ic - nchunks;
+        NI = __shfl_sync(kFullMask, vi, 31);
+        const int total = __shfl_sync(kFullMask, vc, 31);
+        {
+            int cs = chain;
+            for (int s = s_lo; s < s_hi; ++s) {
+                if (shv[s] == 0) cs = s;
+                int lead, ns, sc;
+                group_of(s, cs, lead, ns, sc);
+                if (sc > 0 && s == lead) {
+                    info[item] = make_int2(lead | (ns << 16), 0);
+                    cum[item++] = run;
+                    run += Hkv * sc;
+                }
+                const int c0s = sc > 0 ? sc : 0;
+                info[item] = make_int2(s | (1 << 16), c0s);
+                cum[item++] = run;
+                run += Hkv * (chunks_for(ctx[s], Geo::kRows) - c0s);
+            }
+        }
+        if (tid == 0) cum[NI] = total;
     }
     __syncthreads();
 
@@ -908,14 +1159,14 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     // divided among the CTA's warps (cta_share_start).  A warp works out its own CTA's
     // range itself and starts its block-table loads; the CTA-wide array of
     // ranges (for the merges) is filled after that. ----
-    const int64_t T = cum[N];
+    const int64_t T = cum[NI];
     // A small batch uses only as many CTAs as give every worker at least
     // kMinShare chunks (a segment split into one-chunk pieces costs more to
     // merge than the extra workers save), and, while segments are short (up to
     // 2 kMinShare chunks per worker), no more CTAs than segments: equal
     // segments then fall one per CTA and merge in shared memory.  The other
     // CTAs have nothing to do.
-    const int64_t seg_cap = max((int64_t)N * Hkv, (T + NW * 2 * kMinShare - 1) / (NW * 2 * kMinShare));
+    const int64_t seg_cap = max((int64_t)NI * Hkv, (T + NW * 2 * kMinShare - 1) / (NW * 2 * kMinShare));
     const int C = (int)min(min((int64_t)gridDim.x, seg_cap),
                            max((int64_t)1, (T + NW * kMinShare - 1) / (NW * kMinShare)));
     if ((int)blockIdx.x >= C) return;
@@ -927,7 +1178,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         // cuts a segment)
         const int c = (int)blockIdx.x + (lane & 1);
         bool cuts = false;
-        const int64_t v = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap, &cuts);
+        const int64_t v = c == C ? T : snapped_cta_start(cum, NI, Hkv, c, C, T, kSnapCap, &cuts);
         c_lo = __shfl_sync(kFullMask, v, 0);
         c_len = __shfl_sync(kFullMask, v, 1) - c_lo;
         const int r = cut_relief_for(cuts, c_len, NW, kRelief, kReliefDiv);
@@ -940,9 +1191,9 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
 
     // the walk: cut pieces first (see share_order); lane 0 locates the
     // share's first chunk, lane 1 its last
-    ShareOrder order = share_order(cum, N, Hkv, gb, gb);  // empty
+    ShareOrder order = share_order(cum, NI, Hkv, gb, gb);  // empty
     if (n > 0) {
-        const ChunkPos e = locate_chunk(cum, N, Hkv, (lane & 1) ? ge - 1 : gb);
+        const ChunkPos e = locate_chunk(cum, NI, Hkv, (lane & 1) ? ge - 1 : gb);
         ChunkPos first, last;
         first.c = __shfl_sync(kFullMask, e.c, 0);
         first.nch = __shfl_sync(kFullMask, e.nch, 0);
@@ -955,16 +1206,32 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     // its descriptor is built), 0 past the share
     // (at block size 8 a chunk spans two blocks: the second entry comes in the
     // high half, 0 when the chunk does not reach it)
+    // the sequence and the chunk within it of a segment owner's chunk (the
+    // grouped kernel's items start at chunk c0 of their first sequence, whose
+    // table row a group's shared blocks are read through)
+    auto owner_seq = [&](int it) -> int {
+        if constexpr (GRP) return info[it].x & 0xffff;
+        return it;
+    };
+    auto owner_c0 = [&](int it) -> int {
+        if constexpr (GRP) return info[it].y;
+        return 0;
+    };
+    auto owner_rows = [&](int it) -> int {  // query rows of the owner's segments (grouped: its sequences)
+        if constexpr (GRP) return info[it].x >> 16;
+        return G;
+    };
     auto table_entry_at = [&](const ChunkPos &q) -> int2 {
-        const int lb = chunk_block(q.c, BS, Geo::kRows);
-        const int32_t *row = p.block_tables + (int64_t)q.s * p.max_blocks_per_seq;
+        const int sq = owner_seq(q.s);
+        const int lb = chunk_block(owner_c0(q.s) + q.c, BS, Geo::kRows);
+        const int32_t *row = p.block_tables + (int64_t)sq * p.max_blocks_per_seq;
         int second = 0;
-        if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[q.s]) second = __ldg(row + lb + 1);
+        if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[sq]) second = __ldg(row + lb + 1);
         return make_int2(__ldg(row + lb), second);
     };
     auto table_entry = [&](int i) -> int2 {
         if (i >= n) return make_int2(0, 0);
-        return table_entry_at(locate_chunk(cum, N, Hkv, order.at(i)));
+        return table_entry_at(locate_chunk(cum, NI, Hkv, order.at(i)));
     };
     const bool append = p.new_key != nullptr;
     // Descriptor of the chunk at walk position i, built by one lane for a
@@ -982,19 +1249,21 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             report(p.status, PKV_ERR_OUT_OF_RANGE);
             phys2 = 0;
         }
-        const int rows = chunk_rows(q.c, ctx[q.s], Geo::kRows);
-        // the decode step's new token is the last row of the segment's last chunk
-        const bool new_row = append && q.c == q.nch - 1;
+        const int lc = owner_c0(q.s) + q.c;  // the chunk within its sequence
+        const int rows = chunk_rows(lc, ctx[owner_seq(q.s)], Geo::kRows);
+        // the decode step's new token is the last row of the segment's last
+        // chunk (never in a group's shared blocks: they stop before it)
+        const bool new_row = append && q.c == q.nch - 1 && owner_rows(q.s) == (GRP ? 1 : G);
         const int flags = chunk_flags(q, g, gb, ge) | (new_row ? kAppendRow : 0);
         // row of the cache viewed as [num_blocks * Hkv * BS rows]
-        const int y = (int)(((int64_t)phys * Hkv + q.kvh) * BS + (q.c * Geo::kRows) % BS);
+        const int y = (int)(((int64_t)phys * Hkv + q.kvh) * BS + (lc * Geo::kRows) % BS);
         const int y2 = (int)(((int64_t)phys2 * Hkv + q.kvh) * BS);
         return make_int4(q.s | (q.kvh << 16), rows | (flags << 8), y, y2);
     };
     auto chunk_desc = [&](int i, int2 tab) -> int4 {
         if (i >= n) return make_int4(0, 0, 0, 0);
         const int64_t g = order.at(i);
-        return chunk_desc_at(g, locate_chunk(cum, N, Hkv, g), tab);
+        return chunk_desc_at(g, locate_chunk(cum, NI, Hkv, g), tab);
     };
     // windows 0 and 1: each lane locates its two positions in one search and
     // starts their table loads; window 0's descriptors follow as soon as the
@@ -1007,7 +1276,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         ChunkPos q0, q1;
         int2 tab0 = make_int2(0, 0);
         if (n > 0) {
-            locate_chunk2(cum, N, Hkv, lane < n ? order.at(lane) : gb, 32 + lane < n ? order.at(32 + lane) : gb,
+            locate_chunk2(cum, NI, Hkv, lane < n ? order.at(lane) : gb, 32 + lane < n ? order.at(32 + lane) : gb,
                           q0, q1);
             if (lane < n) tab0 = table_entry_at(q0);
             if (32 + lane < n) tab_nxt = table_entry_at(q1);
@@ -1036,7 +1305,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         const int y = __shfl_sync(kFullMask, desc.z, j);
         const int y2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, desc.w, j) : 0;
         if (lane == 0) {
-            const int s = sk & 0xffff, kvh = sk >> 16;
+            const int s = owner_seq(sk & 0xffff), kvh = sk >> 16;
+            const int nq = owner_rows(sk & 0xffff);  // grouped: the item's sequences, one query row each
             const int rows = rf & 0xff, flags = rf >> 8;
             const bool new_row = (flags & kAppendRow) != 0;
             const int stage = i % ST;
@@ -1049,11 +1319,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             // (the second lands 8 rows down, at +1 KB in each half)
             const bool short_box = Geo::kBPC == 2 || rows <= 8;
             const bool second = Geo::kBPC == 2 && rows > 8;
-            wmeta[2 * stage] = make_int4(s, kvh, rows, flags);
+            wmeta[2 * stage] = make_int4(sk & 0xffff, kvh, rows, flags);  // x: the segment's owner
             wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
             mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
                                                   : 2 * Geo::kTileBytes) +
-                                           ((flags & kFirst) ? Geo::kQBytes : 0) +
+                                           ((flags & kFirst) ? (GRP ? nq * D * 2 : Geo::kQBytes) : 0) +
                                            (new_row ? 2 * Geo::kRowBytes : 0));
             if (!short_box) {
                 tma_load_3d(kdst, &p.tmap_k, 0, y, 0, bar);
@@ -1069,9 +1339,16 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                     }
                 }
             }
-            if (flags & kFirst)
-                bulk_g2s(wq_a + stage * Geo::kSlotBytes, p.query + ((int64_t)s * p.num_heads + kvh * G) * D,
-                         Geo::kQBytes, bar);
+            if (flags & kFirst) {
+                if constexpr (GRP) {
+                    for (int j = 0; j < nq; ++j)
+                        bulk_g2s(wq_a + stage * Geo::kSlotBytes + j * D * 2,
+                                 p.query + ((int64_t)(s + j) * p.num_heads + kvh) * D, D * 2, bar);
+                } else {
+                    bulk_g2s(wq_a + stage * Geo::kSlotBytes, p.query + ((int64_t)s * p.num_heads + kvh * G) * D,
+                             Geo::kQBytes, bar);
+                }
+            }
             if (new_row) {
                 const int64_t src = ((int64_t)s * Hkv + kvh) * D;
                 bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
@@ -1096,16 +1373,25 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     for (; issued < min(ST, n); ++issued) issue(issued);
     // the CTA-wide ranges (needed only by the merges)
     for (int c = tid; c <= C; c += NW * 32)
-        bounds[c] = c == C ? T : snapped_cta_start(cum, N, Hkv, c, C, T, kSnapCap);
+        bounds[c] = c == C ? T : snapped_cta_start(cum, NI, Hkv, c, C, T, kSnapCap);
     __syncthreads();  // the ranges are visible to every warp's merges
     epoch = __shfl_sync(kFullMask, epoch, 0);
     const int parity = epoch & 1;
-    unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;
+    // (the grouped kernel has up to 2 items per sequence, and per (sequence,
+    // KV head) counters of the two parts besides)
+    const int64_t nseg = (int64_t)(GRP ? 2 * N : N) * Hkv;
+    unsigned long long *count_now = p.ws_count + (int64_t)parity * nseg;
+    unsigned long long *fc_now = GRP ? p.ws_fc + (int64_t)parity * N * Hkv : nullptr;
     {
-        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * N * Hkv;
+        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * nseg;
         const unsigned long long next_tag = (unsigned long long)(epoch + 1) << 32;
-        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)C * NW * 32)
+        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < nseg; i += (int64_t)C * NW * 32)
             count_next[i] = next_tag;
+        if constexpr (GRP) {
+            unsigned long long *fc_next = p.ws_fc + (int64_t)(parity ^ 1) * N * Hkv;
+            for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)C * NW * 32)
+                fc_next[i] = next_tag;
+        }
         if (blockIdx.x == 0 && tid == 0) p.ws_sync[1 + (parity ^ 1)] = next_tag;
     }
     // rows of empty contexts are zero; no worker visits them
@@ -1127,7 +1413,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
     const WorkerCtx<NW> wc{cum, bounds, C, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
-                           c_lo, c_len, r0, r1};
+                           c_lo, c_len, r0, r1, ctx, info, fc_now};
 
     // the CTA's merge queue (count_piece / merge_part)
     auto vload = [](const int *a) { return *reinterpret_cast<const volatile int *>(a); };
@@ -1138,7 +1424,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             if (idx < kMergeQueue) *reinterpret_cast<volatile int *>(&mq.entry[idx]) = s | (kvh << 16);
         }
         idx = __shfl_sync(kFullMask, idx, 0);
-        if (idx >= kMergeQueue) merge_part<D, G, NW>(p, wc, s, kvh, segment_info(p, wc, s, kvh), lane);
+        if (idx >= kMergeQueue) merge_part<D, G, NW, GRP>(p, wc, s, kvh, segment_info(p, wc, s, kvh), lane);
     };
     // After its own share a warp merges queued parts until the queue is empty.
     // No entry is left behind: a warp pushes only during its own share and
@@ -1173,7 +1459,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                 return;
             }
             fence_acq_rel_cta();
-            merge_part<D, G, NW>(p, wc, v & 0xffff, v >> 16, segment_info(p, wc, v & 0xffff, v >> 16), lane);
+            merge_part<D, G, NW, GRP>(p, wc, v & 0xffff, v >> 16, segment_info(p, wc, v & 0xffff, v >> 16), lane);
         }
     };
     // whether this CTA queues its merges (the same for all its warps): when
@@ -1221,13 +1507,15 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
 #pragma unroll
                 for (int j = 0; j < D / 2; ++j) oc[j] = 0.f;
             } else {
-                // query rows of the group as mma A fragments (rows g >= G stay 0)
+                // query rows of the group as mma A fragments (rows g >= G stay 0;
+                // grouped: rows past the item's sequences too)
+                const int nq = GRP ? owner_rows(md.x) : G;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     qa[kk][0] =
-                        gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
+                        gq < nq ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 2 * tq) * 2) : 0u;
                     qa[kk][1] =
-                        gq < G ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 8 + 2 * tq) * 2) : 0u;
+                        gq < nq ? *reinterpret_cast<const uint32_t *>(sq + (gq * D + 16 * kk + 8 + 2 * tq) * 2) : 0u;
                 }
 #pragma unroll
                 for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -1277,7 +1565,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             if constexpr (kCudaCore)
                 stored = finish_piece_cc<D, NW>(p, wc, md, m, l, oc, si, lane);
             else
-                stored = finish_piece<D, G, NW>(p, wc, md, m, l, o, si, lane);
+                stored = finish_piece<D, G, NW, GRP>(p, wc, md, m, l, o, si, lane);
         }
         if (stored &&
             count_piece<D, G, NW>(wc, si, lane)) {
@@ -1289,7 +1577,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                 fence_acq_rel_cta();  // the part's pieces are visible to whoever merges it
                 push(md.x, md.y);
             } else {
-                merge_part<D, G, NW>(p, wc, md.x, md.y, si, lane);
+                merge_part<D, G, NW, GRP>(p, wc, md.x, md.y, si, lane);
             }
         }
     }

@@ -9,7 +9,13 @@
 
 #define PKV_CAT2(a, b, c) a##b##_g##c
 #define PKV_CAT(a, b, c) PKV_CAT2(a, b, c)
+#ifdef PKV_GRP
+#define PKV_CATG2(a, b) a##b##_grp
+#define PKV_CATG(a, b) PKV_CATG2(a, b)
+#define PKV_INFO_FN PKV_CATG(decode_kernel_info_d, PKV_D)
+#else
 #define PKV_INFO_FN PKV_CAT(decode_kernel_info_d, PKV_D, PKV_G)
+#endif
 
 namespace pkv {
 namespace {
@@ -29,12 +35,18 @@ constexpr int kStages = PKV_DECODE_STAGES;
 constexpr int kStages = (PKV_D == 64) ? 4 : 2;
 #endif
 
+#ifdef PKV_GRP
+constexpr bool kGrouped = true;   // the grouped (prefix-sharing) kernel: 8 query rows per item
+#else
+constexpr bool kGrouped = false;
+#endif
+
 template <int BS>
 DecodeKernelInfo info_of() {
     using Geo = DecodeGeometry<PKV_D, BS, PKV_G>;
-    using Smem = DecodeSmem<kWarps, kStages, PKV_D, BS, PKV_G>;
+    using Smem = DecodeSmem<kWarps, kStages, PKV_D, BS, PKV_G, kGrouped>;
     DecodeKernelInfo i;
-    i.fn = reinterpret_cast<const void *>(&paged_decode_kernel<PKV_D, BS, PKV_G, kWarps, kStages>);
+    i.fn = reinterpret_cast<const void *>(&paged_decode_kernel<PKV_D, BS, PKV_G, kWarps, kStages, kGrouped>);
     i.threads = kWarps * 32;
     i.warps = kWarps;
     i.rows_per_chunk = Geo::kRows;
@@ -49,7 +61,9 @@ DecodeKernelInfo info_of() {
 
 bool PKV_INFO_FN(int block_size, DecodeKernelInfo *info) {
     switch (block_size) {
+#ifndef PKV_GRP
         case 8: *info = info_of<8>(); return true;
+#endif
         case 16: *info = info_of<16>(); return true;
         case 32: *info = info_of<32>(); return true;
         case 64: *info = info_of<64>(); return true;

@@ -301,3 +301,41 @@ def test_swap_errors(pkv):
     assert a.swap_in([s]).tolist() == [[0, 2], [1, 3]] and a.num_free_host() == 2   # FIFO: 0, 1 went to the back
     a.host_pool(8)                      # none in use: may be replaced
     assert a.num_free_host() == 8
+
+
+def test_shared_prefix_export_matches_the_tables(pkv):
+    """The decode hint of prefix sharing: for each sequence of a batch, the
+    leading blocks its table has in common with the previous sequence's, as
+    read off the oracle model's tables; forks share until copy-on-write."""
+    rng = np.random.default_rng(31)
+    model = BlockManagerModel(400, 16, rng.permutation(400).astype(np.int32))
+    alloc = pkv.BlockAllocator(400, 16, np.asarray(model.free, dtype=np.int32))
+    seqs = []
+    for root_len in (40, 64, 17, 0, 100):
+        r = model.new_seq()
+        assert alloc.new_seq() == r
+        for _ in range(root_len):
+            model.append_token(r)
+        alloc.append_tokens(r, root_len)
+        seqs.append(r)
+        for _ in range(int(rng.integers(0, 6))):
+            c = model.fork(r)
+            assert alloc.fork(r) == c
+            extra = int(rng.integers(0, 40))
+            for _ in range(extra):
+                model.append_token(c)
+            alloc.append_tokens(c, extra)
+            seqs.append(c)
+    order = list(rng.permutation(seqs)[: len(seqs) // 2]) + seqs
+    got = alloc.shared_prefix(order)
+    tables = [model.tables[s] for s in order]
+    expect = [0]
+    for a, b in zip(tables, tables[1:]):
+        k = 0
+        while k < min(len(a), len(b)) and a[k] == b[k]:
+            k += 1
+        expect.append(k)
+    assert got.tolist() == expect
+    assert max(expect) > 0 and 0 in expect[1:]
+    with pytest.raises(pkv.PkvError):
+        alloc.shared_prefix([seqs[0], 999])
