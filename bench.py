@@ -110,6 +110,9 @@ def parse_args(argv=None):
                         "that writes the new tokens itself)")
     p.add_argument("--no-graph", action="store_true",
                    help="launch every step directly instead of replaying captured CUDA graphs")
+    p.add_argument("--shared", action="store_true",
+                   help="decode through the prefix-sharing entry point (paged_attention_decode_shared) with the "
+                        "block manager's shared-prefix hints")
     p.add_argument("--identity-tables", action="store_true",
                    help="same workload with each sequence's blocks contiguous and in order")
     p.add_argument("--layers", type=int, default=0,
@@ -306,6 +309,7 @@ def build_state(cfg, device, identity_tables=False, e2e_headroom_steps=0, block_
     t["value_cache"] = W.normal_fp16_large(shape, wl.seed * 1000 + 5, device)
     st = {
         "wl": wl, "alloc": alloc, "mb": mb, "nb": nb, "t": t,
+        "shared": torch.from_numpy(alloc.shared_prefix(wl.batch)).to(device),
         "slots": torch.from_numpy(slots.astype(np.int64)).to(device),
         "pairs": torch.from_numpy(pairs.astype(np.int64)).reshape(-1, 2).to(device),
         "tables": torch.from_numpy(tables).to(device),
@@ -331,6 +335,12 @@ def write_step(pkv, st):
 
 def decode_step(pkv, st, ws, num_ctas):
     t = st["t"]
+    if st.get("use_shared"):
+        kw = dict(key=t["key"], value=t["value"]) if st.get("fused") else {}
+        pkv.paged_attention_decode_shared(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"],
+                                          st["lens"], st["shared"], st["wl"].scale, num_ctas=num_ctas,
+                                          workspace=ws, status=st["status"], **kw)
+        return
     if st.get("fused"):
         pkv.paged_attention_decode_append(st["out"], t["query"], t["key"], t["value"], t["key_cache"],
                                           t["value_cache"], st["tables"], st["lens"], st["wl"].scale,
@@ -373,8 +383,9 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     import torch
     wl, alloc = st["wl"], st["alloc"]
     n, h, hkv, d, mb = wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, st["mb"]
+    shared = bool(st.get("use_shared"))
     parts = [("q", n * h * d * 2), ("k", n * hkv * d * 2), ("v", n * hkv * d * 2), ("tables", n * mb * 4),
-             ("lens", n * 4)]
+             ("lens", n * 4)] + ([("shared", n * 4)] if shared else [])
     offs, off = {}, 0
     for name, nbytes in parts:
         offs[name] = (off, nbytes)
@@ -391,6 +402,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     tab_np = [stage_np[i, offs["tables"][0]:offs["tables"][0] + offs["tables"][1]].view(np.int32).reshape(n, mb)
               for i in range(steps)]
     lens_np = [stage_np[i, offs["lens"][0]:offs["lens"][0] + offs["lens"][1]].view(np.int32) for i in range(steps)]
+    shared_np = [stage_np[i, offs["shared"][0]:offs["shared"][0] + offs["shared"][1]].view(np.int32)
+                 for i in range(steps)] if shared else None
     h_rows = [h_stage[i] for i in range(steps)]
     d_stage = torch.empty(step_bytes, dtype=torch.uint8, device=device)
 
@@ -403,6 +416,7 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     d_v = dview("v", torch.float16, (n, hkv, d))
     d_tables = dview("tables", torch.int32, (n, mb))
     d_lens = dview("lens", torch.int32, (n,))
+    d_shared = dview("shared", torch.int32, (n,)) if shared else None
     t = st["t"]
     h_out = torch.empty((n, h, d), dtype=torch.float16).pin_memory()
     # by default the kernel writes the output straight into the pinned host
@@ -410,7 +424,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     # device memory and a D2H copy follows the launch
     plan = pkv.DecodePlan(st["out"] if copy_out else h_out, d_q, t["key_cache"], t["value_cache"], d_tables,
                           d_lens, wl.scale,
-                          key=d_k, value=d_v, num_ctas=num_ctas, workspace=ws, status=st["status"])
+                          key=d_k, value=d_v, num_ctas=num_ctas, workspace=ws, status=st["status"],
+                          shared_blocks=d_shared)
     h_slots = np.empty(n, dtype=np.int64)
     h_pairs_t = torch.empty((n, 2), dtype=torch.int64).pin_memory()
     h_pairs32 = np.empty((n, 2), dtype=np.int32)
@@ -429,6 +444,8 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
         sequence and writes the tables and lengths into step i's region."""
         _, pairs = alloc.append_batch(batch, slots_out=h_slots, pairs_out=h_pairs32)
         alloc.export(batch, mb, tables_out=tab_np[i], lens_out=lens_np[i])
+        if shared:
+            alloc.shared_prefix(batch, out=shared_np[i])
         return pairs.copy() if len(pairs) else None
 
     barrier(dist, device)
@@ -566,16 +583,19 @@ def unique_kv_bytes(tables, lens, block_size, num_kv_heads, head_dim):
     return 2 * sum(rows.values()) * num_kv_heads * head_dim * 2
 
 
-def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False):
+def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False, shared=False):
     """One workload's decode launch (the fused append + attend of the bench
-    step, through a DecodePlan): back-to-back mean and L2-flushed median."""
+    step, through a DecodePlan; shared: the prefix-sharing plan with the block
+    manager's hints): back-to-back mean and L2-flushed median."""
     import torch
     stream = torch.cuda.current_stream()
     st = build_state(name, device, identity_tables=identity_tables)
     wl, t = st["wl"], st["t"]
-    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, 0, device)
+    ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, 0, device,
+                           shared=shared)
     plan = pkv.DecodePlan(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"], st["lens"],
-                          wl.scale, key=t["key"], value=t["value"], workspace=ws, status=st["status"])
+                          wl.scale, key=t["key"], value=t["value"], workspace=ws, status=st["status"],
+                          shared_blocks=st["shared"] if shared else None)
     for _ in range(5):
         plan.launch()
     b2b = time_launches(plan.launch, reps, stream)
@@ -587,7 +607,7 @@ def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False):
          "kv_bytes": kv, "GB_s": round(kv / mean_us / 1e3, 1), "frac": round(kv / mean_us / 1e3 / peak, 4),
          "GB_s_l2_flushed": round(kv / med_us / 1e3, 1), "frac_l2_flushed": round(kv / med_us / 1e3 / peak, 4),
          "seqs_per_s": round(wl.num_seqs / mean_us * 1e6, 1),
-         "traffic": None if identity_tables else recorded_traffic(name)}
+         "traffic": None if identity_tables else recorded_traffic(name + ("_shared" if shared else ""))}
     if name == "prefix":
         u = unique_kv_bytes(st["tables"].cpu().numpy(), wl.context_lens, wl.block_size, wl.num_kv_heads,
                             wl.head_dim)
@@ -670,6 +690,9 @@ def run_secondary(pkv, device, peak, st_main, ws_main, reps=50):
                   "frac_l2_flushed": round(kv / statistics.median(fl) / 1e6 / peak, 4)}}
     for name in ("chat", "gqa", "prefix"):
         res[name] = measure_decode(pkv, name, device, peak, reps, flush)
+    # the prefix workload again, its shared prompt read once per group of 8
+    # forks (paged_attention_decode_shared)
+    res["prefix_shared"] = measure_decode(pkv, "prefix", device, peak, reps, flush, shared=True)
     ident = measure_decode(pkv, "7b", device, peak, reps, flush, identity_tables=True)
     shuf = res["7b"]["decode_us_mean"]
     res["paging_overhead_7b"] = {
@@ -707,9 +730,10 @@ def run_pkv(args):
     if not args.two_launch:
         st["fused"] = True
         st["launches_per_step"] -= 1
+    st["use_shared"] = args.shared
     wl = st["wl"]
     ws = pkv.new_workspace(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.block_size,
-                           args.num_ctas, device)
+                           args.num_ctas, device, shared=args.shared)
     kv_bytes = wl.kv_read_bytes()
     clocks = ClockSampler(local_rank)
 
@@ -792,7 +816,7 @@ def run_pkv(args):
     value = world * kv_bytes * args.steps / (ms_total / 1e3) / 1e9
     achieved = kv_bytes / (dec_mean / 1e3) / 1e9
     # the ncu record was taken on the default launch of the default inputs
-    traffic = recorded_traffic(args.config) if default_launch else None
+    traffic = recorded_traffic(args.config + ("_shared" if args.shared else "")) if default_launch else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -830,7 +854,11 @@ def run_pkv(args):
         "host_us_per_step": round(host_s / args.steps * 1e6, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("pkv_paged_attention_decode (paged_decode_kernel, merge fused)" if args.two_launch
+                     "kernel": (("pkv_paged_attention_decode_shared (paged_decode_kernel, grouped: shared "
+                                 "blocks read once per group of forks" + ("" if args.two_launch else
+                                                                          ", writes the new tokens") + ")")
+                                if args.shared else
+                                "pkv_paged_attention_decode (paged_decode_kernel, merge fused)" if args.two_launch
                                 else "pkv_paged_attention_decode_append (paged_decode_kernel: writes the new "
                                      "tokens, merge fused)"),
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"

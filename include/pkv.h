@@ -272,10 +272,11 @@ void pkv_decode_plan_destroy(pkv_decode_plan_t *plan);
  * Up to 8 consecutive sequences that share blocks form a group; the group's
  * shared full blocks (never the block of a member's last token) are read
  * once for all of them, with the members' queries as the rows of one
- * tensor-core tile, and each member's remaining blocks on its own.  The two
- * parts of a member's row are merged in a fixed order, so results are
- * run-to-run deterministic for a fixed grid; they agree with the plain decode
- * within rounding (not bit for bit).  The grouped kernel serves group 1
+ * tensor-core tile, then each member's own blocks with only its row live.
+ * Results are run-to-run deterministic for a fixed grid and agree with the
+ * plain decode within rounding (not bit for bit).  On a batch without
+ * sharing the plain calls are faster (the grouped kernel keeps 8 rows per
+ * segment): pass the hints where forks share blocks.  The grouped kernel serves group 1
  * (num_heads == num_kv_heads), block sizes 16 to 128 and up to 1024
  * sequences; other calls run the plain kernel (shared_blocks is then not
  * read).  The workspace is pkv_decode_workspace_size_shared(...) bytes, and

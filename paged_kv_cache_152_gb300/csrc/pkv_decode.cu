@@ -216,7 +216,7 @@ size_t workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_di
     if (resolve(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_ctas, &r, grouped) != PKV_OK)
         return 0;
     return DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas,
-                                 grouped ? kGroupRows : num_heads / num_kv_heads, head_dim, grouped)
+                                 grouped ? kGroupRows : num_heads / num_kv_heads, head_dim)
         .total;
 }
 
@@ -273,7 +273,7 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     if (rc != PKV_OK) return rc;
     const int group = num_heads / num_kv_heads;
     const DecodeWorkspace ws = DecodeWorkspace::plan(num_seqs, num_kv_heads, r.workers, r.ctas,
-                                                     grouped ? kGroupRows : group, head_dim, grouped);
+                                                     grouped ? kGroupRows : group, head_dim);
     if (workspace_bytes < ws.total) return PKV_ERR_INVALID_ARG;
     unsigned char *wsb = static_cast<unsigned char *>(workspace);
 
@@ -310,9 +310,6 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.ws_count = reinterpret_cast<unsigned long long *>(wsb + ws.count);
     p.status = dev_status;
     p.shared_blocks = grouped ? shared_blocks : nullptr;
-    p.ws_sh = grouped ? reinterpret_cast<float *>(wsb + ws.sh) : nullptr;
-    p.ws_pv = grouped ? reinterpret_cast<float *>(wsb + ws.pv) : nullptr;
-    p.ws_fc = grouped ? reinterpret_cast<unsigned long long *>(wsb + ws.fc) : nullptr;
     p.num_seqs = num_seqs;
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;

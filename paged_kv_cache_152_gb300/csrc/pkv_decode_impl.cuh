@@ -108,8 +108,9 @@ struct DecodeGeometry {
 // Dynamic shared memory (from a 1024-byte aligned base):
 // [stages][query + new-row slots][barriers][chunk meta][cum (N+1)][ctx (N)][bounds (C+1)]
 // [partial slots (optional): NW workers x 2 (first / last piece) x G x (2 + D) fp32].
-// (grouped kernel: [ctx (N)][shared (N)][cum (2N+1)] padded to 8 bytes, then
-// [item (2N) int2][bounds (C+1)] -- 32 bytes per sequence)
+// (grouped kernel: [ctx (N)][shared (N)][cum over items] padded to 8 bytes,
+// then [items int2][bounds (C+1)]; items are at most N, the arrays have room
+// for 2N -- 32 bytes per sequence)
 template <int NW, int ST, int D, int BS, int G, bool GRP = false>
 struct DecodeSmem {
     using Geo = DecodeGeometry<D, BS, G>;
@@ -145,10 +146,13 @@ __device__ __forceinline__ void zero_tail_rows(unsigned char *vt, int R, int lan
 // rows 2t, 2t+1 (+8) of the scores; the output is kept transposed, O^T
 // [dims x heads]: o[i] holds dims 16i + g and 16i + g + 8 of heads 2t and
 // 2t + 1 (o[i][0] / o[i][2] head 2t, o[i][1] / o[i][3] head 2t + 1).
-template <int D, int BS, int G>
+// MASK (the grouped kernel): when live >= 0 only query row `live` sees this
+// chunk -- the other rows' scores are masked, and a row that has seen no key
+// of its piece yet keeps its empty state (max -inf, sum 0, output 0).
+template <int D, int BS, int G, bool MASK = false>
 __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, const uint32_t (&qa)[D / 16][2],
                                               float scale_log2, float &m, float &l, float (&o)[D / 16][4],
-                                              int lane) {
+                                              int lane, int live = -1) {
     using Geo = DecodeGeometry<D, BS, G>;
     const int t = lane & 3;
     const int mi = lane >> 3;   // which 8x8 matrix this lane addresses in ldmatrix
@@ -192,18 +196,21 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     // ---- online softmax (per query head; rows past R masked) ----------------
     float x[Geo::kNT][2];
     float mx = -CUDART_INF_F;
+    const bool row_live = !MASK || live < 0 || (lane >> 2) == live;  // this lane's query row
 #pragma unroll
     for (int nt = 0; nt < Geo::kNT; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int row = 8 * nt + 2 * t + j;
-            x[nt][j] = row < R ? s[nt][j] * scale_log2 : -CUDART_INF_F;
+            x[nt][j] = row < R && row_live ? s[nt][j] * scale_log2 : -CUDART_INF_F;
             mx = fmaxf(mx, x[nt][j]);
         }
     mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, 2));
-    const float mn = fmaxf(m, mx);          // row 0 is valid: finite
-    const float corr = exp2f(m - mn);       // m = -inf at a piece's start -> 0
+    const float mn = fmaxf(m, mx);          // row 0 is valid: finite (MASK: a masked row may stay -inf)
+    // the exponents' reference: mn, or 0 while the row is still empty (MASK)
+    const float mref = MASK ? (mn == -CUDART_INF_F ? 0.f : mn) : mn;
+    const float corr = exp2f(m - mref);     // m = -inf at a piece's start -> 0
     m = mn;
     l *= corr;
     // the output columns are heads 2t and 2t + 1: their factors come from
@@ -222,7 +229,7 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     for (int nt = 0; nt < Geo::kNT; ++nt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            pr[nt][j] = exp2f(x[nt][j] - mn);  // masked rows: exp2(-inf) = 0
+            pr[nt][j] = exp2f(x[nt][j] - mref);  // masked rows: exp2(-inf) = 0
             l += pr[nt][j];
         }
     // P as A fragments: hi = fp16(p), lo = fp16(p - hi)
@@ -400,11 +407,8 @@ struct WorkerCtx {
     float *part;             // partial slots of this CTA's workers (shared), or NULL
     int64_t lo, len;         // this CTA's range [lo, lo + len)
     int r0, r1;              // chunks its first / last worker give up (cta_share_start)
-    // grouped kernel only (else NULL): sequences' contexts, the items, and
-    // this call's per-(sequence, KV head) counters of the two parts
-    const int *ctx;
+    // grouped kernel only (else NULL): the items (groups and lone sequences)
     const int2 *info;
-    unsigned long long *fc;
 
     // first chunk of worker w, one of this CTA's workers or the next CTA's first
     __device__ __forceinline__ int64_t start(int64_t w) const {
@@ -477,7 +481,9 @@ __device__ __forceinline__ PieceRef cta_piece(const DecodeParams &p, int64_t c, 
 //     M' = max(M, m_p),  X' = X 2^(M - M') + x_p 2^(m_p - M')  for X = L, O.
 // Lane j holds output dims j*PER .. j*PER + PER - 1 of every head; M and L
 // are the same on all lanes.
-template <int D, int G>
+// SAFE (the grouped kernel): a row may be empty (max -inf) in both the state
+// and the piece; the exponents are then taken against 0 and nothing changes.
+template <int D, int G, bool SAFE = false>
 struct MergeState {
     static constexpr int PER = D / 32;
     float M[G], L[G], O[G][PER];
@@ -507,8 +513,9 @@ struct MergeState {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const float mn = fmaxf(M[g], ml[g].x);
-            const float f_old = exp2f(M[g] - mn);
-            const float f_new = exp2f(ml[g].x - mn);
+            const float mref = SAFE ? (mn == -CUDART_INF_F ? 0.f : mn) : mn;
+            const float f_old = exp2f(M[g] - mref);
+            const float f_new = exp2f(ml[g].x - mref);
             L[g] = L[g] * f_old + ml[g].y * f_new;
 #pragma unroll
             for (int k = 0; k < PER; ++k) O[g][k] = O[g][k] * f_old + a[g][k] * f_new;
@@ -542,8 +549,8 @@ struct MergeState {
 
 // Folds pieces 0 .. cnt-1 (ref(i) -> PieceRef) into st, in order, one round
 // trip per piece: for a few pieces, or for pieces in shared memory.
-template <int D, int G, class Ref>
-__device__ __forceinline__ void merge_seq(MergeState<D, G> &st, int cnt, Ref ref, int lane) {
+template <int D, int G, bool SAFE, class Ref>
+__device__ __forceinline__ void merge_seq(MergeState<D, G, SAFE> &st, int cnt, Ref ref, int lane) {
 #pragma unroll 1
     for (int i = 0; i < cnt; ++i) {
         const PieceRef r = ref(i);
@@ -555,8 +562,8 @@ __device__ __forceinline__ void merge_seq(MergeState<D, G> &st, int cnt, Ref ref
 // to 32 pieces at a time, lane j fetches piece j's (m, l) -- one round trip
 // for all of them -- the warp reduces M and L with shuffles, then sums the
 // output slices in piece order with the loads of several pieces in flight.
-template <int D, int G, class Ref>
-__device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref ref, int lane) {
+template <int D, int G, bool SAFE, class Ref>
+__device__ __forceinline__ void merge_wide(MergeState<D, G, SAFE> &st, int cnt, Ref ref, int lane) {
     constexpr int PER = D / 32;
     constexpr int U = G >= 8 ? 1 : (G >= 4 ? 2 : 4 / G);  // pieces whose slices are loaded together
 #pragma unroll 1
@@ -575,9 +582,10 @@ __device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref re
             float mx = ml.x;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
-            const float mn = fmaxf(st.M[g], mx);  // some piece exists: finite
-            const float f_old = exp2f(st.M[g] - mn);
-            wgt[g] = mine.exists ? exp2f(ml.x - mn) : 0.f;
+            const float mn = fmaxf(st.M[g], mx);  // some piece exists: finite (SAFE: maybe -inf)
+            const float mref = SAFE ? (mn == -CUDART_INF_F ? 0.f : mn) : mn;
+            const float f_old = exp2f(st.M[g] - mref);
+            wgt[g] = mine.exists ? exp2f(ml.x - mref) : 0.f;
             float ls = ml.y * wgt[g];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(kFullMask, ls, o);
@@ -615,88 +623,42 @@ __device__ __forceinline__ void merge_wide(MergeState<D, G> &st, int cnt, Ref re
 // ---- the grouped (prefix-sharing) kernel ----------------------------------
 // The caller tells, per sequence, how many leading blocks its table shares
 // with the previous sequence's.  Up to 8 consecutive sequences that share
-// blocks form a group; the work is cut into ITEMS instead of sequences: a
-// group's shared full blocks, read once with the members' queries as the rows
-// of one segment (group 1: one query row per member, like the heads of a
-// group-8 segment), then every member's own remaining chunks.  A member's
-// output is the merge of its two parts: each part is stored in its slot and
-// counted in on the member's counter, and whichever completes the count
-// folds them (shared part first, then its own) and writes the row.
-// Sequences outside groups are items of their own, written as usual.
+// blocks form a GROUP, and a group is one segment owner (an item) instead of
+// its sequences: for each KV head its chunks are the group's shared full
+// blocks, read once with every member's query as a row of the tile, then each
+// member's own chunks in member order, during which only that member's row
+// is live (the others' scores are masked, their softmax state untouched).
+// Row g of the segment is then exactly member g's decode over its whole
+// context, and it completes, splits across workers and merges like a head of
+// a group-8 segment.  A sequence outside every group is an item of its own.
+constexpr int kOwn = 32;         // chunk flag: a member's own chunk (one live row)
+constexpr int kMemberShift = 6;  // ... and which member, in the next 3 flag bits
+
 struct ItemInfo {
     int s0;  // first (or only) sequence
-    int ns;  // sequences: >= 2 for a group's shared part
-    int c0;  // the item's first chunk within the sequence
+    int ns;  // sequences (members)
+    int sc;  // shared chunks at the start of every KV head's segment
 };
 __device__ __forceinline__ ItemInfo item_info(const int2 *info, int it) {
     const int2 v = info[it];
     return {v.x & 0xffff, v.x >> 16, v.y};
 }
 
-// The slot of sequence s's part over its group's shared blocks (shared) or
-// over its own chunks: (max, sum) then the D unnormalised outputs.
-template <int D>
-__device__ __forceinline__ float *part_slot(const DecodeParams &p, bool shared, int s, int kvh) {
-    return (shared ? p.ws_sh : p.ws_pv) + ((int64_t)s * p.num_kv_heads + kvh) * (2 + D);
-}
-
-// After item `it`'s rows were stored in their part slots: count each row's
-// chunks in on its sequence's counter; every sequence whose count is then
-// complete gets its two parts merged, in a fixed order, and its row written.
-template <int D, int NW>
-__device__ __forceinline__ void settle_parts(const DecodeParams &p, const WorkerCtx<NW> &wc, int it, int kvh,
-                                             int lane) {
-    const ItemInfo ii = item_info(wc.info, it);
-    const int amount = (wc.cum[it + 1] - wc.cum[it]) / p.num_kv_heads;
-    fence_acq_rel_gpu();  // the parts are visible device-wide before they are counted
-    __syncwarp();
-    bool last = false;
-    if (lane < ii.ns) {
-        const int sq = ii.s0 + lane;
-        const int total = chunks_for(wc.ctx[sq], 16);
-        last = count_in_tagged(wc.fc + (int64_t)sq * p.num_kv_heads + kvh, wc.epoch, total, amount) == total;
-    }
-    unsigned mask = __ballot_sync(kFullMask, last);
-    if (mask == 0) return;
-    fence_acq_rel_gpu();
-    while (mask) {
-        const int g = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int sq = ii.s0 + g;
-        float *a = part_slot<D>(p, true, sq, kvh);
-        float *b = part_slot<D>(p, false, sq, kvh);
-        MergeState<D, 1> ms;
-        ms.init();
-        ms.add(PieceRef{a, a + 2, false, true}, lane);
-        ms.add(PieceRef{b, b + 2, false, true}, lane);
-        ms.write_out(p, sq, kvh, lane);
-    }
-}
-
-// The result of item `it` after a merge (lane j holds dims j*D/32 ... of each
-// row): a sequence's whole output row, or the parts of the item's sequences.
-template <int D, int G, int NW>
-__device__ __forceinline__ void emit_merged_grp(const DecodeParams &p, const WorkerCtx<NW> &wc,
-                                                const MergeState<D, G> &ms, int it, int kvh, int lane) {
+// Output rows g < ns of item `it`'s segment for KV head kvh, from a merge
+// (lane j holds dims j*D/32 ... of every row): row g is member g's output.
+template <int D, int G, bool SAFE>
+__device__ __forceinline__ void write_rows_grp(const DecodeParams &p, const ItemInfo &ii, int kvh,
+                                               const MergeState<D, G, SAFE> &ms, int lane) {
     constexpr int PER = D / 32;
-    const ItemInfo ii = item_info(wc.info, it);
-    if (ii.ns == 1 && ii.c0 == 0) {
-        __half *dst = p.out + ((int64_t)ii.s0 * p.num_heads + kvh) * D + lane * PER;
-        const float inv = 1.f / ms.L[0];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(ms.O[0][k] * inv);
-        return;
-    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         if (g < ii.ns) {
-            float *slot = part_slot<D>(p, ii.ns > 1, ii.s0 + g, kvh);
-            if (lane == 0) *reinterpret_cast<float2 *>(slot) = make_float2(ms.M[g], ms.L[g]);
+            __half *dst = p.out + ((int64_t)(ii.s0 + g) * p.num_heads + kvh) * D + lane * PER;
+            const float inv = 1.f / ms.L[g];
 #pragma unroll
-            for (int k = 0; k < PER; ++k) slot[2 + lane * PER + k] = ms.O[g][k];
+            for (int k = 0; k < PER; ++k) dst[k] = __float2half_rn(ms.O[g][k] * inv);
         }
     }
-    settle_parts<D, NW>(p, wc, it, kvh, lane);
 }
 
 // Finish a piece: sum l over the 4 lanes of each head, then write the output
@@ -721,32 +683,17 @@ __device__ __forceinline__ bool finish_piece(const DecodeParams &p, const Worker
         return (g & 1) ? make_float2(y, own_o) : make_float2(own_e, y);
     };
     if constexpr (GRP) {
-        // a whole item: a sequence's output row (row 0), or its rows' parts
-        const ItemInfo ii = item_info(wc.info, s);
-        if ((flags & kWhole) && !(ii.ns == 1 && ii.c0 == 0)) {
-            float *dst = part_slot<D>(p, ii.ns > 1, ii.s0 + (hh < ii.ns ? hh : 0), kvh) + 2 + d0;
+        if (flags & kWhole) {
+            // a whole segment of a group (or of a lone sequence): row hh is
+            // member hh's output row
+            const ItemInfo ii = item_info(wc.info, s);
+            const float inv = 1.f / __shfl_sync(kFullMask, l, 4 * hh);  // l of row hh
+            __half *dst = p.out + ((int64_t)(ii.s0 + (hh < ii.ns ? hh : 0)) * p.num_heads + kvh) * D + d0;
 #pragma unroll
             for (int i = 0; i < D / 16; ++i) {
                 const float2 a = pair(o[i][0], o[i][1]);
                 const float2 b = pair(o[i][2], o[i][3]);
                 if (hh < ii.ns) {
-                    *reinterpret_cast<float2 *>(dst + 16 * i) = a;
-                    *reinterpret_cast<float2 *>(dst + 16 * i + 8) = b;
-                }
-            }
-            if (t == 0 && g < ii.ns)
-                *reinterpret_cast<float2 *>(part_slot<D>(p, ii.ns > 1, ii.s0 + g, kvh)) = make_float2(m, l);
-            settle_parts<D, NW>(p, wc, s, kvh, lane);
-            return false;
-        }
-        if (flags & kWhole) {
-            const float inv = 1.f / __shfl_sync(kFullMask, l, 0);  // l of row 0
-            __half *dst = p.out + ((int64_t)ii.s0 * p.num_heads + kvh) * D + d0;
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-                const float2 a = pair(o[i][0], o[i][1]);
-                const float2 b = pair(o[i][2], o[i][3]);
-                if (hh == 0) {
                     *reinterpret_cast<uint32_t *>(dst + 16 * i) = pack_half2(a.x * inv, a.y * inv);
                     *reinterpret_cast<uint32_t *>(dst + 16 * i + 8) = pack_half2(b.x * inv, b.y * inv);
                 }
@@ -865,16 +812,16 @@ __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCt
         r.exists = st < wc.start(w + 1);
         return r;
     };
-    MergeState<D, G> ms;
+    MergeState<D, G, GRP> ms;
     ms.init();
     const int cnt = (int)(wb - wa + 1);
     if (cnt <= 4 || wc.part != nullptr)
-        merge_seq<D, G>(ms, cnt, wref, lane);
+        merge_seq(ms, cnt, wref, lane);
     else
-        merge_wide<D, G>(ms, cnt, wref, lane);
+        merge_wide(ms, cnt, wref, lane);
     if (si.local) {
         if constexpr (GRP)
-            emit_merged_grp<D, G, NW>(p, wc, ms, s, kvh, lane);
+            write_rows_grp(p, item_info(wc.info, s), kvh, ms, lane);
         else
             ms.write_out(p, s, kvh, lane);
         return;
@@ -895,14 +842,14 @@ __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCt
         r.exists = wc.bounds[c] < wc.bounds[c + 1];
         return r;
     };
-    MergeState<D, G> ms2;
+    MergeState<D, G, GRP> ms2;
     ms2.init();
     if (cb - ca < 4)
-        merge_seq<D, G>(ms2, cb - ca + 1, cref, lane);
+        merge_seq(ms2, cb - ca + 1, cref, lane);
     else
-        merge_wide<D, G>(ms2, cb - ca + 1, cref, lane);
+        merge_wide(ms2, cb - ca + 1, cref, lane);
     if constexpr (GRP)
-        emit_merged_grp<D, G, NW>(p, wc, ms2, s, kvh, lane);
+        write_rows_grp(p, item_info(wc.info, s), kvh, ms2, lane);
     else
         ms2.write_out(p, s, kvh, lane);
 }
@@ -1077,8 +1024,9 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         // Each sequence's group (the leader and its members, up to 8
         // consecutive sequences of one chain) and the shared full blocks P:
         // at most the blocks every member shares with its predecessor, and
-        // never the block of a member's last token.  Items per sequence: a
-        // group's leader opens the shared item, then every member has its own.
+        // never the block of a member's last token.  A group (P >= 1) is one
+        // item; its chunks per KV head: the P shared blocks', then every
+        // member's own.
         auto group_of = [&](int s, int cs, int &lead, int &ns, int &shared_chunks) {
             lead = cs + ((s - cs) & ~7);
             ns = 1;
@@ -1098,7 +1046,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                 if (shv[s] == 0) cs = s;
                 int lead, ns, sc;
                 group_of(s, cs, lead, ns, sc);
-                nitems += (sc > 0 && s == lead) ? 2 : 1;
+                nitems += sc > 0 ? (s == lead ? 1 : 0) : 1;
                 nchunks += Hkv * (chunks_for(ctx[s], Geo::kRows) - (sc > 0 && s != lead ? sc : 0));
             }
         }
@@ -1140,15 +1088,13 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                 if (shv[s] == 0) cs = s;
                 int lead, ns, sc;
                 group_of(s, cs, lead, ns, sc);
-                if (sc > 0 && s == lead) {
-                    info[item] = make_int2(lead | (ns << 16), 0);
+                // a group's leader opens its item (its members' own chunks follow
+                // inside it); a lone sequence is an item of its own
+                if (sc == 0 || s == lead) {
+                    info[item] = sc > 0 ? make_int2(lead | (ns << 16), sc) : make_int2(s | (1 << 16), 0);
                     cum[item++] = run;
-                    run += Hkv * sc;
                 }
-                const int c0s = sc > 0 ? sc : 0;
-                info[item] = make_int2(s | (1 << 16), c0s);
-                cum[item++] = run;
-                run += Hkv * (chunks_for(ctx[s], Geo::kRows) - c0s);
+                run += Hkv * (chunks_for(ctx[s], Geo::kRows) - (sc > 0 && s != lead ? sc : 0));
             }
         }
         if (tid == 0) cum[NI] = total;
@@ -1206,27 +1152,35 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     // its descriptor is built), 0 past the share
     // (at block size 8 a chunk spans two blocks: the second entry comes in the
     // high half, 0 when the chunk does not reach it)
-    // the sequence and the chunk within it of a segment owner's chunk (the
-    // grouped kernel's items start at chunk c0 of their first sequence, whose
-    // table row a group's shared blocks are read through)
-    auto owner_seq = [&](int it) -> int {
-        if constexpr (GRP) return info[it].x & 0xffff;
-        return it;
+    // Where chunk c (of nch) of a segment owned by `it` lies: its sequence,
+    // the chunk within that sequence, whether it is the sequence's last, and
+    // (grouped) the member whose own chunk it is (-1: all rows see it).
+    struct Where {
+        int seq, lc, member;
+        bool last;
     };
-    auto owner_c0 = [&](int it) -> int {
-        if constexpr (GRP) return info[it].y;
-        return 0;
-    };
-    auto owner_rows = [&](int it) -> int {  // query rows of the owner's segments (grouped: its sequences)
-        if constexpr (GRP) return info[it].x >> 16;
-        return G;
+    auto where = [&](int it, int c, int nch) -> Where {
+        if constexpr (!GRP) {
+            return {it, c, -1, c == nch - 1};
+        } else {
+            const ItemInfo ii = item_info(info, it);
+            if (c < ii.sc) return {ii.s0, c, -1, false};
+            int r = c - ii.sc, j = 0;
+            int own = chunks_for(ctx[ii.s0], Geo::kRows) - ii.sc;
+            while (j < ii.ns - 1 && r >= own) {
+                r -= own;
+                ++j;
+                own = chunks_for(ctx[ii.s0 + j], Geo::kRows) - ii.sc;
+            }
+            return {ii.s0 + j, ii.sc + r, ii.ns > 1 ? j : -1, r == own - 1};
+        }
     };
     auto table_entry_at = [&](const ChunkPos &q) -> int2 {
-        const int sq = owner_seq(q.s);
-        const int lb = chunk_block(owner_c0(q.s) + q.c, BS, Geo::kRows);
-        const int32_t *row = p.block_tables + (int64_t)sq * p.max_blocks_per_seq;
+        const Where w = where(q.s, q.c, q.nch);
+        const int lb = chunk_block(w.lc, BS, Geo::kRows);
+        const int32_t *row = p.block_tables + (int64_t)w.seq * p.max_blocks_per_seq;
         int second = 0;
-        if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[sq]) second = __ldg(row + lb + 1);
+        if (Geo::kBPC == 2 && (lb + 1) * BS < ctx[w.seq]) second = __ldg(row + lb + 1);
         return make_int2(__ldg(row + lb), second);
     };
     auto table_entry = [&](int i) -> int2 {
@@ -1236,7 +1190,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     const bool append = p.new_key != nullptr;
     // Descriptor of the chunk at walk position i, built by one lane for a
     // window of 32 positions at a time (lane j: position win + j) from its
-    // table entry `tab`: x = sequence | KV head << 16, y = rows | flags << 8,
+    // table entry `tab`: x = segment owner | KV head << 16, y = rows | flags << 8,
     // z / w = the cache row of its box (of each block's box at block size 8).
     // Issuing a chunk is then a few shuffles and the copies.
     auto chunk_desc_at = [&](int64_t g, const ChunkPos &q, int2 tab) -> int4 {
@@ -1249,14 +1203,15 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             report(p.status, PKV_ERR_OUT_OF_RANGE);
             phys2 = 0;
         }
-        const int lc = owner_c0(q.s) + q.c;  // the chunk within its sequence
-        const int rows = chunk_rows(lc, ctx[owner_seq(q.s)], Geo::kRows);
-        // the decode step's new token is the last row of the segment's last
+        const Where w = where(q.s, q.c, q.nch);
+        const int rows = chunk_rows(w.lc, ctx[w.seq], Geo::kRows);
+        // the decode step's new token is the last row of its sequence's last
         // chunk (never in a group's shared blocks: they stop before it)
-        const bool new_row = append && q.c == q.nch - 1 && owner_rows(q.s) == (GRP ? 1 : G);
-        const int flags = chunk_flags(q, g, gb, ge) | (new_row ? kAppendRow : 0);
+        const bool new_row = append && w.last;
+        const int flags = chunk_flags(q, g, gb, ge) | (new_row ? kAppendRow : 0) |
+                          (w.member >= 0 ? kOwn | (w.member << kMemberShift) : 0);
         // row of the cache viewed as [num_blocks * Hkv * BS rows]
-        const int y = (int)(((int64_t)phys * Hkv + q.kvh) * BS + (lc * Geo::kRows) % BS);
+        const int y = (int)(((int64_t)phys * Hkv + q.kvh) * BS + (w.lc * Geo::kRows) % BS);
         const int y2 = (int)(((int64_t)phys2 * Hkv + q.kvh) * BS);
         return make_int4(q.s | (q.kvh << 16), rows | (flags << 8), y, y2);
     };
@@ -1305,9 +1260,17 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         const int y = __shfl_sync(kFullMask, desc.z, j);
         const int y2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, desc.w, j) : 0;
         if (lane == 0) {
-            const int s = owner_seq(sk & 0xffff), kvh = sk >> 16;
-            const int nq = owner_rows(sk & 0xffff);  // grouped: the item's sequences, one query row each
+            const int it = sk & 0xffff, kvh = sk >> 16;
             const int rows = rf & 0xff, flags = rf >> 8;
+            // the query rows' first sequence and count (grouped: the members,
+            // one row each), and the sequence whose new token a chunk carries
+            int s = it, nq = G, snew = it;
+            if constexpr (GRP) {
+                const ItemInfo ii = item_info(info, it);
+                s = ii.s0;
+                nq = ii.ns;
+                snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
+            }
             const bool new_row = (flags & kAppendRow) != 0;
             const int stage = i % ST;
             const uint32_t bar = bar_a + stage * 8;
@@ -1319,7 +1282,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             // (the second lands 8 rows down, at +1 KB in each half)
             const bool short_box = Geo::kBPC == 2 || rows <= 8;
             const bool second = Geo::kBPC == 2 && rows > 8;
-            wmeta[2 * stage] = make_int4(sk & 0xffff, kvh, rows, flags);  // x: the segment's owner
+            wmeta[2 * stage] = make_int4(it, kvh, rows, flags);  // x: the segment's owner
             wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
             mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
                                                   : 2 * Geo::kTileBytes) +
@@ -1350,7 +1313,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                 }
             }
             if (new_row) {
-                const int64_t src = ((int64_t)s * Hkv + kvh) * D;
+                const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
                 bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
                 bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes + Geo::kRowBytes, p.new_value + src,
                          Geo::kRowBytes, bar);
@@ -1377,21 +1340,12 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     __syncthreads();  // the ranges are visible to every warp's merges
     epoch = __shfl_sync(kFullMask, epoch, 0);
     const int parity = epoch & 1;
-    // (the grouped kernel has up to 2 items per sequence, and per (sequence,
-    // KV head) counters of the two parts besides)
-    const int64_t nseg = (int64_t)(GRP ? 2 * N : N) * Hkv;
-    unsigned long long *count_now = p.ws_count + (int64_t)parity * nseg;
-    unsigned long long *fc_now = GRP ? p.ws_fc + (int64_t)parity * N * Hkv : nullptr;
+    unsigned long long *count_now = p.ws_count + (int64_t)parity * N * Hkv;
     {
-        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * nseg;
+        unsigned long long *count_next = p.ws_count + (int64_t)(parity ^ 1) * N * Hkv;
         const unsigned long long next_tag = (unsigned long long)(epoch + 1) << 32;
-        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < nseg; i += (int64_t)C * NW * 32)
+        for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)C * NW * 32)
             count_next[i] = next_tag;
-        if constexpr (GRP) {
-            unsigned long long *fc_next = p.ws_fc + (int64_t)(parity ^ 1) * N * Hkv;
-            for (int64_t i = (int64_t)blockIdx.x * NW * 32 + tid; i < (int64_t)N * Hkv; i += (int64_t)C * NW * 32)
-                fc_next[i] = next_tag;
-        }
         if (blockIdx.x == 0 && tid == 0) p.ws_sync[1 + (parity ^ 1)] = next_tag;
     }
     // rows of empty contexts are zero; no worker visits them
@@ -1413,7 +1367,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
     const WorkerCtx<NW> wc{cum, bounds, C, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
-                           c_lo, c_len, r0, r1, ctx, info, fc_now};
+                           c_lo, c_len, r0, r1, info};
 
     // the CTA's merge queue (count_piece / merge_part)
     auto vload = [](const int *a) { return *reinterpret_cast<const volatile int *>(a); };
@@ -1509,7 +1463,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             } else {
                 // query rows of the group as mma A fragments (rows g >= G stay 0;
                 // grouped: rows past the item's sequences too)
-                const int nq = GRP ? owner_rows(md.x) : G;
+                int nq = G;
+                if constexpr (GRP) nq = item_info(info, md.x).ns;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     qa[kk][0] =
@@ -1554,7 +1509,8 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             consume_chunk_cc<D>(wst + stage * Geo::kStageBytes, wst + stage * Geo::kStageBytes + Geo::kTileBytes,
                                 md.z, qc, p.scale_log2, m, l, oc, lane);
         else
-            consume_chunk<D, BS, G>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane);
+            consume_chunk<D, BS, G, GRP>(kt, kt + Geo::kTileBytes, md.z, qa, p.scale_log2, m, l, o, lane,
+                                         (GRP && (md.w & kOwn)) ? (md.w >> kMemberShift) & 7 : -1);
         // refill the stage first: a piece's finish (and a cut piece's count and
         // merge) then overlaps the copies in flight instead of draining the ring
         __syncwarp();

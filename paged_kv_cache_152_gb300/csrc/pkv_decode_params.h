@@ -37,11 +37,9 @@ struct DecodeParams {
     unsigned long long *ws_sync;  // [3]
     unsigned long long *ws_count; // [2][N*Hkv]
     int32_t *status;              // nullable
-    // grouped (prefix-sharing) kernel only, else NULL:
-    const int32_t *shared_blocks; // [N] leading blocks sequence s shares with s - 1 (the caller's hint)
-    float *ws_sh;                 // [N * Hkv][2 + D] a sequence's partial over its group's shared blocks
-    float *ws_pv;                 // [N * Hkv][2 + D] ... over its own remaining blocks
-    unsigned long long *ws_fc;    // [2][N * Hkv] per (sequence, KV head): chunks of both parts counted in
+    // grouped (prefix-sharing) kernel only, else NULL: the leading blocks
+    // sequence s shares with s - 1 (the caller's hint), [N]
+    const int32_t *shared_blocks;
     int num_seqs;
     int num_heads;
     int num_kv_heads;
@@ -55,27 +53,21 @@ struct DecodeParams {
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
-// group = query rows per segment (8 for the grouped kernel); grouped: the
-// segment counters cover up to 2 items per sequence, and the two per-sequence
-// partials and their counters follow.
+// group = query rows per segment (8 for the grouped kernel, whose segments'
+// owners -- groups and lone sequences -- are at most num_seqs).
 struct DecodeWorkspace {
-    size_t sync, count, ml, acc, cml, cacc, sh, pv, fc, total;
+    size_t sync, count, ml, acc, cml, cacc, total;
     static DecodeWorkspace plan(int num_seqs, int num_kv_heads, int64_t workers, int64_t ctas, int group,
-                                int head_dim, bool grouped = false) {
+                                int head_dim) {
         auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-        const size_t segs = (size_t)(grouped ? 2 : 1) * num_seqs * num_kv_heads;
-        const size_t pairs = (size_t)num_seqs * num_kv_heads;
         DecodeWorkspace w;
         w.sync = 0;
         w.count = 256;
-        w.ml = w.count + up(2 * 8 * segs);
+        w.ml = w.count + up(2 * 8 * (size_t)num_seqs * num_kv_heads);
         w.acc = w.ml + up(4 * (size_t)workers * 2 * group * 2);
         w.cml = w.acc + up(4 * (size_t)workers * 2 * group * head_dim);
         w.cacc = w.cml + up(4 * (size_t)ctas * 2 * group * 2);
-        w.sh = w.cacc + up(4 * (size_t)ctas * 2 * group * head_dim);
-        w.pv = w.sh + (grouped ? up(4 * pairs * (2 + head_dim)) : 0);
-        w.fc = w.pv + (grouped ? up(4 * pairs * (2 + head_dim)) : 0);
-        w.total = w.fc + (grouped ? up(2 * 8 * pairs) : 0);
+        w.total = w.cacc + up(4 * (size_t)ctas * 2 * group * head_dim);
         return w;
     }
 };
