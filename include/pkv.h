@@ -53,10 +53,9 @@
  *   - Base pointers of the caches, query, key, value and out must be 16-byte
  *     aligned (torch allocations are 256-byte aligned).
  *   - Calls launch on the calling thread's current CUDA device, which must be
- *     the one that holds their device pointers.  Use one device per process:
- *     each decode kernel's dynamic shared-memory limit is raised once per
- *     process, so a decode call on a second device of the same process may
- *     fail with PKV_ERR_CUDA (an error status, never a fault).
+ *     the one that holds their device pointers.  Several devices in one process
+ *     are fine (each decode kernel's dynamic shared-memory limit is raised per
+ *     device); a plan, like any call, runs on the device it was created on.
  */
 #ifndef PKV_H
 #define PKV_H

@@ -84,22 +84,35 @@ bool shape_supported(int num_heads, int num_kv_heads, int head_dim, int block_si
     return decode_kernel_info(head_dim, num_heads / num_kv_heads, block_size, &info);
 }
 
-// Raises the kernel's dynamic shared-memory limit to `smem` if needed.
+// Raises the kernel's dynamic shared-memory limit to `smem` on the current
+// device if needed.  The attribute is held per device, so what was raised is
+// remembered per (device, kernel).
 int ensure_smem_attr(const void *fn, size_t smem) {
+    constexpr int kSlots = 512;
     static std::mutex mu;
-    static const void *fns[128];
-    static size_t set[128];
-    static int nfns = 0;
+    static const void *fns[kSlots];
+    static int devs[kSlots];
+    static size_t set[kSlots];
+    static int n = 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(mu);
     int k = 0;
-    while (k < nfns && fns[k] != fn) ++k;
-    if (k < nfns && set[k] >= smem) return PKV_OK;
+    while (k < n && !(fns[k] == fn && devs[k] == dev)) ++k;
+    if (k < n && set[k] >= smem) return PKV_OK;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
-    if (k == nfns && nfns < 128) fns[nfns++] = fn;
-    if (k < 128) set[k] = smem;
+    if (k == n && n < kSlots) {
+        fns[n] = fn;
+        devs[n] = dev;
+        ++n;
+    }
+    if (k < kSlots) set[k] = smem;
     return PKV_OK;
 }
 
