@@ -497,31 +497,33 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
 
 
 def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, steps):
-    """Where an e2e step's time goes: the same serving step with its parts
-    issued as separate operations (the H2D copy of the staging region, the
-    plan's launch, the D2H copy of the output), CUDA events between them,
-    host clocks around the submission, the block manager's work for the next
-    step and the wait.  Untimed for the e2e value; medians in microseconds."""
+    """Where an e2e step's time goes: the same serving step through the same
+    library call (pkv_decode_plan_step: the staged inputs in, the launch, the
+    output out), then the step's launch once more on its own, CUDA events
+    around both; host clocks around the submission, the block manager's work
+    for the next step and the wait.  Untimed for the e2e value; medians in
+    microseconds.  device_in_and_out_us = the step's device time minus the
+    kernel's."""
     import torch
     if steps <= 0:
         return None
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     host = {"submit": [], "block_manager": [], "wait_after_block_manager": [], "step_wall": []}
     sh = stream.cuda_stream
     n_rows = len(h_rows)
+    step_bytes = d_stage.numel()
+    d_ptr = d_stage.data_ptr()
+    out_ptr = h_out.data_ptr() if h_out is not None else None
     prepare(0)
     done = torch.cuda.Event()
     for j in range(steps):
         i = j % n_rows
         ta = time.perf_counter()
         ev[j][0].record(stream)
-        d_stage.copy_(h_rows[i], non_blocking=True)
+        plan.step_raw(d_ptr, h_rows[i].data_ptr(), step_bytes, out_ptr, sh)
         ev[j][1].record(stream)
-        plan.launch_raw(sh)
+        plan.launch_raw(sh)  # the same launch again, alone (rewrites the same new rows)
         ev[j][2].record(stream)
-        if h_out is not None:  # (else the kernel has written the host buffer itself)
-            h_out.copy_(d_out, non_blocking=True)
-        ev[j][3].record(stream)
         done.record(stream)
         tb = time.perf_counter()
         if j + 1 < steps:
@@ -536,18 +538,17 @@ def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, s
         host["step_wall"].append(td - ta)
     torch.cuda.synchronize()
     med = lambda xs: round(statistics.median(xs) * 1e6, 2)  # noqa: E731
-    dev = {"h2d": [e[0].elapsed_time(e[1]) / 1e3 for e in ev], "kernel": [e[1].elapsed_time(e[2]) / 1e3 for e in ev],
-           "d2h": [e[2].elapsed_time(e[3]) / 1e3 for e in ev]}
-    out = {f"device_{k}_us": med(v) for k, v in dev.items()}
+    step = [e[0].elapsed_time(e[1]) / 1e3 for e in ev]
+    kern = [e[1].elapsed_time(e[2]) / 1e3 for e in ev]
+    out = {"device_step_us": med(step), "device_kernel_us": med(kern),
+           "device_in_and_out_us": med([a - b for a, b in zip(step, kern)])}
     out.update({f"host_{k}_us": med(v) for k, v in host.items()})
-    gpu = [a + b + c for a, b, c in zip(dev["h2d"], dev["kernel"], dev["d2h"])]
-    out["outside_device_work_us"] = med([w - g for w, g in zip(host["step_wall"], gpu)])
+    out["outside_device_work_us"] = med([w - a - b for w, a, b in zip(host["step_wall"], step, kern)])
     out["steps"] = steps
-    out["how"] = ("the parts of the step as separate calls (torch H2D copy of the staging region, the plan's "
-                  "launch, and a torch D2H copy of the output only when the kernel does not write the host "
-                  "buffer itself) with CUDA events between them; host clocks around the "
-                  "submission, the next step's block-manager work and the wait; outside_device_work_us = wall "
-                  "time of the step minus its three device intervals")
+    out["how"] = ("each step: pkv_decode_plan_step (staged inputs in, the launch, the output out) between CUDA "
+                  "events, then the same launch alone between events; host clocks around the submission, the "
+                  "next step's block-manager work and the wait; outside_device_work_us = wall time minus both "
+                  "device intervals")
     return out
 
 

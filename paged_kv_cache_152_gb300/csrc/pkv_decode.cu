@@ -29,6 +29,8 @@ struct pkv_decode_plan {
 
 namespace pkv {
 
+bool stage_in_by_kernel(void *dev_dst, const void *host_src, size_t bytes, cudaStream_t stream);  // pkv_stage.cu
+
 #define PKV_DECLARE_INFO(d, g) bool decode_kernel_info_d##d##_g##g(int, DecodeKernelInfo *);
 PKV_DECLARE_INFO(64, 1)
 PKV_DECLARE_INFO(64, 2)
@@ -497,7 +499,10 @@ extern "C" int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in,
                                     size_t in_bytes, void *host_out, pkv_stream_t stream) {
     if (!plan || (in_bytes && (!dev_in || !host_in))) return PKV_ERR_INVALID_ARG;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (in_bytes && cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    // mapped page-locked input: copied by a kernel reading it over the link
+    // (one wave of 16-byte loads), else by a copy engine
+    if (in_bytes && !stage_in_by_kernel(dev_in, host_in, in_bytes, s) &&
+        cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }
