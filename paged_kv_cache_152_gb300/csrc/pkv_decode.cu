@@ -199,7 +199,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // The cache as a 3-D tensor: 64 dims (innermost), num_blocks * Hkv *
 // block_size rows (stride head_dim * 2 bytes), head_dim / 64 halves (stride
 // 128 bytes), read with the 128-byte swizzle in boxes of {64, box_rows,
-// box_halves}: a box lands in shared memory as [half][row][64 dims].
+// box_halves}: a box lands in shared memory as [half][row][64 dims].  No L2
+// promotion: a box is one contiguous run of whole 128-byte lines already,
+// and widening the requests measured ~1% slower (7b 96.1 against 94.8 us).
 int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int block_size,
                      int head_dim, int box_rows, int box_halves) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -211,7 +213,7 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int nu
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(cache), dims, strides,
                               box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
