@@ -405,18 +405,17 @@ struct WorkerCtx {
     int *cta_count;          // per-worker-slot counters of this CTA (shared)
     int *cta_cross;          // counter of the segment that reaches in from before this CTA (shared)
     float *part;             // partial slots of this CTA's workers (shared), or NULL
-    int64_t lo, len;         // this CTA's range [lo, lo + len)
-    int r0, r1;              // chunks its first / last worker give up (cta_share_start)
+    const int64_t *starts;   // this CTA's NW + 1 worker starts (shared; the last is its range's end)
     // grouped kernel only (else NULL): the items (groups and lone sequences)
     const int2 *info;
 
     // first chunk of worker w, one of this CTA's workers or the next CTA's first
     __device__ __forceinline__ int64_t start(int64_t w) const {
-        return cta_share_start(lo, len, NW, (int)(w - (int64_t)blockIdx.x * NW), r0, r1);
+        return starts[w - (int64_t)blockIdx.x * NW];
     }
-    // this CTA's worker whose share holds chunk g (lo <= g < lo + len)
+    // this CTA's worker whose share holds chunk g (inside the CTA's range)
     __device__ __forceinline__ int64_t worker_of(int64_t g) const {
-        return (int64_t)blockIdx.x * NW + worker_in_cta<NW>(lo, len, g, r0, r1);
+        return (int64_t)blockIdx.x * NW + worker_in_starts<NW>(starts, g);
     }
 };
 
@@ -926,6 +925,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         bounds = reinterpret_cast<int64_t *>(smem + Smem::kCum + (((size_t)(2 * N + 1) * 4 + 7) & ~(size_t)7));
     }
     __shared__ int cta_count[NW];
+    __shared__ int64_t worker_starts[NW + 1];
     __shared__ int exit_count;
     __shared__ int cta_cross;
     __shared__ MergeQueue mq;
@@ -1118,7 +1118,6 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     if ((int)blockIdx.x >= C) return;
     const int64_t wid = (int64_t)blockIdx.x * NW + warp;
     int64_t gb, ge, c_lo, c_len;
-    int r0, r1;
     {
         // lane 0: the CTA range's start, lane 1: its end (and whether each
         // cuts a segment)
@@ -1128,10 +1127,16 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         c_lo = __shfl_sync(kFullMask, v, 0);
         c_len = __shfl_sync(kFullMask, v, 1) - c_lo;
         const int r = cut_relief_for(cuts, c_len, NW, kRelief, kReliefDiv);
-        r0 = __shfl_sync(kFullMask, r, 0);
-        r1 = __shfl_sync(kFullMask, r, 1);
-        gb = cta_share_start(c_lo, c_len, NW, warp, r0, r1);
-        ge = cta_share_start(c_lo, c_len, NW, warp + 1, r0, r1);
+        const int r0 = __shfl_sync(kFullMask, r, 0);
+        const int r1 = __shfl_sync(kFullMask, r, 1);
+        // lane 0 this warp's start, lane 1 its end
+        const int64_t st = cta_share_start(c_lo, c_len, NW, warp + (lane & 1), r0, r1);
+        gb = __shfl_sync(kFullMask, st, 0);
+        ge = __shfl_sync(kFullMask, st, 1);
+        // the CTA's worker starts, looked up by the merges (after the barrier
+        // that follows the first copies)
+        if (lane == 0) worker_starts[warp] = gb;
+        if (lane == 0 && warp == NW - 1) worker_starts[NW] = ge;
     }
     const int n = gb < ge ? (int)(ge - gb) : 0;
 
@@ -1367,7 +1372,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     if (p.smem_partials)
         part = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(bounds + C + 1) + 15) & ~(uintptr_t)15);
     const WorkerCtx<NW> wc{cum, bounds, C, wid, gb, ge, epoch, count_now, cta_count, &cta_cross, part,
-                           c_lo, c_len, r0, r1, info};
+                           worker_starts, info};
 
     // the CTA's merge queue (count_piece / merge_part)
     auto vload = [](const int *a) { return *reinterpret_cast<const volatile int *>(a); };

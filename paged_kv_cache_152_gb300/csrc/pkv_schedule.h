@@ -168,13 +168,6 @@ PKV_HD int64_t snapped_cta_start(const int *cum, int n, int num_kv_heads, int64_
     return nominal;
 }
 
-// First chunk of worker w given the CTA bounds.
-PKV_HD int64_t worker_start2(const int64_t *bounds, int nw, int64_t w) {
-    const int64_t c = w / nw, k = w % nw;
-    const int64_t a = bounds[c], len = bounds[c + 1] - a;
-    return a + (k * len) / nw;
-}
-
 // Start of worker k (0 <= k <= nw) of a CTA whose range is [a, a + len):
 // equal shares, except that the first worker gives up r0 chunks and the last
 // r1, spread evenly over the workers between them (nw >= 3).  A worker whose
@@ -206,32 +199,15 @@ PKV_HD int cut_relief(const int *cum, int n, int num_kv_heads, int64_t b, int64_
     return cut_relief_for(locate_chunk(cum, n, num_kv_heads, b).c != 0, len, nw, relief, div);
 }
 
-// The worker k of that CTA (0 <= k < NW) whose share holds chunk g,
-// a <= g < a + len (the last one when empty shares start at g).
+// The worker k of a CTA (0 <= k < NW) whose share holds chunk g, given the
+// CTA's NW + 1 worker starts (the last one when empty shares start at g).
 template <int NW>
-PKV_HD int worker_in_cta(int64_t a, int64_t len, int64_t g, int r0, int r1) {
+PKV_HD int worker_in_starts(const int64_t *starts, int64_t g) {
     int k = 0;
-    for (int j = 1; j < NW; ++j) k += (cta_share_start(a, len, NW, j, r0, r1) <= g) ? 1 : 0;
+    for (int j = 1; j < NW; ++j) k += starts[j] <= g ? 1 : 0;
     return k;
 }
 
-// Largest w (of C*nw workers) with worker_start2(w) <= g, 0 <= g < T.
-PKV_HD int64_t worker_of2(const int64_t *bounds, int C, int nw, int64_t g) {
-    int lo = 0, hi = C;  // bounds[lo] <= g < bounds[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (bounds[mid] <= g) lo = mid; else hi = mid;
-    }
-    const int64_t a = bounds[lo], len = bounds[lo + 1] - a;
-    // largest k with (k * len) / nw <= g - a
-    const int64_t k = ((g - a + 1) * nw + len - 1) / len - 1;
-    return (int64_t)lo * nw + (k < nw - 1 ? k : nw - 1);
-}
-
-// worker_of2 without its 64-bit division, for a compile-time NW: look in CTA
-// `hint` first (where a caller's own segments usually are), else binary-search
-// the CTA, then count the CTA's worker starts at or below g.  Same result as
-// worker_of2.
 // The CTA whose range holds chunk g (0 <= g < T): `hint` when it does, else
 // the largest c with bounds[c] <= g.
 PKV_HD int cta_of(const int64_t *bounds, int C, int64_t g, int hint) {
@@ -242,15 +218,6 @@ PKV_HD int cta_of(const int64_t *bounds, int C, int64_t g, int hint) {
         if (bounds[mid] <= g) lo = mid; else hi = mid;
     }
     return lo;
-}
-
-template <int NW>
-PKV_HD int64_t worker_of_cta(const int64_t *bounds, int C, int64_t g, int hint) {
-    const int c = cta_of(bounds, C, g, hint);
-    const int64_t a = bounds[c], len = bounds[c + 1] - a;
-    int k = 0;
-    for (int j = 1; j < NW; ++j) k += (a + ((int64_t)j * len) / NW <= g) ? 1 : 0;
-    return (int64_t)c * NW + k;
 }
 
 // The order in which a worker walks its share [gb, ge): its cut pieces first

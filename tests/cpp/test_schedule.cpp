@@ -33,9 +33,9 @@ static void run_case(const std::vector<int> &ctx, int hkv, int bs, int sr, int m
 }
 
 template <int NW>
-static int worker_in_cta_rt(int nw, int64_t a, int64_t len, int64_t g, int r0, int r1) {
+static int worker_in_starts_rt(int nw, const int64_t *starts, int64_t g) {
     CHECK(nw == NW, "nw");
-    return worker_in_cta<NW>(a, len, g, r0, r1);
+    return worker_in_starts<NW>(starts, g);
 }
 
 static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr, int mb, int64_t W, int split,
@@ -106,25 +106,29 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
             }
         }
     }
+    // each CTA's worker starts, as the kernel's warps compute them (the
+    // merges look workers up in this array)
+    std::vector<int64_t> starts(split == 1 ? (size_t)C * (nw + 1) : 0);
+    for (int c = 0; split == 1 && c < C; ++c) {
+        const int64_t a = bounds[c], len = bounds[c + 1] - a;
+        for (int k = 0; k <= nw; ++k) {
+            starts[(size_t)c * (nw + 1) + k] = cta_share_start(a, len, nw, k, r0[c], r1[c]);
+            if (relief == 0)  // equal shares
+                CHECK(starts[(size_t)c * (nw + 1) + k] == a + (k * len) / nw, "equal share %d of cta %d", k, c);
+        }
+    }
     auto wstart = [&](int64_t w) -> int64_t {
         if (split == 0) return worker_start(w, W, T);
         if (w >= W) return T;
-        if (relief > 0) {
-            const int64_t c = w / nw;
-            return cta_share_start(bounds[c], bounds[c + 1] - bounds[c], nw, (int)(w % nw), r0[c], r1[c]);
-        }
-        return worker_start2(bounds.data(), nw, w);
+        return starts[(size_t)(w / nw) * (nw + 1) + w % nw];
     };
     auto wof = [&](int64_t g) -> int64_t {
         if (split == 0) return worker_of(g, W, T);
-        if (relief > 0) {
-            const int c = cta_of(bounds.data(), C, g, 0);
-            const int64_t a = bounds[c], len = bounds[c + 1] - a;
-            const int k = nw == 3 ? worker_in_cta_rt<3>(nw, a, len, g, r0[c], r1[c])
-                                  : worker_in_cta_rt<8>(nw, a, len, g, r0[c], r1[c]);
-            return (int64_t)c * nw + k;
-        }
-        return worker_of2(bounds.data(), C, nw, g);
+        const int c = cta_of(bounds.data(), C, g, 0);
+        const int64_t *st = starts.data() + (size_t)c * (nw + 1);
+        const int k = nw == 1 ? worker_in_starts_rt<1>(nw, st, g)
+                    : nw == 3 ? worker_in_starts_rt<3>(nw, st, g) : worker_in_starts_rt<8>(nw, st, g);
+        return (int64_t)c * nw + k;
     };
     // ranges partition [0, T)
     std::vector<int> owner(T, -1);
@@ -137,15 +141,11 @@ static void run_case_split(const std::vector<int> &ctx, int hkv, int bs, int sr,
         CHECK(owner[g] >= 0, "uncovered chunk %lld", (long long)g);
         CHECK(wof(g) == owner[g], "worker_of(%lld)=%lld want %d (split %d)", (long long)g, (long long)wof(g),
               owner[g], split);
-        if (split == 1 && relief == 0) {
-            // the constant-divisor search, from every hint CTA
+        if (split == 1) {
+            // the CTA look-up, from several hint CTAs
             for (int hint = 0; hint < C; hint += (C > 16 ? C / 7 : 1)) {
-                int64_t w2 = -1;
-                if (nw == 1) w2 = worker_of_cta<1>(bounds.data(), C, g, hint);
-                if (nw == 3) w2 = worker_of_cta<3>(bounds.data(), C, g, hint);
-                if (nw == 8) w2 = worker_of_cta<8>(bounds.data(), C, g, hint);
-                CHECK(w2 == owner[g], "worker_of_cta(%lld, hint %d)=%lld want %d", (long long)g, hint,
-                      (long long)w2, owner[g]);
+                const int c = cta_of(bounds.data(), C, g, hint);
+                CHECK(bounds[c] <= g && g < bounds[c + 1], "cta_of(%lld, hint %d)", (long long)g, hint);
             }
         }
         {
