@@ -24,12 +24,16 @@ every step (--no-graph: direct binding calls).
 * e2e: the same metric through the public API with host buffers: every step
   the C++ block manager appends one token per sequence and exports the tables
   into the step's pinned staging region (with its queries and new K/V rows);
-  one pkv_decode_plan_step call copies the region host->device, appends the
-  new tokens and attends, the kernel writing the output straight into a
-  pinned host buffer over the CPU-GPU link (--e2e-copy-out: a device->host
+  one pkv_decode_plan_step_mapped call launches the step, whose kernel reads
+  the region straight from host memory over the CPU-GPU link (the lengths and
+  tables in its prologue, each piece's query and each new row a few chunks
+  ahead of their use), appends the new tokens, attends and writes the output
+  straight into a pinned host buffer (--e2e-staged: pkv_decode_plan_step,
+  which first copies the region host->device; --e2e-copy-out: a device->host
   copy after the launch instead); the host waits
   for the step (polling an event); the next step's block-manager work
-  overlaps the GPU's work on this step.  20 untimed warm-up steps first; the
+  overlaps the GPU's work on this step; the staging region is a ring of 4
+  pinned rows (--e2e-ring).  20 untimed warm-up steps first; the
   line also gives the per-step wall-time percentiles.
 * roofline: the decode launch timed alone with CUDA events on its stream
   over the timed region; algorithmic bytes / mean duration vs the
@@ -98,6 +102,11 @@ def parse_args(argv=None):
                    help="override the workload's block size (8, 16, 32, 64, 128): the block-size sweep")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-ring", type=int, default=E2E_RING,
+                   help="e2e: pinned staging rows used in turn (0: one per step, each touched once)")
+    p.add_argument("--e2e-staged", action="store_true",
+                   help="e2e: pkv_decode_plan_step, which copies the staged inputs host->device before the launch "
+                        "(default: pkv_decode_plan_step_mapped, the kernel reads them from host memory)")
     p.add_argument("--e2e-copy-out", action="store_true",
                    help="e2e: the kernel writes device memory and a D2H copy brings the output back (default: "
                         "the kernel writes the pinned host buffer directly)")
@@ -364,21 +373,29 @@ def device_step(pkv, st, ws, num_ctas, ev=None):
 
 E2E_WARMUP = 20  # untimed serving steps before the timed ones (first-use costs on the host)
 E2E_BREAKDOWN = 50  # untimed steps after them, each part timed on its own
+E2E_RING = 4  # pinned staging rows, used in turn (a serving loop keeps a few; one fresh row per step
+#               costs the device first-touch misses on 350 MB of host pages: p90 step +40-110 us)
 
 
-def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_steps=0, copy_out=False):
+def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_steps=0, copy_out=False,
+            staged=False, ring=0):
     """Serving-loop steps through the public API with host buffers.
 
     Every step: the C++ block manager appends one token per sequence and
     exports the tables and lengths straight into the step's page-locked
     staging region, which also holds the step's queries and new K/V rows;
     copy-on-write pairs (if any) go through copy_blocks; then ONE library call
-    (pkv_decode_plan_step of a DecodePlan built once: append the new tokens +
-    attend) copies the region host->device and launches the step, whose
-    kernel writes the output into pinned host memory (copy_out: a D2H copy
-    follows); the stream is synchronised.  The
+    (pkv_decode_plan_step_mapped of a DecodePlan built once on a device
+    region of the staging layout: append the new tokens + attend) launches
+    the step, whose kernel reads the region from host memory and writes the
+    output into pinned host memory (staged: pkv_decode_plan_step copies the
+    region host->device first; copy_out: a D2H copy follows); the host waits
+    for the step.  The
     block-manager work of step i+1 runs on the host while the GPU runs step
-    i (as a serving loop schedules ahead)."""
+    i (as a serving loop schedules ahead).  The staging region has `ring`
+    rows used in turn (0: one row per step); the block manager rewrites a
+    row's tables and lengths every step, its queries and new rows were
+    drawn once."""
     import numpy as np
     import torch
     wl, alloc = st["wl"], st["alloc"]
@@ -392,19 +409,21 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
         off += -(-nbytes // 256) * 256
     step_bytes = off
     timed = steps
-    steps = warmup + timed  # every step has its own staging row
-    h_stage = torch.empty((steps, step_bytes), dtype=torch.uint8).pin_memory()
+    steps = warmup + timed
+    rows = ring if ring > 0 else steps  # staging rows, used in turn (default: one per step)
+    h_stage = torch.empty((rows, step_bytes), dtype=torch.uint8).pin_memory()
     rng = np.random.default_rng(wl.seed + 77)
     stage_np = h_stage.numpy()
     for name in ("q", "k", "v"):
         o, nbytes = offs[name]
-        stage_np[:, o:o + nbytes].view(np.float16)[:] = rng.standard_normal((steps, nbytes // 2)).astype(np.float16)
-    tab_np = [stage_np[i, offs["tables"][0]:offs["tables"][0] + offs["tables"][1]].view(np.int32).reshape(n, mb)
-              for i in range(steps)]
-    lens_np = [stage_np[i, offs["lens"][0]:offs["lens"][0] + offs["lens"][1]].view(np.int32) for i in range(steps)]
-    shared_np = [stage_np[i, offs["shared"][0]:offs["shared"][0] + offs["shared"][1]].view(np.int32)
+        stage_np[:, o:o + nbytes].view(np.float16)[:] = rng.standard_normal((rows, nbytes // 2)).astype(np.float16)
+    tab_np = [stage_np[i % rows, offs["tables"][0]:offs["tables"][0] + offs["tables"][1]].view(np.int32)
+              .reshape(n, mb) for i in range(steps)]
+    lens_np = [stage_np[i % rows, offs["lens"][0]:offs["lens"][0] + offs["lens"][1]].view(np.int32)
+               for i in range(steps)]
+    shared_np = [stage_np[i % rows, offs["shared"][0]:offs["shared"][0] + offs["shared"][1]].view(np.int32)
                  for i in range(steps)] if shared else None
-    h_rows = [h_stage[i] for i in range(steps)]
+    h_rows = [h_stage[i % rows] for i in range(steps)]
     d_stage = torch.empty(step_bytes, dtype=torch.uint8, device=device)
 
     def dview(name, dtype, shape):
@@ -435,6 +454,7 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     d_stage_ptr, h_out_ptr = d_stage.data_ptr(), (h_out.data_ptr() if copy_out else None)
     h_row_ptrs = [r.data_ptr() for r in h_rows]
     done = torch.cuda.Event()
+    step_fn = plan.step_raw if staged else plan.step_mapped_raw
     batch = np.asarray(wl.batch, dtype=np.int32)
     kv_per_token = 2 * hkv * d * 2
     bytes_total = 0
@@ -466,8 +486,9 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
             d_pairs[:len(pairs)].copy_(h_pairs_t[:len(pairs)], non_blocking=True)
             h2d += len(pairs) * 16 if timed_step else 0
             pkv.copy_blocks(t["key_cache"], t["value_cache"], d_pairs[:len(pairs)], status=st["status"])
-        # one library call: the region host -> device, the launch, the output device -> host
-        plan.step_raw(d_stage_ptr, h_row_ptrs[i], step_bytes, h_out_ptr, sh)
+        # one library call: the launch reading the region from host memory (staged: copied
+        # host -> device first), the output into host memory
+        step_fn(d_stage_ptr, h_row_ptrs[i], step_bytes, h_out_ptr, sh)
         if timed_step:
             bytes_total += int(lens_np[i].sum()) * kv_per_token
             h2d += step_bytes
@@ -488,22 +509,24 @@ def run_e2e(pkv, st, ws, num_ctas, steps, device, dist, warmup=0, breakdown_step
     marks.append(t_end)
     per = sorted(b - a for a, b in zip(marks, marks[1:]))
     pct = lambda q: round(per[min(len(per) - 1, int(q * len(per)))] * 1e6, 1)
-    breakdown = e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out if copy_out else None, st["out"],
-                              stream, breakdown_steps)
+    breakdown = e2e_breakdown(plan, step_fn, prepare, alloc, d_stage, h_rows, h_out if copy_out else None,
+                              st["out"], stream, breakdown_steps)
     plan.close()
     return {"bytes": bytes_total, "elapsed": elapsed, "h2d": h2d // timed, "d2h": d2h // timed,
             "step_us": {"p50": pct(0.5), "p90": pct(0.9), "max": round(per[-1] * 1e6, 1)},
             "breakdown": breakdown}
 
 
-def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, steps):
+def e2e_breakdown(plan, step_fn, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, steps):
     """Where an e2e step's time goes: the same serving step through the same
-    library call (pkv_decode_plan_step: the staged inputs in, the launch, the
-    output out), then the step's launch once more on its own, CUDA events
-    around both; host clocks around the submission, the block manager's work
-    for the next step and the wait.  Untimed for the e2e value; medians in
-    microseconds.  device_in_and_out_us = the step's device time minus the
-    kernel's."""
+    library call (step_fn: pkv_decode_plan_step_mapped, the launch reading the
+    inputs from host memory, or pkv_decode_plan_step, the staged inputs in
+    and the launch; then the output out), then the step's launch once more
+    on its own on the same inputs already in device memory (copied there
+    before the first event), CUDA events around both; host clocks around the
+    submission, the block manager's work for the next step and the wait.
+    Untimed for the e2e value; medians in microseconds.
+    device_in_and_out_us = the step's device time minus the kernel's."""
     import torch
     if steps <= 0:
         return None
@@ -518,9 +541,10 @@ def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, s
     done = torch.cuda.Event()
     for j in range(steps):
         i = j % n_rows
+        d_stage.copy_(h_rows[i], non_blocking=True)  # the same inputs in device memory for the launch alone
         ta = time.perf_counter()
         ev[j][0].record(stream)
-        plan.step_raw(d_ptr, h_rows[i].data_ptr(), step_bytes, out_ptr, sh)
+        step_fn(d_ptr, h_rows[i].data_ptr(), step_bytes, out_ptr, sh)
         ev[j][1].record(stream)
         plan.launch_raw(sh)  # the same launch again, alone (rewrites the same new rows)
         ev[j][2].record(stream)
@@ -545,9 +569,10 @@ def e2e_breakdown(plan, prepare, alloc, d_stage, h_rows, h_out, d_out, stream, s
     out.update({f"host_{k}_us": med(v) for k, v in host.items()})
     out["outside_device_work_us"] = med([w - a - b for w, a, b in zip(host["step_wall"], step, kern)])
     out["steps"] = steps
-    out["how"] = ("each step: pkv_decode_plan_step (staged inputs in, the launch, the output out) between CUDA "
-                  "events, then the same launch alone between events; host clocks around the submission, the "
-                  "next step's block-manager work and the wait; outside_device_work_us = wall time minus both "
+    out["how"] = ("each step: the e2e loop's library call (the launch reading its inputs from host memory, or "
+                  "the staged copy in and the launch; the output out) between CUDA events, then the same launch "
+                  "alone on the same inputs in device memory between events; host clocks around the submission, "
+                  "the next step's block-manager work and the wait; outside_device_work_us = wall time minus both "
                   "device intervals")
     return out
 
@@ -798,7 +823,8 @@ def run_pkv(args):
     e2e = None
     if e2e_steps:
         e2e = run_e2e(pkv, st, ws, args.num_ctas, e2e_steps, device, dist, warmup=E2E_WARMUP,
-                      breakdown_steps=E2E_BREAKDOWN, copy_out=args.e2e_copy_out)
+                      breakdown_steps=E2E_BREAKDOWN, copy_out=args.e2e_copy_out, staged=args.e2e_staged,
+                      ring=args.e2e_ring)
     clock_info = clocks.finish()
 
     # the secondary measurements: on the default run of one process only
@@ -876,10 +902,18 @@ def run_pkv(args):
                        "output": ("D2H copy after the launch" if args.e2e_copy_out else
                                   "written by the kernel straight into the pinned host buffer over the CPU-GPU "
                                   "link (the plan's out is mapped host memory); no copy after the launch"),
+                       "input": ("pkv_decode_plan_step: the region copied host->device, then the launch"
+                                 if args.e2e_staged else
+                                 "pkv_decode_plan_step_mapped: the kernel reads the region from pinned host memory "
+                                 "over the CPU-GPU link (no copy in)"),
+                       "staging": (f"{args.e2e_ring} pinned rows used in turn" if args.e2e_ring > 0 else
+                                   "one pinned row per step") +
+                                  " (tables and lengths rewritten by the block manager every step; queries and "
+                                  "new rows drawn once)",
                        "includes": "host block manager append + table export into the step's pinned staging "
-                                   "region (queries, new K/V, tables, lengths); one pkv_decode_plan_step call "
-                                   "per step: H2D copy of the region, the launch (append new tokens + attend), "
-                                   "the output into host memory; the host waits for each step (polling an event); "
+                                   "region (queries, new K/V, tables, lengths); one library call per step: the "
+                                   "region's bytes into the GPU, the launch (append new tokens + attend), the "
+                                   "output into host memory; the host waits for each step (polling an event); "
                                    "the next step's block-manager work overlaps this step's GPU work"}
     if secondary is not None:
         line["secondary"] = secondary

@@ -248,6 +248,33 @@ int pkv_decode_plan_launch(const pkv_decode_plan_t *plan, pkv_stream_t stream);
  */
 int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void *host_in, size_t in_bytes,
                          void *host_out, pkv_stream_t stream);
+
+/*
+ * pkv_decode_plan_step_mapped: one serving step whose inputs the kernel reads
+ * straight from page-locked host memory, with no copy in: every input pointer
+ * of the plan (query, key, value, block_tables, context_lens, shared_blocks)
+ * that lies in [dev_base, dev_base + in_bytes) is read at the same offset of
+ * host_in, over the CPU-GPU link; the others as created.  dev_base is only an
+ * address here (the region the plan was created on): it is neither read nor
+ * written.  The queries and new K/V rows are copied by the kernel's lanes 16
+ * bytes at a time, a few chunks ahead of their use, and the lengths and
+ * tables are read in its prologue.  Then the output goes to host_out as in
+ * pkv_decode_plan_step (NULL: none; a plan whose out is mapped host memory
+ * needs none).  Same results, bit for bit, as staging host_in into dev_base
+ * and launching.
+ *
+ *   host_in  page-locked host memory mapped for the current device
+ *            (cudaHostAlloc / cudaMallocHost with unified addressing, or
+ *            cudaHostRegisterMapped), in_bytes long, holding the inputs at
+ *            their offsets in the plan's region; query, key and value
+ *            16-byte aligned.  The caller must not write it until the
+ *            stream has passed the launch.
+ * PKV_ERR_INVALID_ARG for a NULL plan, in_bytes == 0, host_in that is not
+ * such memory (cudaPointerGetAttributes) or a misaligned input (nothing is
+ * enqueued); PKV_ERR_CUDA when the launch or the copy out fails to enqueue.
+ */
+int pkv_decode_plan_step_mapped(const pkv_decode_plan_t *plan, const void *dev_base, const void *host_in,
+                                size_t in_bytes, void *host_out, pkv_stream_t stream);
 void pkv_decode_plan_destroy(pkv_decode_plan_t *plan);
 
 /*

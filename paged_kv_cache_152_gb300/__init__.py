@@ -102,6 +102,7 @@ SIGNATURES = {
                                                _vp, _c_size, _vp, ctypes.POINTER(_vp)]),
     "pkv_decode_plan_launch": (_c_int, [_vp, _vp]),
     "pkv_decode_plan_step": (_c_int, [_vp, _vp, _vp, _c_size, _vp, _vp]),
+    "pkv_decode_plan_step_mapped": (_c_int, [_vp, _vp, _vp, _c_size, _vp, _vp]),
     "pkv_decode_plan_destroy": (None, [_vp]),
     "pkv_alloc_host_pool": (_c_int, [_vp, _c_int, _i32p]),
     "pkv_swap_out": (_c_int, [_vp, _i32p, _c_int, _i32p, _c_int, _intp]),
@@ -497,6 +498,32 @@ class DecodePlan:
                                                   _ptr(host_in) if nbytes else None, nbytes,
                                                   _ptr(host_out), _stream(stream)), "pkv_decode_plan_step")
         return host_out
+
+    def step_mapped(self, dev_base, host_in, host_out=None, stream=None):
+        """One serving step whose inputs the kernel reads straight from the
+        pinned host tensor host_in (pkv_decode_plan_step_mapped): each plan
+        input inside dev_base (the device region the plan was created on,
+        same byte size, not touched) is read at the same offset of host_in.
+        Then out -> host_out as in step().  The caller must not write host_in
+        until the stream has passed the launch."""
+        nbytes = host_in.numel() * host_in.element_size()
+        if host_in.is_cuda or not host_in.is_contiguous() or not dev_base.is_cuda or \
+                nbytes != dev_base.numel() * dev_base.element_size():
+            raise ValueError("host_in must be a contiguous pinned host tensor the byte size of dev_base")
+        if host_out is not None and (host_out.is_cuda or not host_out.is_contiguous() or
+                                     host_out.numel() * host_out.element_size() !=
+                                     self.out.numel() * self.out.element_size()):
+            raise ValueError("host_out must be a contiguous host tensor the size of out")
+        with self._guard(stream):
+            _check(self._lib.pkv_decode_plan_step_mapped(self._h, _ptr(dev_base), _ptr(host_in), nbytes,
+                                                         _ptr(host_out), _stream(stream)),
+                   "pkv_decode_plan_step_mapped")
+        return host_out
+
+    def step_mapped_raw(self, dev_base_ptr, host_in_ptr, nbytes, host_out_ptr, stream_handle):
+        """step_mapped() with raw pointers (ints) and a raw stream handle."""
+        _check(self._lib.pkv_decode_plan_step_mapped(self._h, dev_base_ptr, host_in_ptr, nbytes, host_out_ptr,
+                                                     stream_handle), "pkv_decode_plan_step_mapped")
 
     def step_raw(self, dev_in_ptr, host_in_ptr, nbytes, host_out_ptr, stream_handle):
         """step() with raw pointers (ints) and a raw stream handle, unchecked

@@ -12,6 +12,8 @@
 #include <mutex>
 #include <new>
 
+#include <type_traits>
+
 #include "../../include/pkv.h"
 #include "pkv_decode_impl.cuh"
 #include "pkv_launch.h"
@@ -335,6 +337,7 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.wait_limit_ns = kWaitLimitNs;
     p.smem_partials = r.smem_partials ? 1 : 0;
+    p.host_inputs = 0;  // pkv_decode_plan_step_mapped sets it on its copy
 
     plan->out_bytes = (size_t)num_seqs * num_heads * head_dim * 2;
     plan->fn = r.info.fn;
@@ -512,6 +515,49 @@ extern "C" int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in,
     if (rc != PKV_OK) return rc;
     if (host_out && plan->out_bytes &&
         cudaMemcpyAsync(host_out, plan->params.out, plan->out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+extern "C" int pkv_decode_plan_step_mapped(const pkv_decode_plan_t *plan, const void *dev_base, const void *host_in,
+                                           size_t in_bytes, void *host_out, pkv_stream_t stream) {
+    if (!plan || !dev_base || !host_in || in_bytes == 0) return PKV_ERR_INVALID_ARG;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, host_in) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return PKV_ERR_INVALID_ARG;
+    // every input inside the region moves to the same offset of the mapping
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(dev_base), hi = lo + in_bytes;
+    const intptr_t delta = reinterpret_cast<intptr_t>(attr.devicePointer) - static_cast<intptr_t>(lo);
+    DecodeParams prm = plan->params;
+    auto move = [&](auto &ptr) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+        if (ptr && a >= lo && a < hi) ptr = reinterpret_cast<std::remove_reference_t<decltype(ptr)>>(a + delta);
+    };
+    move(prm.query);
+    move(prm.new_key);
+    move(prm.new_value);
+    move(prm.block_tables);
+    move(prm.context_lens);
+    move(prm.shared_blocks);
+    auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    if (!aligned(prm.query) || (prm.new_key && (!aligned(prm.new_key) || !aligned(prm.new_value))))
+        return PKV_ERR_INVALID_ARG;
+    prm.host_inputs = 1;
+    if (!plan->empty) {
+        void *args[] = {&prm};
+        if (launch_pdl(plan->fn, dim3(plan->ctas), dim3(plan->threads), plan->smem, stream, args) != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+    }
+    if (host_out && plan->out_bytes &&
+        cudaMemcpyAsync(host_out, plan->params.out, plan->out_bytes, cudaMemcpyDeviceToHost,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
     }

@@ -977,7 +977,9 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     }
     if (lane == 31) warp_sums[warp] = incl;
     if (tid == 0) {
-        for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), 1);
+        // lane 0's arrival (with the copies' byte count); with host inputs
+        // also every lane's, after its 16-byte copies
+        for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), p.host_inputs ? 33 : 1);
         fence_barrier_init();
     }
     if (tid < NW) cta_count[tid] = 0;
@@ -1264,21 +1266,23 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         const int rf = __shfl_sync(kFullMask, desc.y, j);
         const int y = __shfl_sync(kFullMask, desc.z, j);
         const int y2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, desc.w, j) : 0;
+        const int it = sk & 0xffff, kvh = sk >> 16;
+        const int rows = rf & 0xff, flags = rf >> 8;
+        // the query rows' first sequence and count (grouped: the members,
+        // one row each), and the sequence whose new token a chunk carries
+        int s = it, nq = G, snew = it;
+        if constexpr (GRP) {
+            const ItemInfo ii = item_info(info, it);
+            s = ii.s0;
+            nq = ii.ns;
+            snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
+        }
+        const bool new_row = (flags & kAppendRow) != 0;
+        const int stage = i % ST;
+        const uint32_t bar = bar_a + stage * 8;
+        const uint32_t slot = wq_a + stage * Geo::kSlotBytes;
+        const bool lane_copies = p.host_inputs != 0;  // the query and new rows: the lanes' 16-byte copies
         if (lane == 0) {
-            const int it = sk & 0xffff, kvh = sk >> 16;
-            const int rows = rf & 0xff, flags = rf >> 8;
-            // the query rows' first sequence and count (grouped: the members,
-            // one row each), and the sequence whose new token a chunk carries
-            int s = it, nq = G, snew = it;
-            if constexpr (GRP) {
-                const ItemInfo ii = item_info(info, it);
-                s = ii.s0;
-                nq = ii.ns;
-                snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
-            }
-            const bool new_row = (flags & kAppendRow) != 0;
-            const int stage = i % ST;
-            const uint32_t bar = bar_a + stage * 8;
             const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
             const uint32_t vdst = kdst + Geo::kTileBytes;
             // a whole chunk inside one block is one box per cache; a last chunk
@@ -1289,10 +1293,11 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             const bool second = Geo::kBPC == 2 && rows > 8;
             wmeta[2 * stage] = make_int4(it, kvh, rows, flags);  // x: the segment's owner
             wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
+            const uint32_t side = lane_copies ? 0u
+                                              : ((flags & kFirst) ? (GRP ? nq * D * 2 : Geo::kQBytes) : 0) +
+                                                    (new_row ? 2 * Geo::kRowBytes : 0);
             mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
-                                                  : 2 * Geo::kTileBytes) +
-                                           ((flags & kFirst) ? (GRP ? nq * D * 2 : Geo::kQBytes) : 0) +
-                                           (new_row ? 2 * Geo::kRowBytes : 0));
+                                                  : 2 * Geo::kTileBytes) + side);
             if (!short_box) {
                 tma_load_3d(kdst, &p.tmap_k, 0, y, 0, bar);
                 tma_load_3d(vdst, &p.tmap_v, 0, y, 0, bar);
@@ -1307,22 +1312,45 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                     }
                 }
             }
-            if (flags & kFirst) {
+            if (!lane_copies && (flags & kFirst)) {
                 if constexpr (GRP) {
                     for (int j = 0; j < nq; ++j)
-                        bulk_g2s(wq_a + stage * Geo::kSlotBytes + j * D * 2,
-                                 p.query + ((int64_t)(s + j) * p.num_heads + kvh) * D, D * 2, bar);
+                        bulk_g2s(slot + j * D * 2, p.query + ((int64_t)(s + j) * p.num_heads + kvh) * D, D * 2,
+                                 bar);
                 } else {
-                    bulk_g2s(wq_a + stage * Geo::kSlotBytes, p.query + ((int64_t)s * p.num_heads + kvh * G) * D,
-                             Geo::kQBytes, bar);
+                    bulk_g2s(slot, p.query + ((int64_t)s * p.num_heads + kvh * G) * D, Geo::kQBytes, bar);
+                }
+            }
+            if (!lane_copies && new_row) {
+                const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
+                bulk_g2s(slot + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
+                bulk_g2s(slot + Geo::kQBytes + Geo::kRowBytes, p.new_value + src, Geo::kRowBytes, bar);
+            }
+        }
+        if (lane_copies) {
+            // inputs in host memory: the lanes copy them 16 bytes each, so that
+            // the link's latency is paid once per chunk, under the copies
+            // already in flight; every lane then arrives on the barrier when
+            // its copies have landed
+            constexpr int kVec = D / 8;  // 16-byte vectors per row
+            if (flags & kFirst) {
+                for (int v = lane; v < nq * kVec; v += 32) {
+                    const int r = v / kVec, c = v - r * kVec;
+                    const int64_t row = GRP ? (int64_t)(s + r) * p.num_heads + kvh
+                                            : (int64_t)s * p.num_heads + kvh * G + r;
+                    cp_async_16(slot + (r * D + c * 8) * 2, p.query + row * D + c * 8);
                 }
             }
             if (new_row) {
                 const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
-                bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
-                bulk_g2s(wq_a + stage * Geo::kSlotBytes + Geo::kQBytes + Geo::kRowBytes, p.new_value + src,
-                         Geo::kRowBytes, bar);
+                for (int v = lane; v < 2 * kVec; v += 32) {
+                    const bool is_v = v >= kVec;
+                    const int c = is_v ? v - kVec : v;
+                    cp_async_16(slot + Geo::kQBytes + (is_v ? Geo::kRowBytes : 0) + c * 16,
+                                (is_v ? p.new_value : p.new_key) + src + c * 8);
+                }
             }
+            cp_async_mbar_arrive_noinc(bar);
         }
     };
 

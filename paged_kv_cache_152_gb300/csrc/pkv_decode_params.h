@@ -50,6 +50,11 @@ struct DecodeParams {
     // 1: partials of segments cut between workers of one CTA are kept in the
     // CTA's shared memory (after the CTA bounds); 0: in ws_ml / ws_acc
     int smem_partials;
+    // 1: query, new_key and new_value may be page-locked host memory mapped
+    // for the device (a mapped plan step): the lanes copy them with 16-byte
+    // cp.async, each stage barrier counting every lane's arrival; 0: one bulk
+    // copy each, by lane 0
+    int host_inputs;
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.

@@ -95,6 +95,21 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// One thread's 16-byte copy global -> shared through the load path (any
+// global address, page-locked host memory mapped for the device included);
+// dst and src 16-byte aligned.  Completion is tracked with
+// cp_async_mbar_arrive_noinc.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The calling thread's arrival on the barrier, made when all its earlier
+// cp_async_16 copies have landed (it counts as one of the barrier's expected
+// arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Two-dimensional tensor copy global -> shared through a tensor map (TMA),
 // completing the box's bytes on the barrier.  x (innermost coordinate) times
 // the element size must be a multiple of 16 bytes.
