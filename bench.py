@@ -14,8 +14,12 @@ the whole context, in ONE launch (paged_attention_decode_append; split
 pieces are merged inside it).  --two-launch runs the write as its own
 reshape_and_cache launch before a read-only decode instead.  The workload
 has no copy-on-write pair at its decode step, so copy_blocks launches
-nothing.  The step's launches are captured once as CUDA graphs and replayed
-every step (--no-graph: direct binding calls).
+nothing.  The decode goes through a DecodePlan (validated once; each step is
+the launch alone) and the K timed steps go back to back on one stream, CUDA
+events only at the two ends of the timed region: with programmatic dependent
+launch each launch's prologue overlaps the previous launch's tail, as
+consecutive layers of a model step do (--no-graph: the binding's one-shot
+calls instead).
 
 * value: KV bytes the decode reads (2 * sum(ctx) * Hkv * D * 2) per step,
   times K steps, over the device-timed K steps (CUDA events, barrier +
@@ -118,7 +122,7 @@ def parse_args(argv=None):
                    help="reshape_and_cache, then a decode that only reads (instead of the decode launch "
                         "that writes the new tokens itself)")
     p.add_argument("--no-graph", action="store_true",
-                   help="launch every step directly instead of replaying captured CUDA graphs")
+                   help="every step through the binding's one-shot calls instead of a DecodePlan launch")
     p.add_argument("--shared", action="store_true",
                    help="decode through the prefix-sharing entry point (paged_attention_decode_shared) with the "
                         "block manager's shared-prefix hints")
@@ -596,6 +600,20 @@ def time_launches(fn, reps, stream, flush=None):
     return [a.elapsed_time(z) for a, z in ev]
 
 
+def period_launches(fn, reps, stream):
+    """Mean period (ms) of `reps` calls of fn() issued back to back, CUDA
+    events at the two ends only: with programmatic dependent launch each
+    launch's prologue overlaps the previous launch's tail."""
+    import torch
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    z.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(z) / reps
+
+
 def unique_kv_bytes(tables, lens, block_size, num_kv_heads, head_dim):
     """K+V bytes of the distinct physical blocks the tables reach (rows in
     use only): what a launch must bring from DRAM when blocks shared between
@@ -612,7 +630,9 @@ def unique_kv_bytes(tables, lens, block_size, num_kv_heads, head_dim):
 def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False, shared=False):
     """One workload's decode launch (the fused append + attend of the bench
     step, through a DecodePlan; shared: the prefix-sharing plan with the block
-    manager's hints): back-to-back mean and L2-flushed median."""
+    manager's hints): the mean of launches each between its own events, the
+    period of launches back to back (events at the ends only) and the
+    L2-flushed median."""
     import torch
     stream = torch.cuda.current_stream()
     st = build_state(name, device, identity_tables=identity_tables)
@@ -625,11 +645,14 @@ def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False, 
     for _ in range(5):
         plan.launch()
     b2b = time_launches(plan.launch, reps, stream)
+    per_us = period_launches(plan.launch, reps, stream) * 1e3
     fl = time_launches(plan.launch, reps, stream, flush)
     assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
     kv = wl.kv_read_bytes()
     mean_us, med_us = statistics.fmean(b2b) * 1e3, statistics.median(fl) * 1e3
-    r = {"decode_us_mean": round(mean_us, 2), "decode_us_median_l2_flushed": round(med_us, 2), "reps": reps,
+    r = {"decode_us_mean": round(mean_us, 2), "period_us_back_to_back": round(per_us, 2),
+         "GB_s_back_to_back": round(kv / per_us / 1e3, 1), "frac_back_to_back": round(kv / per_us / 1e3 / peak, 4),
+         "decode_us_median_l2_flushed": round(med_us, 2), "reps": reps,
          "kv_bytes": kv, "GB_s": round(kv / mean_us / 1e3, 1), "frac": round(kv / mean_us / 1e3 / peak, 4),
          "GB_s_l2_flushed": round(kv / med_us / 1e3, 1), "frac_l2_flushed": round(kv / med_us / 1e3 / peak, 4),
          "seqs_per_s": round(wl.num_seqs / mean_us * 1e6, 1),
@@ -696,7 +719,8 @@ def measure_cache_ops(pkv, device, peak, reps, flush):
 
 def run_secondary(pkv, device, peak, st_main, ws_main, reps=50):
     """The secondary measurements of the default run: the headline launch
-    with L2 flushed between repetitions; chat, gqa and prefix; identity
+    each between its own events, back to back, and with L2 flushed between
+    repetitions; the same for chat, gqa and prefix; identity
     against shuffled tables (the paging overhead); copy_blocks and
     reshape_and_cache."""
     import torch
@@ -707,10 +731,12 @@ def run_secondary(pkv, device, peak, st_main, ws_main, reps=50):
                           st_main["lens"], wl.scale, key=t["key"], value=t["value"], workspace=ws_main,
                           status=st_main["status"])
     b2b = time_launches(plan.launch, reps, stream)
+    per_us = period_launches(plan.launch, reps, stream) * 1e3
     fl = time_launches(plan.launch, reps, stream, flush)
     plan.close()
     kv = wl.kv_read_bytes()
     res = {"7b": {"decode_us_mean": round(statistics.fmean(b2b) * 1e3, 2),
+                  "period_us_back_to_back": round(per_us, 2),
                   "decode_us_median_l2_flushed": round(statistics.median(fl) * 1e3, 2), "reps": reps,
                   "GB_s_l2_flushed": round(kv / statistics.median(fl) / 1e6, 1),
                   "frac_l2_flushed": round(kv / statistics.median(fl) / 1e6 / peak, 4)}}
@@ -769,29 +795,31 @@ def run_pkv(args):
     torch.cuda.synchronize()
     assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
 
-    # the step as two CUDA graphs (cache write, decode): one graph launch each
-    # per step instead of the Python binding's per-call host work
+    # the step as launched in the timed region: the decode through a DecodePlan
+    # (validated once; each launch is the launch alone), after the step's
+    # cache-write calls when it has any (copy-on-write pairs; reshape_and_cache
+    # without the fused decode).  Steps go back to back on one stream: with
+    # programmatic dependent launch each launch's prologue and first table
+    # loads overlap the previous launch's tail, as consecutive layers of a
+    # model step do.  --no-graph: the binding's one-shot calls instead.
     stream = torch.cuda.current_stream()
-    graphs = None
+    sh = stream.cuda_stream
+    t = st["t"]
+    has_write = bool(st["pairs"].shape[0]) or not st.get("fused")
+    plan = None
     if not args.no_graph:
-        # (with the fused launch and no copy-on-write pairs there is no cache-write launch)
-        has_write = not (st.get("fused") and not st["pairs"].shape[0])
-        g_write, g_dec = (torch.cuda.CUDAGraph() if has_write else None), torch.cuda.CUDAGraph()
-        if has_write:
-            with torch.cuda.graph(g_write, capture_error_mode="relaxed"):
-                write_step(pkv, st)
-        with torch.cuda.graph(g_dec, capture_error_mode="relaxed"):
-            decode_step(pkv, st, ws, args.num_ctas)
-        graphs = (g_write, g_dec)
+        kw = dict(key=t["key"], value=t["value"]) if st.get("fused") else {}
+        plan = pkv.DecodePlan(st["out"], t["query"], t["key_cache"], t["value_cache"], st["tables"], st["lens"],
+                              wl.scale, num_ctas=args.num_ctas, workspace=ws, status=st["status"],
+                              shared_blocks=st["shared"] if st.get("use_shared") else None, **kw)
         for _ in range(3):
-            if g_write is not None:
-                g_write.replay()
-            g_dec.replay()
+            if has_write:
+                write_step(pkv, st)
+            plan.launch_raw(sh)
         torch.cuda.synchronize()
 
-    # timed region: K steps, device events, barrier + synchronize both sides
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    # timed region: K steps back to back, CUDA events at its two ends only,
+    # barrier + synchronize both sides
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize()
@@ -800,14 +828,12 @@ def run_pkv(args):
     e_start.record(stream)
     launches = 0
     for i in range(args.steps):
-        if graphs is None:
-            launches += device_step(pkv, st, ws, args.num_ctas, dec_ev[i])
+        if plan is None:
+            launches += device_step(pkv, st, ws, args.num_ctas)
         else:
-            if graphs[0] is not None:
-                graphs[0].replay()
-            dec_ev[i][0].record(stream)
-            graphs[1].replay()
-            dec_ev[i][1].record(stream)
+            if has_write:
+                write_step(pkv, st)
+            plan.launch_raw(sh)
             launches += st["launches_per_step"]
     e_stop.record(stream)
     host_s = time.perf_counter() - h0
@@ -815,10 +841,17 @@ def run_pkv(args):
     clocks.stop()
     barrier(dist, device)
     elapsed_ms = e_start.elapsed_time(e_stop)
-    dec_ms = [a.elapsed_time(b_) for a, b_ in dec_ev]
     assert int(st["status"].item()) == 0, pkv.status_string(int(st["status"].item()))
     ms_total = max_over_ranks(dist, elapsed_ms, device)
-    dec_mean = max_over_ranks(dist, statistics.fmean(dec_ms), device)
+    # the decode launch on its own (each between its own events: no overlap
+    # with a neighbour), for context beside the back-to-back period
+    iso = time_launches(plan.launch if plan is not None else (lambda: decode_step(pkv, st, ws, args.num_ctas)),
+                        min(50, max(5, args.steps)), stream)
+    dec_iso = max_over_ranks(dist, statistics.median(iso), device)
+    # the decode's average launch duration over the timed region: the period
+    # of the back-to-back launches when a step is the decode launch alone,
+    # else the launch on its own
+    dec_mean = ms_total / args.steps if st["launches_per_step"] == 1 else dec_iso
 
     e2e = None
     if e2e_steps:
@@ -874,7 +907,9 @@ def run_pkv(args):
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches * world,
         "launch_mode": ("direct binding calls" if args.no_graph else
-                        "CUDA graphs replayed per step") +
+                        "DecodePlan launches, steps back to back on one stream (programmatic dependent launch: "
+                        "each launch's prologue overlaps the previous launch's tail); CUDA events at the two ends "
+                        "of the timed region only") +
                        ("; reshape_and_cache launch, then a read-only decode launch" if args.two_launch
                         else "; one decode launch per step that also writes the new tokens "
                              "(paged_attention_decode_append)"),
@@ -891,7 +926,10 @@ def run_pkv(args):
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "decode_ms_mean": round(dec_mean, 5),
-                     "decode_ms_median": round(statistics.median(dec_ms), 5)},
+                     "duration": ("the launch period over the timed region (K launches back to back, events at "
+                                  "its ends)" if st["launches_per_step"] == 1 else
+                                  "the decode launch on its own, between its own events"),
+                     "decode_ms_isolated_median": round(dec_iso, 5)},
         "clocks": clock_info,
     }
     if e2e is not None:

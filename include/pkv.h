@@ -271,7 +271,9 @@ int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void
  *            stream has passed the launch.
  * PKV_ERR_INVALID_ARG for a NULL plan, in_bytes == 0, host_in that is not
  * such memory (cudaPointerGetAttributes) or a misaligned input (nothing is
- * enqueued); PKV_ERR_CUDA when the launch or the copy out fails to enqueue.
+ * enqueued); PKV_ERR_UNSUPPORTED if the library was built without the
+ * kernels that read host inputs; PKV_ERR_CUDA when the launch or the copy
+ * out fails to enqueue.
  */
 int pkv_decode_plan_step_mapped(const pkv_decode_plan_t *plan, const void *dev_base, const void *host_in,
                                 size_t in_bytes, void *host_out, pkv_stream_t stream);

@@ -22,6 +22,7 @@
 struct pkv_decode_plan {
     pkv::DecodeParams params;
     const void *fn = nullptr;
+    const void *fn_mapped = nullptr;  // the same launch reading its inputs with the lanes' copies
     int ctas = 0;
     int threads = 0;
     size_t smem = 0;
@@ -45,16 +46,38 @@ PKV_DECLARE_INFO(128, 8)
 #undef PKV_DECLARE_INFO
 bool decode_kernel_info_d64_grp(int, DecodeKernelInfo *);
 bool decode_kernel_info_d128_grp(int, DecodeKernelInfo *);
+#define PKV_DECLARE_MAPPED(d, g) const void *decode_kernel_fn_mapped_d##d##_g##g(int);
+PKV_DECLARE_MAPPED(64, 1)
+PKV_DECLARE_MAPPED(64, 2)
+PKV_DECLARE_MAPPED(64, 4)
+PKV_DECLARE_MAPPED(64, 8)
+PKV_DECLARE_MAPPED(128, 1)
+PKV_DECLARE_MAPPED(128, 2)
+PKV_DECLARE_MAPPED(128, 4)
+PKV_DECLARE_MAPPED(128, 8)
+#undef PKV_DECLARE_MAPPED
+const void *decode_kernel_fn_mapped_d64_grp(int);
+const void *decode_kernel_fn_mapped_d128_grp(int);
 
 bool decode_kernel_info_grouped(int head_dim, int block_size, DecodeKernelInfo *info) {
-    if (head_dim == 64) return decode_kernel_info_d64_grp(block_size, info);
-    if (head_dim == 128) return decode_kernel_info_d128_grp(block_size, info);
+    if (head_dim == 64 && decode_kernel_info_d64_grp(block_size, info)) {
+        info->fn_mapped = decode_kernel_fn_mapped_d64_grp(block_size);
+        return true;
+    }
+    if (head_dim == 128 && decode_kernel_info_d128_grp(block_size, info)) {
+        info->fn_mapped = decode_kernel_fn_mapped_d128_grp(block_size);
+        return true;
+    }
     return false;
 }
 
 bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInfo *info) {
-#define PKV_CASE(d, g) \
-    if (head_dim == d && group == g) return decode_kernel_info_d##d##_g##g(block_size, info);
+#define PKV_CASE(d, g)                                                              \
+    if (head_dim == d && group == g) {                                              \
+        if (!decode_kernel_info_d##d##_g##g(block_size, info)) return false;        \
+        info->fn_mapped = decode_kernel_fn_mapped_d##d##_g##g(block_size);          \
+        return true;                                                                \
+    }
     PKV_CASE(64, 1)
     PKV_CASE(64, 2)
     PKV_CASE(64, 4)
@@ -172,7 +195,8 @@ int resolve(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int blo
     // workspace holds them; same arithmetic either way)
     r->smem_partials = r->smem + r->info.smem_partials + 2 * 1024 <= (size_t)optin;
     if (r->smem_partials) r->smem += r->info.smem_partials;
-    const int rc = ensure_smem_attr(r->info.fn, r->smem);
+    int rc = ensure_smem_attr(r->info.fn, r->smem);
+    if (rc == PKV_OK && r->info.fn_mapped) rc = ensure_smem_attr(r->info.fn_mapped, r->smem);
     if (rc != PKV_OK) return rc;
     r->ctas = num_ctas;
     r->workers = (int64_t)num_ctas * r->info.warps;
@@ -337,10 +361,10 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     p.wait_limit_ns = kWaitLimitNs;
     p.smem_partials = r.smem_partials ? 1 : 0;
-    p.host_inputs = 0;  // pkv_decode_plan_step_mapped sets it on its copy
 
     plan->out_bytes = (size_t)num_seqs * num_heads * head_dim * 2;
     plan->fn = r.info.fn;
+    plan->fn_mapped = r.info.fn_mapped;
     plan->ctas = r.ctas;
     plan->threads = r.info.threads;
     plan->smem = r.smem;
@@ -547,10 +571,11 @@ extern "C" int pkv_decode_plan_step_mapped(const pkv_decode_plan_t *plan, const 
     auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (!aligned(prm.query) || (prm.new_key && (!aligned(prm.new_key) || !aligned(prm.new_value))))
         return PKV_ERR_INVALID_ARG;
-    prm.host_inputs = 1;
     if (!plan->empty) {
+        if (!plan->fn_mapped) return PKV_ERR_UNSUPPORTED;
         void *args[] = {&prm};
-        if (launch_pdl(plan->fn, dim3(plan->ctas), dim3(plan->threads), plan->smem, stream, args) != cudaSuccess) {
+        if (launch_pdl(plan->fn_mapped, dim3(plan->ctas), dim3(plan->threads), plan->smem, stream, args) !=
+            cudaSuccess) {
             cudaGetLastError();
             return PKV_ERR_CUDA;
         }

@@ -1,0 +1,6 @@
+// Decode kernels for head_dim 128, 8 query head(s) per KV head, reading their
+// query and new rows with the lanes' copies (the mapped plan step).
+#define PKV_D 128
+#define PKV_G 8
+#define PKV_MAPPED 1
+#include "pkv_decode_inst.cuh"

@@ -70,6 +70,11 @@
 //  * Rows past the context never reach the output: their scores are masked to
 //    -inf, and in a ragged chunk the warp zeroes those V rows in shared memory
 //    before P.V (whatever the cache holds there, 0 * it stays 0).
+//  * HOSTIN instantiations (the mapped plan step, whose query, new_key and
+//    new_value may be page-locked host memory) copy a piece's query and the
+//    new rows with the lanes' 16-byte cp.async instead of bulk copies, each
+//    stage barrier then counting lane 0's arrival and every lane's; the
+//    other instantiations' code is unchanged.
 //  * Every mbarrier wait gives up after wait_limit_ns, reports
 //    PKV_ERR_DEVICE_TIMEOUT, waits (again bounded) for the warp's copies in
 //    flight and returns.
@@ -853,6 +858,36 @@ __device__ __forceinline__ void merge_part(const DecodeParams &p, const WorkerCt
         ms2.write_out(p, s, kvh, lane);
 }
 
+// Inputs in page-locked host memory (a mapped plan step): the lanes copy a
+// piece's query rows (first chunk) and the new token's K and V rows into the
+// stage's slot 16 bytes each, so that the link's latency is paid once per
+// chunk under the copies already in flight, then every lane arrives on the
+// stage barrier when its copies have landed.  Only the HOSTIN instantiations
+// of the kernel (a mapped plan step) contain it.
+template <int D, int G, bool GRP>
+__device__ __forceinline__ void copy_host_inputs(const DecodeParams &p, uint32_t slot, uint32_t bar, bool first,
+                                              bool new_row, int s, int nq, int snew, int kvh, int lane) {
+    using Geo = DecodeGeometry<D, 16, G>;
+    constexpr int kVec = D / 8;  // 16-byte vectors per row
+    if (first) {
+        for (int v = lane; v < nq * kVec; v += 32) {
+            const int r = v / kVec, c = v - r * kVec;
+            const int64_t row = GRP ? (int64_t)(s + r) * p.num_heads + kvh : (int64_t)s * p.num_heads + kvh * G + r;
+            cp_async_16(slot + (r * D + c * 8) * 2, p.query + row * D + c * 8);
+        }
+    }
+    if (new_row) {
+        const int64_t src = ((int64_t)snew * p.num_kv_heads + kvh) * D;
+        for (int v = lane; v < 2 * kVec; v += 32) {
+            const bool is_v = v >= kVec;
+            const int c = is_v ? v - kVec : v;
+            cp_async_16(slot + Geo::kQBytes + (is_v ? Geo::kRowBytes : 0) + c * 16,
+                        (is_v ? p.new_value : p.new_key) + src + c * 8);
+        }
+    }
+    cp_async_mbar_arrive_noinc(bar);
+}
+
 // The CTA's merge queue (shared memory): segments whose CTA part is complete
 // and waits for merge_part.  At most NW + 1 parts complete in a CTA (a cut
 // segment holds a warp or CTA boundary of the range), so kMergeQueue entries
@@ -864,7 +899,7 @@ struct MergeQueue {
     int head;                // entries taken by consumers
 };
 
-template <int D, int BS, int G, int NW, int ST, bool GRP = false>
+template <int D, int BS, int G, int NW, int ST, bool GRP = false, bool HOSTIN = false>
 __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_constant__ DecodeParams p) {
 #ifdef PKV_DECODE_SNAP_CAP
     constexpr int kSnapCap = PKV_DECODE_SNAP_CAP;
@@ -979,7 +1014,7 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
     if (tid == 0) {
         // lane 0's arrival (with the copies' byte count); with host inputs
         // also every lane's, after its 16-byte copies
-        for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), p.host_inputs ? 33 : 1);
+        for (int i = 0; i < NW * ST; ++i) mbar_init(smem_addr(bars + i), HOSTIN ? 33 : 1);
         fence_barrier_init();
     }
     if (tid < NW) cta_count[tid] = 0;
@@ -1266,23 +1301,21 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         const int rf = __shfl_sync(kFullMask, desc.y, j);
         const int y = __shfl_sync(kFullMask, desc.z, j);
         const int y2 = Geo::kBPC == 2 ? __shfl_sync(kFullMask, desc.w, j) : 0;
-        const int it = sk & 0xffff, kvh = sk >> 16;
-        const int rows = rf & 0xff, flags = rf >> 8;
-        // the query rows' first sequence and count (grouped: the members,
-        // one row each), and the sequence whose new token a chunk carries
-        int s = it, nq = G, snew = it;
-        if constexpr (GRP) {
-            const ItemInfo ii = item_info(info, it);
-            s = ii.s0;
-            nq = ii.ns;
-            snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
-        }
-        const bool new_row = (flags & kAppendRow) != 0;
-        const int stage = i % ST;
-        const uint32_t bar = bar_a + stage * 8;
-        const uint32_t slot = wq_a + stage * Geo::kSlotBytes;
-        const bool lane_copies = p.host_inputs != 0;  // the query and new rows: the lanes' 16-byte copies
         if (lane == 0) {
+            const int it = sk & 0xffff, kvh = sk >> 16;
+            const int rows = rf & 0xff, flags = rf >> 8;
+            // the query rows' first sequence and count (grouped: the members,
+            // one row each), and the sequence whose new token a chunk carries
+            int s = it, nq = G, snew = it;
+            if constexpr (GRP) {
+                const ItemInfo ii = item_info(info, it);
+                s = ii.s0;
+                nq = ii.ns;
+                snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
+            }
+            const bool new_row = (flags & kAppendRow) != 0;
+            const int stage = i % ST;
+            const uint32_t bar = bar_a + stage * 8;
             const uint32_t kdst = wst_a + stage * Geo::kStageBytes;
             const uint32_t vdst = kdst + Geo::kTileBytes;
             // a whole chunk inside one block is one box per cache; a last chunk
@@ -1293,9 +1326,10 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
             const bool second = Geo::kBPC == 2 && rows > 8;
             wmeta[2 * stage] = make_int4(it, kvh, rows, flags);  // x: the segment's owner
             wmeta[2 * stage + 1] = make_int4(y, y2, 0, 0);
-            const uint32_t side = lane_copies ? 0u
-                                              : ((flags & kFirst) ? (GRP ? nq * D * 2 : Geo::kQBytes) : 0) +
-                                                    (new_row ? 2 * Geo::kRowBytes : 0);
+            // (with host inputs the lanes' arrivals, not bytes, cover the query and new rows)
+            const uint32_t side = HOSTIN ? 0u
+                                         : ((flags & kFirst) ? (GRP ? nq * D * 2 : Geo::kQBytes) : 0) +
+                                               (new_row ? 2 * Geo::kRowBytes : 0);
             mbar_arrive_expect_tx(bar, (short_box ? (second ? 4 : 2) * Geo::kHalves * Geo::kBoxBytes
                                                   : 2 * Geo::kTileBytes) + side);
             if (!short_box) {
@@ -1312,45 +1346,37 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
                     }
                 }
             }
-            if (!lane_copies && (flags & kFirst)) {
-                if constexpr (GRP) {
-                    for (int j = 0; j < nq; ++j)
-                        bulk_g2s(slot + j * D * 2, p.query + ((int64_t)(s + j) * p.num_heads + kvh) * D, D * 2,
-                                 bar);
-                } else {
-                    bulk_g2s(slot, p.query + ((int64_t)s * p.num_heads + kvh * G) * D, Geo::kQBytes, bar);
+            if constexpr (!HOSTIN) {
+                const uint32_t slot = wq_a + stage * Geo::kSlotBytes;
+                if (flags & kFirst) {
+                    if constexpr (GRP) {
+                        for (int j = 0; j < nq; ++j)
+                            bulk_g2s(slot + j * D * 2, p.query + ((int64_t)(s + j) * p.num_heads + kvh) * D, D * 2,
+                                     bar);
+                    } else {
+                        bulk_g2s(slot, p.query + ((int64_t)s * p.num_heads + kvh * G) * D, Geo::kQBytes, bar);
+                    }
                 }
-            }
-            if (!lane_copies && new_row) {
-                const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
-                bulk_g2s(slot + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
-                bulk_g2s(slot + Geo::kQBytes + Geo::kRowBytes, p.new_value + src, Geo::kRowBytes, bar);
+                if (new_row) {
+                    const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
+                    bulk_g2s(slot + Geo::kQBytes, p.new_key + src, Geo::kRowBytes, bar);
+                    bulk_g2s(slot + Geo::kQBytes + Geo::kRowBytes, p.new_value + src, Geo::kRowBytes, bar);
+                }
             }
         }
-        if (lane_copies) {
-            // inputs in host memory: the lanes copy them 16 bytes each, so that
-            // the link's latency is paid once per chunk, under the copies
-            // already in flight; every lane then arrives on the barrier when
-            // its copies have landed
-            constexpr int kVec = D / 8;  // 16-byte vectors per row
-            if (flags & kFirst) {
-                for (int v = lane; v < nq * kVec; v += 32) {
-                    const int r = v / kVec, c = v - r * kVec;
-                    const int64_t row = GRP ? (int64_t)(s + r) * p.num_heads + kvh
-                                            : (int64_t)s * p.num_heads + kvh * G + r;
-                    cp_async_16(slot + (r * D + c * 8) * 2, p.query + row * D + c * 8);
-                }
+        if constexpr (HOSTIN) {
+            // inputs in host memory: every lane takes part (copy_host_inputs)
+            const int it = sk & 0xffff, kvh = sk >> 16, flags = rf >> 8;
+            int s = it, nq = G, snew = it;
+            if constexpr (GRP) {
+                const ItemInfo ii = item_info(info, it);
+                s = ii.s0;
+                nq = ii.ns;
+                snew = ii.s0 + ((flags & kOwn) ? (flags >> kMemberShift) & 7 : 0);
             }
-            if (new_row) {
-                const int64_t src = ((int64_t)snew * Hkv + kvh) * D;
-                for (int v = lane; v < 2 * kVec; v += 32) {
-                    const bool is_v = v >= kVec;
-                    const int c = is_v ? v - kVec : v;
-                    cp_async_16(slot + Geo::kQBytes + (is_v ? Geo::kRowBytes : 0) + c * 16,
-                                (is_v ? p.new_value : p.new_key) + src + c * 8);
-                }
-            }
-            cp_async_mbar_arrive_noinc(bar);
+            const int stage = i % ST;
+            copy_host_inputs<D, G, GRP>(p, wq_a + stage * Geo::kSlotBytes, bar_a + stage * 8, (flags & kFirst) != 0,
+                                        (flags & kAppendRow) != 0, s, nq, snew, kvh, lane);
         }
     };
 

@@ -1,6 +1,8 @@
 // pkv_decode_inst.cuh -- instantiates the decode kernel for one (head_dim,
 // group) pair and every supported block size.  Each pkv_decode_d*_g*.cu
-// includes it once, so the 8 instantiation sets compile in parallel.
+// includes it once, so the 8 instantiation sets compile in parallel; each
+// pkv_decode_d*_*_mapped.cu (PKV_MAPPED) instantiates the same shapes with
+// host inputs (the mapped plan step) and defines only their look-up.
 #include "pkv_decode_impl.cuh"
 
 #ifndef PKV_D
@@ -13,8 +15,10 @@
 #define PKV_CATG2(a, b) a##b##_grp
 #define PKV_CATG(a, b) PKV_CATG2(a, b)
 #define PKV_INFO_FN PKV_CATG(decode_kernel_info_d, PKV_D)
+#define PKV_MAPPED_FN PKV_CATG(decode_kernel_fn_mapped_d, PKV_D)
 #else
 #define PKV_INFO_FN PKV_CAT(decode_kernel_info_d, PKV_D, PKV_G)
+#define PKV_MAPPED_FN PKV_CAT(decode_kernel_fn_mapped_d, PKV_D, PKV_G)
 #endif
 
 namespace pkv {
@@ -41,6 +45,12 @@ constexpr bool kGrouped = true;   // the grouped (prefix-sharing) kernel: 8 quer
 constexpr bool kGrouped = false;
 #endif
 
+#ifdef PKV_MAPPED
+template <int BS>
+const void *mapped_of() {
+    return reinterpret_cast<const void *>(&paged_decode_kernel<PKV_D, BS, PKV_G, kWarps, kStages, kGrouped, true>);
+}
+#else
 template <int BS>
 DecodeKernelInfo info_of() {
     using Geo = DecodeGeometry<PKV_D, BS, PKV_G>;
@@ -54,10 +64,27 @@ DecodeKernelInfo info_of() {
     i.smem_per_seq = Smem::kPerSeq;
     i.smem_per_cta = 8;
     i.smem_partials = Smem::kPartials;
+    i.fn_mapped = nullptr;  // decode_kernel_info fills it in
     return i;
 }
+#endif
 
 }  // namespace
+
+#ifdef PKV_MAPPED
+const void *PKV_MAPPED_FN(int block_size) {
+    switch (block_size) {
+#ifndef PKV_GRP
+        case 8: return mapped_of<8>();
+#endif
+        case 16: return mapped_of<16>();
+        case 32: return mapped_of<32>();
+        case 64: return mapped_of<64>();
+        case 128: return mapped_of<128>();
+        default: return nullptr;
+    }
+}
+#else
 
 bool PKV_INFO_FN(int block_size, DecodeKernelInfo *info) {
     switch (block_size) {
@@ -71,5 +98,6 @@ bool PKV_INFO_FN(int block_size, DecodeKernelInfo *info) {
         default: return false;
     }
 }
+#endif
 
 }  // namespace pkv

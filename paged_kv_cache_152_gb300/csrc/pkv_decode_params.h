@@ -50,11 +50,6 @@ struct DecodeParams {
     // 1: partials of segments cut between workers of one CTA are kept in the
     // CTA's shared memory (after the CTA bounds); 0: in ws_ml / ws_acc
     int smem_partials;
-    // 1: query, new_key and new_value may be page-locked host memory mapped
-    // for the device (a mapped plan step): the lanes copy them with 16-byte
-    // cp.async, each stage barrier counting every lane's arrival; 0: one bulk
-    // copy each, by lane 0
-    int host_inputs;
 };
 
 // Workspace carve-up (byte offsets), shared by the size query and the launch.
@@ -80,6 +75,10 @@ struct DecodeWorkspace {
 // Host-side description of one compiled decode instantiation.
 struct DecodeKernelInfo {
     const void *fn;        // __global__ function
+    // the same shape's instantiation that reads query, new_key and new_value
+    // with the lanes' 16-byte copies, so that they may be page-locked host
+    // memory (pkv_decode_plan_step_mapped); same shared memory and grid
+    const void *fn_mapped;
     int threads;           // threads per CTA
     int warps;             // workers per CTA
     int rows_per_chunk;
@@ -89,7 +88,8 @@ struct DecodeKernelInfo {
     size_t smem_partials;  // bytes of the optional shared-memory partial slots
 };
 
-// Defined in pkv_decode_d{64,128}_g{1,2,4,8}.cu; false if not compiled.
+// Defined in pkv_decode_d{64,128}_g{1,2,4,8}.cu (fn) and ..._mapped.cu
+// (fn_mapped); false if not compiled.
 bool decode_kernel_info(int head_dim, int group, int block_size, DecodeKernelInfo *info);
 // The grouped (prefix-sharing) kernel of group 1: pkv_decode_d{64,128}_grp.cu.
 bool decode_kernel_info_grouped(int head_dim, int block_size, DecodeKernelInfo *info);
