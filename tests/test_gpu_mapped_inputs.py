@@ -80,12 +80,22 @@ def _step_pair(pkv, wl, append, shared):
 @pytest.mark.parametrize("name,kw,append,shared", [
     ("7b", dict(num_seqs=11), True, False),
     ("7b", dict(num_seqs=11), False, False),
-    ("gqa", dict(num_seqs=12), True, False),
-    ("tiny", {}, True, False),
-    ("prefix", dict(num_seqs=17, prefix_len=40), True, True),
+    ("7b", dict(num_seqs=5, block_size=8), True, False),    # a chunk spans two blocks
+    ("7b", dict(num_seqs=5, block_size=128), True, False),
+    ("gqa", dict(num_seqs=12), True, False),                # group 4
+    ("gqa", dict(num_seqs=6, block_size=64), False, False),
+    ("tiny", {}, True, False),                              # head_dim 64
+    ("tiny", dict(block_size=32), False, False),
+    ("prefix", dict(num_seqs=17, prefix_len=40), True, True),   # the grouped kernel
+    ("prefix", dict(num_seqs=9, prefix_len=40, block_size=32), False, True),
+    ("forked64", {}, True, True),                           # the grouped kernel at head_dim 64
 ])
 def test_mapped_step_matches_device_inputs(pkv, name, kw, append, shared):
-    wl = W.make(name, **kw)
+    if name == "forked64":
+        from test_gpu_shared import forked_workload
+        wl = forked_workload(64, 64, 16, roots=((70, 9),), singles=2)
+    else:
+        wl = W.make(name, **kw)
     direct, mapped, plan_d, plan_h, host, dev, host_out = _step_pair(pkv, wl, append, shared)
     for _ in range(3):  # the same step again: the same bits
         plan_d.launch()
