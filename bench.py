@@ -737,6 +737,8 @@ def run_secondary(pkv, device, peak, st_main, ws_main, reps=50):
     kv = wl.kv_read_bytes()
     res = {"7b": {"decode_us_mean": round(statistics.fmean(b2b) * 1e3, 2),
                   "period_us_back_to_back": round(per_us, 2),
+                  "GB_s_back_to_back": round(kv / per_us / 1e3, 1),
+                  "frac_back_to_back": round(kv / per_us / 1e3 / peak, 4),
                   "decode_us_median_l2_flushed": round(statistics.median(fl) * 1e3, 2), "reps": reps,
                   "GB_s_l2_flushed": round(kv / statistics.median(fl) / 1e6, 1),
                   "frac_l2_flushed": round(kv / statistics.median(fl) / 1e6 / peak, 4)}}
