@@ -599,6 +599,21 @@ def time_launches(fn, reps, stream, flush=None):
     torch.cuda.synchronize()
     return [a.elapsed_time(z) for a, z in ev]
 
+# The longest context each workload's distribution allows: what a contiguous
+# KV cache must reserve per request up front (the waste comparison of
+# [P1] "The problem": max-length reservations against blocks on demand).
+MAX_CONTEXT = {"tiny": 100, "7b": 900, "chat": 2500, "gqa": 4096, "prefix": 1000}
+
+
+def waste_pct(wl, max_len):
+    """KV slots held but unused, in %: paged (the last block of each
+    sequence partly filled) and contiguous (max_len reserved per sequence)."""
+    used = sum(wl.context_lens)
+    paged = wl.block_size * sum(-(-c // wl.block_size) for c in wl.context_lens)
+    return {"paged_waste_pct": round(100 * (1 - used / paged), 2),
+            "contiguous_waste_pct": round(100 * (1 - used / (max_len * wl.num_seqs)), 2),
+            "contiguous_reservation_tokens": max_len}
+
 
 def period_launches(fn, reps, stream):
     """Mean period (ms) of `reps` calls of fn() issued back to back, CUDA
@@ -657,6 +672,7 @@ def measure_decode(pkv, name, device, peak, reps, flush, identity_tables=False, 
          "GB_s_l2_flushed": round(kv / med_us / 1e3, 1), "frac_l2_flushed": round(kv / med_us / 1e3 / peak, 4),
          "seqs_per_s": round(wl.num_seqs / mean_us * 1e6, 1),
          "traffic": None if identity_tables else recorded_traffic(name + ("_shared" if shared else ""))}
+    r.update(waste_pct(wl, MAX_CONTEXT[name]))
     if name == "prefix":
         u = unique_kv_bytes(st["tables"].cpu().numpy(), wl.context_lens, wl.block_size, wl.num_kv_heads,
                             wl.head_dim)
@@ -898,8 +914,7 @@ def run_pkv(args):
                    "num_seqs": wl.num_seqs, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
                    "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": st["nb"],
                    "sum_context": int(sum(wl.context_lens)), "kv_bytes_per_step": kv_bytes,
-                   "paged_waste_pct": round(100 * (1 - sum(wl.context_lens) / (wl.block_size * sum(
-                       -(-c // wl.block_size) for c in wl.context_lens))), 2),
+                   **waste_pct(wl, MAX_CONTEXT[args.config]),
                    "tables": "identity (contiguous, in order)" if args.identity_tables else "shuffled pool",
                    "num_ctas": args.num_ctas or pkv.decode_default_ctas(wl.num_heads, wl.num_kv_heads,
                                                                         wl.head_dim, wl.block_size),
