@@ -222,12 +222,17 @@ __device__ __forceinline__ void consume_chunk(uint32_t kt, uint32_t vt, int R, c
     // the lanes that own those heads' rows
     const float corr_e = __shfl_sync(kFullMask, corr, 8 * t);
     const float corr_o = __shfl_sync(kFullMask, corr, 8 * t + 4);
+    // Inside a piece the running max seldom moves after its first chunks:
+    // when no head's factor differs from 1 the rescale (an exact no-op) is
+    // skipped, and P.V follows the softmax at once.
+    if (__any_sync(kFullMask, corr_e != 1.f || corr_o != 1.f)) {
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-        o[i][0] *= corr_e;
-        o[i][1] *= corr_o;
-        o[i][2] *= corr_e;
-        o[i][3] *= corr_o;
+        for (int i = 0; i < D / 16; ++i) {
+            o[i][0] *= corr_e;
+            o[i][1] *= corr_o;
+            o[i][2] *= corr_e;
+            o[i][3] *= corr_o;
+        }
     }
     float pr[Geo::kNT][2];
 #pragma unroll
