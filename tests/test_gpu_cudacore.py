@@ -53,6 +53,16 @@ def _child_checks():
         case.oracle_write_new_tokens()
         err = max_abs_err(case.out, case.oracle_decode())
         assert err <= TOL, (name, err)
+    # the mapped serving step (inputs read from host memory) in this build
+    from test_gpu_mapped_inputs import _step_pair
+    direct, mapped, plan_d, plan_h, host, dev, host_out = _step_pair(pkv, W.make("7b", num_seqs=9), True, False)
+    plan_d.launch()
+    plan_h.step_mapped(dev, host)
+    torch.cuda.synchronize()
+    assert int(direct.status.item()) == 0 and int(mapped.status.item()) == 0
+    assert torch.equal(host_out.view(torch.int16), direct.out.cpu().view(torch.int16))
+    plan_d.close()
+    plan_h.close()
     print("cudacore ok")
 
 

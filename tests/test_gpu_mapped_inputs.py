@@ -53,7 +53,7 @@ def _region(tensors):
     return host, dev, views
 
 
-def _step_pair(pkv, wl, append, shared):
+def _step_pair(pkv, wl, append, shared, num_ctas=0):
     direct, mapped = Case(wl), Case(wl)
     hints = [torch.from_numpy(c.alloc.shared_prefix(wl.batch)).to("cuda") for c in (direct, mapped)] \
         if shared else [None, None]
@@ -63,7 +63,7 @@ def _step_pair(pkv, wl, append, shared):
         mapped.write_new_tokens()
     plan_d = pkv.DecodePlan(direct.out, direct.t["query"], direct.t["key_cache"], direct.t["value_cache"],
                             direct.tables, direct.lens, wl.scale, status=direct.status, shared_blocks=hints[0],
-                            **kv)
+                            num_ctas=num_ctas, **kv)
     parts = [mapped.t["query"]] + ([mapped.t["key"], mapped.t["value"]] if append else []) + \
         [mapped.tables, mapped.lens] + ([hints[1]] if shared else [])
     host, dev, views = _region(parts)
@@ -73,7 +73,7 @@ def _step_pair(pkv, wl, append, shared):
     sh = views[-1] if shared else None
     host_out = torch.full(tuple(mapped.out.shape), float("nan"), dtype=torch.float16).pin_memory()
     plan_h = pkv.DecodePlan(host_out, q, mapped.t["key_cache"], mapped.t["value_cache"], tables, lens, wl.scale,
-                            key=k, value=v, status=mapped.status, shared_blocks=sh)
+                            key=k, value=v, status=mapped.status, shared_blocks=sh, num_ctas=num_ctas)
     return direct, mapped, plan_d, plan_h, host, dev, host_out
 
 
@@ -107,6 +107,26 @@ def test_mapped_step_matches_device_inputs(pkv, name, kw, append, shared):
         assert torch.equal(mapped.t["value_cache"].view(torch.int16), direct.t["value_cache"].view(torch.int16))
     assert torch.all(dev == 0xFF)  # the device region was never written
     mapped.oracle_write_new_tokens()  # by the step itself, or by reshape_and_cache before it
+    assert max_abs_err(host_out, mapped.oracle_decode()) <= TOL
+    plan_d.close()
+    plan_h.close()
+
+
+@pytest.mark.parametrize("name,kw,shared", [("7b", dict(num_seqs=6), False), ("gqa", dict(num_seqs=5), False),
+                                            ("prefix", dict(num_seqs=12, prefix_len=300), True)])
+@pytest.mark.parametrize("num_ctas", [1, 3, 37])
+def test_mapped_step_small_grids(pkv, name, kw, shared, num_ctas):
+    """Few CTAs: segments cut between workers and CTAs, merged in shared
+    memory and device-wide, with the inputs read from host memory."""
+    wl = W.make(name, **kw)
+    direct, mapped, plan_d, plan_h, host, dev, host_out = _step_pair(pkv, wl, True, shared, num_ctas)
+    for _ in range(2):
+        plan_d.launch()
+        plan_h.step_mapped(dev, host)
+        torch.cuda.synchronize()
+        assert int(direct.status.item()) == 0 and int(mapped.status.item()) == 0
+        assert torch.equal(host_out.view(torch.int16), direct.out.cpu().view(torch.int16))
+    mapped.oracle_write_new_tokens()
     assert max_abs_err(host_out, mapped.oracle_decode()) <= TOL
     plan_d.close()
     plan_h.close()
