@@ -982,6 +982,15 @@ __global__ void __launch_bounds__(NW * 32, 1) paged_decode_kernel(const __grid_c
         prefetch_tensormap(&p.tmap_k8);
         prefetch_tensormap(&p.tmap_v8);
     }
+    if constexpr (HOSTIN) {
+        // block tables in host memory: the CTAs bring them into L2 together
+        // (one line each in turn) while the lengths load and the scan run, so
+        // that the first table reads after the scan do not cross the link
+        const int64_t lines = ((int64_t)p.num_seqs * p.max_blocks_per_seq * 4 + 127) / 128;
+        for (int64_t l = (int64_t)blockIdx.x + (int64_t)tid * gridDim.x; l < lines;
+             l += (int64_t)gridDim.x * blockDim.x)
+            prefetch_l2(reinterpret_cast<const char *>(p.block_tables) + l * 128);
+    }
     // Up to the grid-dependency wait below, the kernel reads only the context
     // lengths and the block tables (inputs of the call, never written by the
     // library's kernels): with programmatic dependent launch, the prologue,
