@@ -132,6 +132,29 @@ def test_mapped_step_small_grids(pkv, name, kw, shared, num_ctas):
     plan_h.close()
 
 
+def test_mapped_step_moves_only_the_inputs_inside_the_region(pkv):
+    """Queries and new rows in the host region, tables and lengths left in
+    device memory outside it: only the inputs inside the region are read from
+    host memory; the same bits as the direct call."""
+    wl = W.make("7b", num_seqs=7)
+    direct, mapped = Case(wl), Case(wl)
+    plan_d = pkv.DecodePlan(direct.out, direct.t["query"], direct.t["key_cache"], direct.t["value_cache"],
+                            direct.tables, direct.lens, wl.scale, key=direct.t["key"], value=direct.t["value"],
+                            status=direct.status)
+    host, dev, (q, k, v) = _region([mapped.t["query"], mapped.t["key"], mapped.t["value"]])
+    host_out = torch.full(tuple(mapped.out.shape), float("nan"), dtype=torch.float16).pin_memory()
+    plan_h = pkv.DecodePlan(host_out, q, mapped.t["key_cache"], mapped.t["value_cache"], mapped.tables, mapped.lens,
+                            wl.scale, key=k, value=v, status=mapped.status)
+    plan_d.launch()
+    plan_h.step_mapped(dev, host)
+    torch.cuda.synchronize()
+    assert int(direct.status.item()) == 0 and int(mapped.status.item()) == 0
+    assert torch.equal(host_out.view(torch.int16), direct.out.cpu().view(torch.int16))
+    assert torch.equal(mapped.t["key_cache"].view(torch.int16), direct.t["key_cache"].view(torch.int16))
+    plan_d.close()
+    plan_h.close()
+
+
 def test_mapped_step_refuses_unmapped_or_misaligned_inputs(pkv):
     """Pageable host memory and a region whose query would be misaligned are
     refused before anything is enqueued."""
