@@ -270,7 +270,8 @@ int pkv_decode_plan_step(const pkv_decode_plan_t *plan, void *dev_in, const void
  *            16-byte aligned.  The caller must not write it until the
  *            stream has passed the launch.
  * PKV_ERR_INVALID_ARG for a NULL plan, in_bytes == 0, host_in that is not
- * such memory (cudaPointerGetAttributes) or a misaligned input (nothing is
+ * such memory (cudaPointerGetAttributes), a misaligned input, or an input
+ * that starts inside the region but runs past its end (nothing is
  * enqueued); PKV_ERR_UNSUPPORTED if the library was built without the
  * kernels that read host inputs; PKV_ERR_CUDA when the launch or the copy
  * out fails to enqueue.

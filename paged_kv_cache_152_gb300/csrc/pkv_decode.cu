@@ -27,6 +27,10 @@ struct pkv_decode_plan {
     int threads = 0;
     size_t smem = 0;
     size_t out_bytes = 0;  // fp16 [num_seqs][num_heads][head_dim]
+    // bytes of each input the kernel reads (query, new key, new value, block
+    // tables, context lengths, shared-prefix hints): a mapped step checks
+    // that an input starting inside its host region also ends there
+    size_t in_extent[6] = {0, 0, 0, 0, 0, 0};
     bool empty = true;
 };
 
@@ -363,6 +367,10 @@ int build_plan(void *out, const void *query, const void *new_key, const void *ne
     p.smem_partials = r.smem_partials ? 1 : 0;
 
     plan->out_bytes = (size_t)num_seqs * num_heads * head_dim * 2;
+    plan->in_extent[0] = (size_t)num_seqs * num_heads * head_dim * 2;
+    plan->in_extent[1] = plan->in_extent[2] = (size_t)num_seqs * num_kv_heads * head_dim * 2;
+    plan->in_extent[3] = (size_t)num_seqs * max_blocks_per_seq * 4;
+    plan->in_extent[4] = plan->in_extent[5] = (size_t)num_seqs * 4;
     plan->fn = r.info.fn;
     plan->fn_mapped = r.info.fn_mapped;
     plan->ctas = r.ctas;
@@ -558,16 +566,20 @@ extern "C" int pkv_decode_plan_step_mapped(const pkv_decode_plan_t *plan, const 
     const uintptr_t lo = reinterpret_cast<uintptr_t>(dev_base), hi = lo + in_bytes;
     const intptr_t delta = reinterpret_cast<intptr_t>(attr.devicePointer) - static_cast<intptr_t>(lo);
     DecodeParams prm = plan->params;
-    auto move = [&](auto &ptr) {
+    bool inside = true;  // every moved input lies wholly inside the region
+    auto move = [&](auto &ptr, size_t extent) {
         const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
-        if (ptr && a >= lo && a < hi) ptr = reinterpret_cast<std::remove_reference_t<decltype(ptr)>>(a + delta);
+        if (!ptr || a < lo || a >= hi) return;
+        if (extent > hi - a) inside = false;
+        ptr = reinterpret_cast<std::remove_reference_t<decltype(ptr)>>(a + delta);
     };
-    move(prm.query);
-    move(prm.new_key);
-    move(prm.new_value);
-    move(prm.block_tables);
-    move(prm.context_lens);
-    move(prm.shared_blocks);
+    move(prm.query, plan->in_extent[0]);
+    move(prm.new_key, plan->in_extent[1]);
+    move(prm.new_value, plan->in_extent[2]);
+    move(prm.block_tables, plan->in_extent[3]);
+    move(prm.context_lens, plan->in_extent[4]);
+    move(prm.shared_blocks, plan->in_extent[5]);
+    if (!inside) return PKV_ERR_INVALID_ARG;
     auto aligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (!aligned(prm.query) || (prm.new_key && (!aligned(prm.new_key) || !aligned(prm.new_value))))
         return PKV_ERR_INVALID_ARG;

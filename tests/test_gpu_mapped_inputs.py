@@ -172,6 +172,11 @@ def test_mapped_step_refuses_unmapped_or_misaligned_inputs(pkv):
     rc = lib.pkv_decode_plan_step_mapped(h, ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()), 0,
                                          None, None)
     assert rc == pkv.PKV_ERR_INVALID_ARG
+    # a region that ends inside its last input (the lengths): the kernel would
+    # read past the host memory given, so the call is refused
+    rc = lib.pkv_decode_plan_step_mapped(h, ctypes.c_void_p(dev.data_ptr()), ctypes.c_void_p(host.data_ptr()),
+                                         host.numel() - 256 + 4, None, None)
+    assert rc == pkv.PKV_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert int(mapped.status.item()) == 0
     assert torch.isnan(host_out).all()  # nothing ran
